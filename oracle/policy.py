@@ -1,0 +1,302 @@
+"""Event-level simulator of the streaming policy (oracle; test infrastructure only).
+
+It computes, from integers alone, the plan (slot size S, residents R, prefetch
+depth d, ring slots Q, pool slots P) and the exact list of schedule events the
+runtime must execute. The runtime's own scheduler is separate code; tests
+compare the two event lists for equality.
+
+Sources:
+  "feat: prefetch streamed layers during compute" (sd.cpp #1905), Summary and
+  the Effective behavior table: depth 0 is synchronous streaming, depth N asks
+  for N future segments reduced to fit the budget; a positive budget is never
+  exceeded by prefetch; the active segment is never evicted; residents are a
+  maximum (auto = -1 keeps as many leading segments as the budget allows);
+  the prefetch window has priority over optional residents; shared parameters
+  are deduplicated; residents are evicted from the end of the prefix under
+  runtime memory pressure; when asynchronous transfer is unavailable or a
+  prefetch allocation fails, execution continues synchronously; max-vram 0
+  disables segmentation.
+  "feat: pool VRAM for streamed layer" (sd.cpp #1906), Summary and the pool
+  behavior table: one contiguous allocation of fixed slots sized for the
+  largest private-parameter footprint; only the peak slot count is allocated;
+  a failing pool is retried with fewer slots of the same size, down to one;
+  the one-slot pool is mandatory execution memory (attempted, with a warning,
+  even above the budget); reduced caps are remembered.
+
+Readings where the pages are silent (each one listed with its reason in the
+design notes of the repository):
+  * budgets are bytes; the budget counts parameter memory only (shared
+    region + pool slots);
+  * tensors are packed at 256-byte aligned offsets; S = max over segments of the
+    aligned sum of private tensor bytes; shared tensors count once;
+  * the prefetch window at step k is the active segment plus the next d
+    streamed (non-resident) segments; residents never consume depth; the window
+    does not cross run boundaries (no cross-forward state, maintainer review);
+  * every streamed segment is loaded through the copy queue when d >= 1,
+    including the first one of a run;
+  * shared parameters are resident (deduplicated) and loaded once in run 0,
+    followed by the resident prefix, both synchronously;
+  * load j of a run goes to ring slot R + (j mod Q) with Q = min(d + 1, N - R).
+"""
+from __future__ import annotations
+
+from dataclasses import dataclass, field
+
+# event kinds (values shared with the C ABI's ls_event_kind)
+SHARED_LOAD, LOAD_RESIDENT, LOAD_SYNC, PREFETCH, ACTIVATE, EVICT = range(6)
+KIND_NAMES = ["SHARED_LOAD", "LOAD_RESIDENT", "LOAD_SYNC", "PREFETCH", "ACTIVATE", "EVICT"]
+
+# status codes (values shared with the C ABI's ls_status)
+OK, WARN_MANDATORY_SLOT, WARN_SYNC_FALLBACK = 0, 1, 2
+ERR_INVALID_ARG, ERR_VERSION, ERR_OOM = -1, -2, -3
+
+ALIGN = 256
+
+
+def align_up(n: int, a: int = ALIGN) -> int:
+    return (n + a - 1) // a * a
+
+
+@dataclass
+class Plan:
+    N: int
+    S: int
+    shared_total: int
+    avail: int          # slots the budget (or a reduced cap) allows
+    d_req: int          # depth that fits the budget (before capping by streamed count)
+    R: int
+    Q: int
+    P: int
+    warn_mandatory: bool = False
+
+    @property
+    def M(self) -> int:
+        return self.N - self.R
+
+    @property
+    def d(self) -> int:
+        return min(self.d_req, self.M)
+
+
+def _plan_for(N: int, S: int, shared_total: int, avail: int, depth: int, resident: int,
+              mandatory: bool) -> Plan:
+    """Depth first, then the longest resident prefix that still fits ``avail`` slots."""
+    d_fit = depth if avail >= N else min(depth, avail - 1)
+    cap = N if resident < 0 else min(resident, N)
+    R = 0
+    for r in range(cap, -1, -1):
+        if min(r + d_fit + 1, N) <= avail:
+            R = r
+            break
+    M = N - R
+    Q = min(d_fit + 1, M) if M > 0 else 0
+    return Plan(N, S, shared_total, avail, d_fit, R, Q, R + Q, mandatory)
+
+
+def plan_slots(seg_slot_bytes: list, shared_bytes: list, depth: int, resident: int,
+               max_vram: int, slot_cap: int | None = None) -> Plan:
+    """Plan from the budget. ``slot_cap`` is a remembered reduced slot count."""
+    N = len(seg_slot_bytes)
+    S = max(seg_slot_bytes)
+    shared_total = sum(align_up(b) for b in shared_bytes)
+    if max_vram == 0 and slot_cap is None:
+        return Plan(N, S, shared_total, N, 0, N, 0, N)
+    if max_vram == 0:
+        avail, mandatory = N, False
+    else:
+        avail = (max_vram - shared_total) // S if max_vram > shared_total else 0
+        mandatory = avail < 1
+        if mandatory:
+            # below one slot: only the mandatory execution slot, no residency, no prefetch
+            return Plan(N, S, shared_total, 1, 0, 0, 1, 1, True)
+    if slot_cap is not None:
+        avail = min(avail, slot_cap)
+    return _plan_for(N, S, shared_total, avail, depth, resident, mandatory)
+
+
+@dataclass
+class Stats:
+    prefetch_queued: int = 0
+    prefetch_activated: int = 0
+    sync_loads: int = 0
+    resident_loads: int = 0
+    shared_loads: int = 0
+    evictions: int = 0
+    sync_fallbacks: int = 0
+    pool_degradations: int = 0
+    bytes_loaded: int = 0
+
+
+@dataclass
+class Sim:
+    """Streaming context state mirrored by the simulator."""
+    seg_slot_bytes: list
+    shared: list                        # [(shared_id, bytes)], distinct ids
+    depth: int
+    resident: int
+    max_vram: int
+    use_pool: int
+    alloc_cap: int | None = None        # parameter allocator refuses beyond this many live bytes
+    fail_async: bool = False            # the first prefetch finds async transfer unavailable
+    plan: Plan | None = None
+    status: int = OK
+    R: int = 0
+    d: int = 0
+    run: int = 0
+    async_ok: bool = True
+    live: int = 0
+    cur_R: int = 0
+    events: list = field(default_factory=list)
+    stats: Stats = field(default_factory=Stats)
+    warnings: set = field(default_factory=set)
+
+    # -------------------------------------------------------------- register
+    def register(self) -> int:
+        """Plan and allocate the shared region and (pool on) the slot pool."""
+        shared_b = [b for _, b in self.shared]
+        p = plan_slots(self.seg_slot_bytes, shared_b, self.depth, self.resident, self.max_vram)
+        if p.warn_mandatory:
+            self.warnings.add(WARN_MANDATORY_SLOT)
+        if not self._alloc(p.shared_total):
+            self.status = ERR_OOM
+            return ERR_OOM
+        if self.use_pool:
+            chosen = None
+            for cap in range(p.P, 0, -1):
+                q = p if cap == p.P else plan_slots(self.seg_slot_bytes, shared_b, self.depth,
+                                                    self.resident, self.max_vram, slot_cap=cap)
+                q.warn_mandatory = p.warn_mandatory
+                if self._alloc(q.P * q.S):
+                    chosen = q
+                    break
+                self.stats.pool_degradations += 1
+            if chosen is None:
+                self._free(p.shared_total)
+                self.status = ERR_OOM
+                return ERR_OOM
+            p = chosen
+        self.plan = p
+        self.R = p.R
+        self.d = p.d_req
+        self.status = WARN_MANDATORY_SLOT if p.warn_mandatory else OK
+        return self.status
+
+    def _alloc(self, nbytes: int) -> bool:
+        if nbytes == 0:
+            return True
+        if self.alloc_cap is not None and self.live + nbytes > self.alloc_cap:
+            return False
+        self.live += nbytes
+        return True
+
+    def _free(self, nbytes: int) -> None:
+        self.live -= nbytes
+
+    def _emit(self, step, kind, seg, slot, nbytes):
+        self.events.append((self.run, step, kind, seg, slot, nbytes))
+
+    # -------------------------------------------------------------- run
+    def run_once(self, load_bytes=None) -> int:
+        """One pass over all segments; returns the run's status.
+
+        ``load_bytes(seg)`` gives the bytes a load of ``seg`` moves in this run
+        (default: its aligned private footprint)."""
+        assert self.plan is not None
+        N = self.plan.N
+        lb = load_bytes or (lambda s: self.seg_slot_bytes[s])
+        sz = self.seg_slot_bytes
+        pool = bool(self.use_pool)
+        fell_back = False
+        ret = OK
+        if self.run == 0:
+            for sid, b in sorted(self.shared):
+                self._emit(-1, SHARED_LOAD, sid, -1, b)
+                self.stats.shared_loads += 1
+                self.stats.bytes_loaded += b
+            for i in range(self.R):
+                if not pool and not self._alloc(sz[i]):
+                    self.R = i          # the prefix ends where memory ran out
+                    break
+                self._emit(-1, LOAD_RESIDENT, i, i, lb(i))
+                self.stats.resident_loads += 1
+                self.stats.bytes_loaded += lb(i)
+        R = self.R                      # this run's resident prefix and ring
+        M = N - R
+        Q = min(self.d + 1, M) if M > 0 else 0
+        d = min(self.d, M)
+        self.cur_R = R
+        next_load = 0
+        prefetched = set()
+        for k in range(N):
+            streamed_upto = max(0, k - R + 1)       # streamed segments with index <= k
+            if d >= 1 and self.async_ok:
+                while next_load < M and next_load < streamed_upto + d:
+                    seg = R + next_load
+                    if self.fail_async or (not pool and not self._alloc_evicting(sz[seg], k)):
+                        self._fallback()
+                        fell_back = True
+                        d = 0
+                        break
+                    self._emit(k, PREFETCH, seg, R + next_load % Q, lb(seg))
+                    self.stats.prefetch_queued += 1
+                    self.stats.bytes_loaded += lb(seg)
+                    prefetched.add(seg)
+                    next_load += 1
+            if k >= R and k not in prefetched:
+                if not pool and not self._alloc_evicting(sz[k], k):
+                    ret = ERR_OOM
+                    break
+                self._emit(k, LOAD_SYNC, k, R + (k - R) % Q, lb(k))
+                self.stats.sync_loads += 1
+                self.stats.bytes_loaded += lb(k)
+                next_load = k - R + 1
+            self._emit(k, ACTIVATE, k, k if k < R else R + (k - R) % Q, 0)
+            if k in prefetched:
+                self.stats.prefetch_activated += 1
+            if not pool and k >= R:
+                self._free(sz[k])
+        self.R = self.cur_R
+        self.run += 1
+        if ret != OK:
+            return ret
+        return WARN_SYNC_FALLBACK if fell_back else OK
+
+    def _fallback(self) -> None:
+        """Asynchronous transfer unavailable or a prefetch allocation failed:
+        continue synchronously, and remember it."""
+        self.async_ok = False
+        self.d = 0
+        self.fail_async = False
+        self.stats.sync_fallbacks += 1
+        self.warnings.add(WARN_SYNC_FALLBACK)
+
+    def _alloc_evicting(self, nbytes: int, k: int) -> bool:
+        """Allocate for a load issued at step k. Under memory pressure, evict
+        residents from the end of the prefix, but only ones already computed in
+        this run (index < k): the active segment is never evicted."""
+        while not self._alloc(nbytes):
+            r = self.cur_R - 1
+            if r < 0 or r >= k:
+                return False
+            self._emit(k, EVICT, r, r, 0)
+            self.stats.evictions += 1
+            self._free(self.seg_slot_bytes[r])
+            self.cur_R = r
+        return True
+
+
+def simulate(seg_slot_bytes, shared=(), depth=0, resident=-1, max_vram=0, use_pool=1, runs=1,
+             alloc_cap=None, fail_async=False, load_bytes=None):
+    """Register then run ``runs`` passes. Returns (sim, [status per run]).
+
+    ``load_bytes`` is None or a list (per run) of per-segment byte counts."""
+    sim = Sim(list(seg_slot_bytes), list(shared), depth, resident, max_vram, use_pool,
+              alloc_cap=alloc_cap, fail_async=fail_async)
+    st = sim.register()
+    if st < 0:
+        return sim, [st]
+    out = []
+    for r in range(runs):
+        lb = None if load_bytes is None else (lambda s, r=r: load_bytes[r][s])
+        out.append(sim.run_once(lb))
+    return sim, out
