@@ -1,0 +1,363 @@
+#!/usr/bin/env python
+"""Layer-streamed execution benchmark (one JSON line on stdout, rank 0).
+
+Workload (default): the 12-segment DiT-style FFN stack — each segment a bf16
+linear 1024->4096 + GELU + linear 4096->1024 + residual (16.8 MB of parameters),
+4096 tokens — with its parameters in pinned host memory, prefetch depth 1, no
+residents, a two-slot pool. One step = one streamed pass over all 12 segments
+(every segment's parameters cross the host link again). Inputs are synthetic
+(seeded N(0,1) activations, N(0, 1/sqrt(fan_in)) weights).
+
+  python bench.py [--gpus N] [--steps K] [--warmup W] [--impl ours|reference]
+
+N > 1 runs N independent replicas (one process per GPU under torchrun): the
+path has no exchange step, so the ranks share nothing but the barrier and the
+max-over-ranks timing. --impl reference times the CPU fp64 oracle instead.
+"""
+from __future__ import annotations
+
+import argparse
+import json
+import os
+import statistics
+import subprocess
+import sys
+import tempfile
+import time
+
+import numpy as np
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+sys.path.insert(0, ROOT)
+
+import synth  # noqa: E402
+
+METRIC = "streamed tokens/s; overlap eff. vs max(H2D,compute); host-link GB/s"
+UNIT = "tokens/s"
+FALLBACK_HBM_GBS, FALLBACK_BF16_TFLOPS = 6800.0, 1900.0
+L2_FLUSH_BYTES = 256 << 20
+
+
+def seg_flops(cfg, tokens) -> float:
+    """Multiply-add FLOPs of one segment (the GEMMs)."""
+    T, H, F = tokens, cfg.hidden, cfg.ffn
+    if cfg.kind == synth.KIND_LINEAR_GELU_F32:
+        return 2.0 * T * H * F
+    if cfg.kind == synth.KIND_FFN_GELU_BF16:
+        return 4.0 * T * H * F
+    if cfg.kind == synth.KIND_FFN_GELU_SHARED_BF16:
+        return 4.0 * T * H * F + 2.0 * T * H * H
+    if cfg.kind == synth.KIND_SWIGLU_BF16:
+        return 6.0 * T * H * F
+    return 6.0 * T * cfg.top_k * H * F
+
+
+def kernel_flops(cfg, tokens) -> dict:
+    T, H, F = tokens, cfg.hidden, cfg.ffn
+    if cfg.kind == synth.KIND_SWIGLU_BF16:
+        return {"gemm_up": 4.0 * T * H * F, "gemm_down": 2.0 * T * H * F}
+    if cfg.kind == synth.KIND_MOE_SWIGLU_BF16:
+        return {"gemm_up": 4.0 * T * cfg.top_k * H * F, "gemm_down": 2.0 * T * cfg.top_k * H * F}
+    return {"gemm_up": 2.0 * T * H * F, "gemm_down": 2.0 * T * H * F, "gemm_proj": 2.0 * T * H * H}
+
+
+def measured_peaks() -> tuple:
+    path = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    try:
+        with open(path) as f:
+            d = json.load(f)
+        return float(d["hbm_gbs"]), float(d["bf16_tflops"]), float(d.get("bf16_tflops_sustained", 0)) or None, "measured"
+    except Exception:
+        return FALLBACK_HBM_GBS, FALLBACK_BF16_TFLOPS, None, "fallback"
+
+
+# ---------------------------------------------------------------- clocks
+class ClockSampler:
+    FIELDS = ("index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
+              "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
+              "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
+
+    def __init__(self, gpu_id: str):
+        self.path = tempfile.mktemp(suffix=".csv")
+        self.f = open(self.path, "w")
+        try:
+            self.p = subprocess.Popen(["nvidia-smi", "-i", gpu_id, f"--query-gpu={self.FIELDS}",
+                                       "--format=csv,noheader,nounits", "-lms", "200"],
+                                      stdout=self.f, stderr=subprocess.DEVNULL)
+        except FileNotFoundError:
+            self.p = None
+
+    def stop(self) -> dict:
+        if self.p is not None:
+            self.p.terminate()
+            try:
+                self.p.wait(timeout=5)
+            except subprocess.TimeoutExpired:
+                self.p.kill()
+        self.f.close()
+        sm, mx, reasons = [], [], set()
+        names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
+        for line in open(self.path):
+            parts = [p.strip() for p in line.split(",")]
+            if len(parts) < 9:
+                continue
+            try:
+                sm.append(float(parts[1]))
+                mx.append(float(parts[2]))
+            except ValueError:
+                continue
+            for n, v in zip(names, parts[5:9]):
+                if v.lower() == "active":
+                    reasons.add(n)
+        os.remove(self.path)
+        return {"sm_mhz": statistics.median(sm) if sm else None, "sm_max_mhz": max(mx) if mx else None,
+                "reasons": sorted(reasons), "samples": len(sm)}
+
+
+# ---------------------------------------------------------------- distributed glue
+def dist_env():
+    world = int(os.environ.get("WORLD_SIZE", "1"))
+    rank = int(os.environ.get("RANK", "0"))
+    local = int(os.environ.get("LOCAL_RANK", "0"))
+    return world, rank, local
+
+
+def aggregate(step_seconds: float, units: float, world: int, device=None) -> tuple:
+    """(max step time over ranks, total units over ranks): whole-job throughput
+    is total units / max time. Works on gloo (CPU) and nccl."""
+    if world == 1:
+        return step_seconds, units
+    import torch
+    import torch.distributed as dist
+    t = torch.tensor([step_seconds], dtype=torch.float64, device=device)
+    u = torch.tensor([units], dtype=torch.float64, device=device)
+    dist.all_reduce(t, op=dist.ReduceOp.MAX)
+    dist.all_reduce(u, op=dist.ReduceOp.SUM)
+    return float(t.item()), float(u.item())
+
+
+# ---------------------------------------------------------------- oracle (CPU) timing
+def oracle_time(cfg, tokens: int, reps: int = 1) -> tuple:
+    """fp64 oracle forward of `tokens` rows through every segment; weights are
+    drawn and widened beforehand (generation excluded). Returns (seconds per
+    pass, cores used)."""
+    from oracle import stack as ostack
+    from oracle import forward as F
+    cores = len(os.sched_getaffinity(0))
+    rows = np.arange(tokens)
+    x0 = F.as_f64(synth.draw_x(cfg, tokens), cfg.dtype)
+    shared = ostack.shared_f64(cfg)[0] if cfg.kind == synth.KIND_FFN_GELU_SHARED_BF16 else None
+    segs = [ostack.segment_f64(cfg, s) for s in range(cfg.n_segments)] \
+        if cfg.kind != synth.KIND_MOE_SWIGLU_BF16 else [None] * cfg.n_segments
+    times = []
+    for _ in range(reps):
+        t0 = time.perf_counter()
+        x = x0
+        for s in range(cfg.n_segments):
+            x = ostack.apply_segment(cfg, s, x, rows=rows, tensors=segs[s], shared=shared)
+        times.append(time.perf_counter() - t0)
+    return min(times), cores
+
+
+def run_reference(args, cfg, world, rank):
+    if rank != 0:
+        return 0
+    tokens = args.ref_tokens
+    for _ in range(args.warmup):
+        oracle_time(cfg, tokens)
+    secs = [oracle_time(cfg, tokens)[0] for _ in range(args.steps)]
+    cores = len(os.sched_getaffinity(0))
+    mean = statistics.mean(secs)
+    value = tokens / mean
+    sample = f"{tokens} of {cfg.tokens} tokens through all {cfg.n_segments} segments per step (rows are independent)"
+    line = {"impl": "reference", "metric": METRIC, "value": value, "unit": UNIT, "n_gpus": args.gpus,
+            "steps": args.steps, "warmup": args.warmup, "ms_per_step": mean * 1e3, "higher_is_better": True,
+            "scaling": "weak", "vs_baseline": None, "dtype": "f64", "data": "synthetic",
+            "config": {"workload": cfg.name, "tokens": cfg.tokens, "segments": cfg.n_segments},
+            "cpu_baseline": {"value": value, "unit": UNIT, "cores": cores, "kind": "oracle", "sample": sample},
+            "e2e": {"value": value, "unit": UNIT, "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0}}
+    print(json.dumps(line), flush=True)
+    return 0
+
+
+# ---------------------------------------------------------------- GPU arm
+def ce_link_peak(torch, nbytes=1 << 30, reps=10) -> float:
+    """Pinned host -> device copy-engine bandwidth (best of reps), GB/s."""
+    h = torch.empty(nbytes, dtype=torch.uint8).pin_memory()
+    h.fill_(1)
+    d = torch.empty(nbytes, dtype=torch.uint8, device="cuda")
+    s = torch.cuda.Stream()
+    best = 1e30
+    for _ in range(reps):
+        e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        with torch.cuda.stream(s):
+            e0.record()
+            d.copy_(h, non_blocking=True)
+            e1.record()
+        e1.synchronize()
+        best = min(best, e0.elapsed_time(e1))
+    del h, d
+    return nbytes / (best * 1e-3) / 1e9
+
+
+def run_ours(args, cfg, world, rank, local):
+    import torch
+    from host_offloaded_weight_gb300 import lstream as L
+
+    torch.cuda.set_device(local)
+    dev = torch.device("cuda", local)
+    if world > 1:
+        import torch.distributed as dist
+        dist.init_process_group("nccl", device_id=dev)
+    hbm_peak, tc_peak, tc_sustained, peak_src = measured_peaks()
+    link_peak = ce_link_peak(torch)
+    hs = synth.HostStack(cfg)
+    p = L.ls_params_init(prefetch_depth=cfg.prefetch_depth, resident_layers=cfg.resident_layers,
+                         max_vram_bytes=cfg.max_vram_bytes, use_pool=cfg.use_pool,
+                         copy_path={"auto": 0, "kernel": 1, "engine": 2}[args.copy_path],
+                         copy_ctas=args.copy_ctas, reserve_sms=args.reserve_sms, kernel_timing=1)
+    ctx = L.ls_ctx_create(p)
+    L.ls_register_segments(ctx, hs.segments, hs.shared_map)
+    T = cfg.tokens
+    xb = synth.draw_x(cfg)
+    x = torch.from_numpy(xb.view(np.int16)).view(torch.bfloat16).to(dev) if cfg.dtype == "bf16" \
+        else torch.from_numpy(xb).to(dev)
+    y = torch.empty_like(x)
+    logits = None
+    if cfg.kind == synth.KIND_MOE_SWIGLU_BF16:
+        logits = torch.from_numpy(np.stack([synth.draw_logits(cfg, l) for l in range(cfg.n_segments)])).to(dev)
+    s = torch.cuda.current_stream()
+    flush = torch.empty(L2_FLUSH_BYTES, dtype=torch.uint8, device=dev)
+    for _ in range(args.warmup):
+        L.ls_run(ctx, x, y, T, s, logits=logits, top_k=cfg.top_k)
+    n_ev0 = len(L.ls_get_schedule(ctx))
+    L.ls_get_kernel_times(ctx, reset=True)
+    ev = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)) for _ in range(args.steps)]
+    if world > 1:
+        torch.distributed.barrier()
+    torch.cuda.synchronize()
+    gpu_id = "GPU-" + str(torch.cuda.get_device_properties(local).uuid)
+    sampler = ClockSampler(gpu_id)
+    time.sleep(0.3)
+    for i in range(args.steps):
+        flush.zero_()                    # write 256 MB (> 129 MB L2) between timed passes
+        ev[i][0].record(s)
+        L.ls_run_async(ctx, x, y, T, s, logits=logits, top_k=cfg.top_k)
+        ev[i][1].record(s)
+    L.ls_sync(ctx)
+    torch.cuda.synchronize()
+    if world > 1:
+        torch.distributed.barrier()
+    clocks = sampler.stop()
+    step_ms = [a.elapsed_time(b) for a, b in ev]
+    mean_s = statistics.mean(step_ms) / 1e3
+    ktimes = L.ls_get_kernel_times(ctx, reset=True)
+    sched = L.ls_get_schedule(ctx)[n_ev0:]
+    stats = L.ls_get_stats(ctx)
+    link_bytes = sum(e[5] for e in sched if e[2] in (L.LS_EV_PREFETCH, L.LS_EV_LOAD_SYNC)) / args.steps
+    flops = seg_flops(cfg, T) * cfg.n_segments
+    max_s, total_tokens = aggregate(mean_s, float(T), world, dev if world > 1 else None)
+    value = total_tokens / max_s
+    # --- end to end through the host-buffer entry point (copies in the timed region)
+    xh = x.cpu().pin_memory()
+    yh = torch.empty_like(xh).pin_memory()
+    lh = logits.cpu().pin_memory() if logits is not None else None
+    for _ in range(2):
+        L.ls_run_host(ctx, xh, yh, T, lh, cfg.top_k)
+    if world > 1:
+        torch.distributed.barrier()
+    t0 = time.perf_counter()
+    for _ in range(args.steps):
+        L.ls_run_host(ctx, xh, yh, T, lh, cfg.top_k)
+    e2e_s = (time.perf_counter() - t0) / args.steps
+    e2e_max, e2e_tokens = aggregate(e2e_s, float(T), world, dev if world > 1 else None)
+    h2d = xh.numel() * xh.element_size() + (lh.numel() * 4 if lh is not None else 0)
+    d2h = yh.numel() * yh.element_size()
+    L.ls_get_kernel_times(ctx, reset=True)
+    # --- kernels: live averages over the timed region
+    kt = {k: {"launches": n, "avg_ms": ms / max(n, 1), "total_ms": ms} for k, (n, ms) in ktimes.items()}
+    launches = sum(v["launches"] for k, v in kt.items() if k != "copy_engine")
+    if "copy_engine" in kt:
+        launches += kt["copy_engine"]["launches"]  # one publish kernel per copy-engine load
+    dominant = max(kt, key=lambda k: kt[k]["total_ms"]) if kt else None
+    kf = kernel_flops(cfg, T)
+    per_load = link_bytes / max(1, sum(1 for e in sched if e[2] in (L.LS_EV_PREFETCH, L.LS_EV_LOAD_SYNC)) / args.steps)
+    def roof(name):
+        if name in ("copy_h2slot", "copy_engine"):
+            ach = per_load / (kt[name]["avg_ms"] * 1e-3) / 1e9
+            return {"kernel": name, "bound": "host_link", "achieved": ach, "peak": link_peak, "unit": "GB/s",
+                    "frac": ach / link_peak, "traffic": TRAFFIC.get((cfg.name, name)),
+                    "peak_source": "pinned copy-engine H2D, 1 GiB, best of 10, measured in this run"}
+        if name in kf:
+            ach = kf[name] / (kt[name]["avg_ms"] * 1e-3) / 1e12
+            return {"kernel": name, "bound": "tensor", "achieved": ach, "peak": tc_peak, "unit": "TFLOP/s",
+                    "frac": ach / tc_peak, "traffic": TRAFFIC.get((cfg.name, name)),
+                    "peak_source": f"bf16_tflops ({peak_src})"}
+        return None
+    roofline = roof(dominant) if dominant else None
+    gemm_name = "gemm_down" if "gemm_down" in kt else None
+    line = {
+        "metric": METRIC, "value": value, "unit": UNIT, "n_gpus": world, "steps": args.steps,
+        "warmup": args.warmup, "ms_per_step": max_s * 1e3, "higher_is_better": True, "scaling": "weak",
+        "vs_baseline": None, "dtype": "bf16" if cfg.dtype == "bf16" else "f32", "data": "synthetic",
+        "config": {"workload": cfg.name, "tokens": T, "segments": cfg.n_segments, "hidden": cfg.hidden,
+                   "ffn": cfg.ffn, "prefetch_depth": cfg.prefetch_depth, "resident_layers": cfg.resident_layers,
+                   "max_vram_bytes": cfg.max_vram_bytes, "pool": cfg.use_pool,
+                   "copy_path": ["auto", "kernel", "engine"][stats["copy_path"]],
+                   "parallelism": f"replicas{world}" if world > 1 else "single",
+                   "l2": "flushed between timed passes (256 MB write)"},
+        "overlap_eff": max(link_bytes / (link_peak * 1e9), flops / (tc_peak * 1e12)) / mean_s,
+        "link_gbs": link_bytes / mean_s / 1e9, "link_peak_gbs": link_peak,
+        "link_frac": link_bytes / mean_s / 1e9 / link_peak,
+        "bytes_per_step": link_bytes, "flops_per_step": flops,
+        "roofline": roofline,
+        "roofline_gemm": roof(gemm_name) if gemm_name else None,
+        "kernels": kt,
+        "gpu_launches": launches,
+        "clocks": {k: clocks[k] for k in ("sm_mhz", "sm_max_mhz", "reasons")},
+        "e2e": {"value": e2e_tokens / e2e_max, "unit": UNIT, "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h},
+        "copy_paths_gbs": {"kernel": stats["copy_kernel_gbs"], "engine": stats["copy_engine_gbs"]},
+    }
+    L.ls_ctx_destroy(ctx)
+    del hs
+    if rank == 0 and not args.no_cpu_baseline:
+        secs, cores = oracle_time(cfg, args.cpu_tokens)
+        line["cpu_baseline"] = {"value": args.cpu_tokens / secs, "unit": UNIT, "cores": cores, "kind": "oracle",
+                                "sample": f"{args.cpu_tokens} of {T} tokens through all {cfg.n_segments} segments, "
+                                          "fp64, weights widened beforehand"}
+    if rank == 0:
+        print(json.dumps(line), flush=True)
+    if world > 1:
+        torch.distributed.destroy_process_group()
+    return 0
+
+
+# DRAM bytes per launch from ncu captures of the current kernels (None = not captured).
+TRAFFIC: dict = {}
+
+
+def main() -> int:
+    ap = argparse.ArgumentParser(description=__doc__, formatter_class=argparse.RawDescriptionHelpFormatter)
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=20)
+    ap.add_argument("--warmup", type=int, default=3)
+    ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
+    ap.add_argument("--workload", default=synth.DIT.name, choices=sorted(synth.STACKS))
+    ap.add_argument("--copy-path", default="auto", choices=["auto", "kernel", "engine"])
+    ap.add_argument("--copy-ctas", type=int, default=0)
+    ap.add_argument("--reserve-sms", type=int, default=-1)
+    ap.add_argument("--cpu-tokens", type=int, default=1024)
+    ap.add_argument("--ref-tokens", type=int, default=256)
+    ap.add_argument("--no-cpu-baseline", action="store_true")
+    args = ap.parse_args()
+    if args.warmup < 3:
+        ap.error("--warmup must be at least 3")
+    world, rank, local = dist_env()
+    cfg = synth.STACKS[args.workload]
+    if args.impl == "reference":
+        return run_reference(args, cfg, world, rank)
+    return run_ours(args, cfg, world, rank, local)
+
+
+if __name__ == "__main__":
+    sys.exit(main())

@@ -1,0 +1,663 @@
+// bf16 GEMM on the sm_103a tensor cores: C[M,N] = A[M,K] * B[N,K]^T, fp32
+// accumulation in tensor memory, with the segment's elementwise work fused into
+// the epilogue (bias, GELU, residual add, SiLU-gated product, routing weight).
+//
+// Structure (one persistent CTA per SM, 192 threads):
+//   warp 0     TMA producer: 128x64 A tile and 256x64 B tile (or two 128x64 B
+//              tiles for the gate/up pair) per stage, 128-byte swizzle, into a
+//              4-stage shared-memory ring guarded by full/empty mbarriers.
+//   warp 1     allocates 512 TMEM columns (two 128x256 fp32 accumulators) and
+//              issues tcgen05.mma (M=128, K=16 per instruction) from one thread;
+//              tcgen05.commit releases smem stages and hands finished
+//              accumulators to the epilogue.
+//   warps 2-5  epilogue: tcgen05.ld of their 32 TMEM lanes (one output row per
+//              thread), fused elementwise work, 16-byte stores. The second
+//              accumulator lets the next tile's mainloop run meanwhile.
+// Tiles are visited in a fixed order and each output element is produced by
+// one thread from one fixed-order accumulation, so results do not depend on
+// the grid size or on where the weights live.
+//
+// Grouped mode (expert GEMM of the MoE stack): rows of A are already sorted by
+// expert; group g owns rows [group_bounds[g], group_bounds[g+1]) and reads its
+// own B matrix at row b_base_row + g * b_group_stride_rows of the B view.
+//
+// Every mbarrier wait is bounded in time; on expiry the CTA records an error
+// word, stops issuing work, waits (bounded) for its own copies and MMAs, frees
+// its TMEM and exits.
+#include <cuda.h>
+
+#include "common.cuh"
+#include "kernels.h"
+
+#include <mutex>
+#include <unordered_map>
+
+namespace ls {
+namespace {
+
+constexpr int BM = 128;
+constexpr int BK = 64;
+constexpr int ACC_COLS = 256;
+constexpr int STAGES = 4;
+constexpr int A_BYTES = BM * BK * 2;
+constexpr int B_BYTES = ACC_COLS * BK * 2;
+constexpr int STAGE_BYTES = A_BYTES + B_BYTES;
+constexpr int NUM_THREADS = 192;
+constexpr int SMEM_BYTES = STAGES * STAGE_BYTES + 1024 + 256;
+constexpr uint64_t MBAR_LIMIT_NS = 2000000000ull;  // 2 s beyond any ready-word wait: far above a legitimate stall
+constexpr int MAX_GROUPS = 256;
+
+struct GemmParams {
+    CUtensorMap tmA;
+    CUtensorMap tmB;
+    int M, N, K;
+    int num_m_tiles, num_n_tiles, num_k_blocks, num_tiles;
+    int b2_row_off;
+    const __nv_bfloat16* bias;
+    const __nv_bfloat16* resid;
+    int64_t ldr;
+    void* C;
+    int64_t ldc;
+    const int* group_bounds;
+    int n_groups;
+    int b_group_stride_rows;
+    int b_base_row;
+    const int* row_table;
+    const float* row_weight;
+    const uint32_t* ready;
+    uint32_t epoch;
+    uint64_t wait_ns;
+    uint32_t* err;
+    uint32_t wait_code;
+    uint64_t mbar_limit_ns;  // bound of every internal mbarrier wait
+};
+
+// ------------------------------------------------------------------ PTX helpers
+__device__ __forceinline__ uint32_t smem_u32(const void* p) {
+    return (uint32_t)__cvta_generic_to_shared(p);
+}
+__device__ __forceinline__ void mbar_init(uint32_t bar, uint32_t count) {
+    asm volatile("mbarrier.init.shared::cta.b64 [%0], %1;" ::"r"(bar), "r"(count) : "memory");
+}
+__device__ __forceinline__ void mbar_expect_tx(uint32_t bar, uint32_t bytes) {
+    asm volatile("mbarrier.arrive.expect_tx.shared::cta.b64 _, [%0], %1;" ::"r"(bar), "r"(bytes)
+                 : "memory");
+}
+__device__ __forceinline__ void mbar_arrive(uint32_t bar) {
+    asm volatile("mbarrier.arrive.shared::cta.b64 _, [%0];" ::"r"(bar) : "memory");
+}
+__device__ __forceinline__ bool mbar_try_wait(uint32_t bar, uint32_t parity) {
+    uint32_t ok;
+    asm volatile(
+        "{\n\t.reg .pred p;\n\t"
+        "mbarrier.try_wait.parity.shared::cta.b64 p, [%1], %2;\n\t"
+        "selp.u32 %0, 1, 0, p;\n\t}"
+        : "=r"(ok)
+        : "r"(bar), "r"(parity)
+        : "memory");
+    return ok != 0;
+}
+// Bounded wait; false (with the error word set) if the phase did not complete in time.
+__device__ __noinline__ bool mbar_wait(uint32_t bar, uint32_t parity, uint32_t* err, uint32_t role,
+                                       uint64_t limit_ns) {
+    if (mbar_try_wait(bar, parity)) return true;
+    const uint64_t t0 = globaltimer_ns();
+    while (!mbar_try_wait(bar, parity)) {
+        if (globaltimer_ns() - t0 > limit_ns) {
+            raise_error(err, DERR_GEMM_TIMEOUT | (role << 8));
+            return false;
+        }
+    }
+    return true;
+}
+__device__ __forceinline__ void tma_load_2d(uint32_t dst, const CUtensorMap* map, uint32_t bar,
+                                            int c0, int c1) {
+    asm volatile(
+        "cp.async.bulk.tensor.2d.shared::cluster.global.tile.mbarrier::complete_tx::bytes"
+        " [%0], [%1, {%2, %3}], [%4];" ::"r"(dst),
+        "l"(reinterpret_cast<uint64_t>(map)), "r"(c0), "r"(c1), "r"(bar)
+        : "memory");
+}
+__device__ __forceinline__ void tma_prefetch_desc(const CUtensorMap* map) {
+    asm volatile("prefetch.tensormap [%0];" ::"l"(reinterpret_cast<uint64_t>(map)) : "memory");
+}
+__device__ __forceinline__ void tc_fence_before() {
+    asm volatile("tcgen05.fence::before_thread_sync;" ::: "memory");
+}
+__device__ __forceinline__ void tc_fence_after() {
+    asm volatile("tcgen05.fence::after_thread_sync;" ::: "memory");
+}
+__device__ __forceinline__ void tmem_alloc(uint32_t dst_smem, uint32_t ncols) {
+    asm volatile("tcgen05.alloc.cta_group::1.sync.aligned.shared::cta.b32 [%0], %1;" ::"r"(dst_smem),
+                 "r"(ncols)
+                 : "memory");
+}
+__device__ __forceinline__ void tmem_relinquish() {
+    asm volatile("tcgen05.relinquish_alloc_permit.cta_group::1.sync.aligned;" ::: "memory");
+}
+__device__ __forceinline__ void tmem_dealloc(uint32_t taddr, uint32_t ncols) {
+    asm volatile("tcgen05.dealloc.cta_group::1.sync.aligned.b32 %0, %1;" ::"r"(taddr), "r"(ncols)
+                 : "memory");
+}
+__device__ __forceinline__ void umma_bf16(uint32_t d_tmem, uint64_t a_desc, uint64_t b_desc,
+                                          uint32_t idesc, uint32_t accumulate) {
+    asm volatile(
+        "{\n\t.reg .pred p;\n\t"
+        "setp.ne.b32 p, %4, 0;\n\t"
+        "tcgen05.mma.cta_group::1.kind::f16 [%0], %1, %2, %3, p;\n\t}" ::"r"(d_tmem),
+        "l"(a_desc), "l"(b_desc), "r"(idesc), "r"(accumulate)
+        : "memory");
+}
+__device__ __forceinline__ void umma_commit(uint32_t bar) {
+    asm volatile(
+        "tcgen05.commit.cta_group::1.mbarrier::arrive::one.shared::cluster.b64 [%0];" ::"r"(bar)
+        : "memory");
+}
+__device__ __forceinline__ void tmem_ld32(uint32_t taddr, uint32_t (&r)[32]) {
+    asm volatile(
+        "tcgen05.ld.sync.aligned.32x32b.x32.b32 "
+        "{%0,%1,%2,%3,%4,%5,%6,%7,%8,%9,%10,%11,%12,%13,%14,%15,"
+        "%16,%17,%18,%19,%20,%21,%22,%23,%24,%25,%26,%27,%28,%29,%30,%31}, [%32];"
+        : "=r"(r[0]), "=r"(r[1]), "=r"(r[2]), "=r"(r[3]), "=r"(r[4]), "=r"(r[5]), "=r"(r[6]),
+          "=r"(r[7]), "=r"(r[8]), "=r"(r[9]), "=r"(r[10]), "=r"(r[11]), "=r"(r[12]), "=r"(r[13]),
+          "=r"(r[14]), "=r"(r[15]), "=r"(r[16]), "=r"(r[17]), "=r"(r[18]), "=r"(r[19]),
+          "=r"(r[20]), "=r"(r[21]), "=r"(r[22]), "=r"(r[23]), "=r"(r[24]), "=r"(r[25]),
+          "=r"(r[26]), "=r"(r[27]), "=r"(r[28]), "=r"(r[29]), "=r"(r[30]), "=r"(r[31])
+        : "r"(taddr));
+}
+__device__ __forceinline__ void tmem_ld_wait() {
+    asm volatile("tcgen05.wait::ld.sync.aligned;" ::: "memory");
+}
+
+// Instruction descriptor of kind::f16: D fp32, A and B bf16, both K-major.
+__host__ __device__ constexpr uint32_t make_idesc(int M, int N) {
+    return (1u << 4) | (1u << 7) | (1u << 10) | ((uint32_t)(N >> 3) << 17) |
+           ((uint32_t)(M >> 4) << 24);
+}
+// Shared-memory matrix descriptor: K-major, 128-byte swizzle, 8-row groups 1024 B apart.
+__device__ __forceinline__ uint64_t make_sdesc(uint32_t saddr) {
+    uint64_t d = (uint64_t)((saddr >> 4) & 0x3FFF);
+    d |= (uint64_t)1 << 16;
+    d |= (uint64_t)(1024 >> 4) << 32;
+    d |= (uint64_t)1 << 46;
+    d |= (uint64_t)2 << 61;
+    return d;
+}
+
+// ------------------------------------------------------------------ tile mapping
+struct Tile {
+    int a_row;     // first A row of the tile
+    int row_end;   // rows >= row_end are padding (not stored)
+    int b_row;     // first B row of the tile
+    int n0;        // first output column
+};
+
+template <bool GROUPED, bool DUAL>
+__device__ __forceinline__ Tile tile_of(const GemmParams& p, int t, const int* s_mt_prefix) {
+    constexpr int BN = DUAL ? ACC_COLS / 2 : ACC_COLS;
+    Tile r;
+    if (!GROUPED) {
+        int m = t % p.num_m_tiles, n = t / p.num_m_tiles;
+        r.a_row = m * BM;
+        r.row_end = p.M;
+        r.n0 = n * BN;
+        r.b_row = r.n0;
+    } else {
+        int total_m = s_mt_prefix[p.n_groups];
+        int mt = t % total_m, n = t / total_m;
+        int lo = 0, hi = p.n_groups - 1;  // last group g with prefix[g] <= mt
+        while (lo < hi) {
+            int mid = (lo + hi + 1) >> 1;
+            if (s_mt_prefix[mid] <= mt) lo = mid; else hi = mid - 1;
+        }
+        int g = lo;
+        int g0 = p.group_bounds[g];
+        r.a_row = g0 + (mt - s_mt_prefix[g]) * BM;
+        r.row_end = p.group_bounds[g + 1];
+        r.n0 = n * BN;
+        r.b_row = p.b_base_row + g * p.b_group_stride_rows + r.n0;
+    }
+    return r;
+}
+
+__device__ __forceinline__ float bf2f(uint16_t h) { return __uint_as_float((uint32_t)h << 16); }
+__device__ __forceinline__ float gelu_f(float v) { return 0.5f * v * (1.0f + erff(v * 0.70710678118654752f)); }
+__device__ __forceinline__ float silu_f(float v) { return v / (1.0f + __expf(-v)); }
+
+// Epilogue of one 32-column chunk of one row.
+template <int EPI>
+__device__ __forceinline__ void epilogue_chunk(const GemmParams& p, int row, int n, const float* v,
+                                               const float* u, int out_row) {
+    if (EPI == EPI_SCALE_F32) {
+        const int dst = p.row_table[out_row];
+        const float w = p.row_weight[dst];
+        float* c = reinterpret_cast<float*>(p.C) + (int64_t)dst * p.ldc + n;
+        if (n + 32 <= p.N) {
+#pragma unroll
+            for (int j = 0; j < 32; j += 4)
+                *reinterpret_cast<float4*>(c + j) = make_float4(w * v[j], w * v[j + 1], w * v[j + 2], w * v[j + 3]);
+        } else {
+            for (int j = 0; j < 32 && n + j < p.N; ++j) c[j] = w * v[j];
+        }
+        return;
+    }
+    float o[32];
+    const bool full = n + 32 <= p.N;
+    if (EPI == EPI_BIAS_GELU || EPI == EPI_BIAS_RESID) {
+        const uint16_t* bb = reinterpret_cast<const uint16_t*>(p.bias) + n;
+        if (full) {
+#pragma unroll
+            for (int j = 0; j < 32; j += 8) {
+                uint4 q = *reinterpret_cast<const uint4*>(bb + j);
+                const uint16_t* h = reinterpret_cast<const uint16_t*>(&q);
+#pragma unroll
+                for (int i = 0; i < 8; ++i) o[j + i] = v[j + i] + bf2f(h[i]);
+            }
+        } else {
+            for (int j = 0; j < 32; ++j) o[j] = v[j] + (n + j < p.N ? bf2f(bb[j]) : 0.f);
+        }
+    } else {
+#pragma unroll
+        for (int j = 0; j < 32; ++j) o[j] = v[j];
+    }
+    if (EPI == EPI_BIAS_GELU) {
+#pragma unroll
+        for (int j = 0; j < 32; ++j) o[j] = gelu_f(o[j]);
+    }
+    if (EPI == EPI_SWIGLU) {
+#pragma unroll
+        for (int j = 0; j < 32; ++j) o[j] = silu_f(o[j]) * u[j];
+    }
+    if (EPI == EPI_BIAS_RESID || EPI == EPI_RESID) {
+        const uint16_t* rr = reinterpret_cast<const uint16_t*>(p.resid) + (int64_t)row * p.ldr + n;
+        if (full) {
+#pragma unroll
+            for (int j = 0; j < 32; j += 8) {
+                uint4 q = *reinterpret_cast<const uint4*>(rr + j);
+                const uint16_t* h = reinterpret_cast<const uint16_t*>(&q);
+#pragma unroll
+                for (int i = 0; i < 8; ++i) o[j + i] += bf2f(h[i]);
+            }
+        } else {
+            for (int j = 0; j < 32; ++j)
+                if (n + j < p.N) o[j] += bf2f(rr[j]);
+        }
+    }
+    __nv_bfloat16* c = reinterpret_cast<__nv_bfloat16*>(p.C) + (int64_t)out_row * p.ldc + n;
+    if (full) {
+#pragma unroll
+        for (int j = 0; j < 32; j += 8) {
+            uint4 q;
+            __nv_bfloat162* h2 = reinterpret_cast<__nv_bfloat162*>(&q);
+#pragma unroll
+            for (int i = 0; i < 4; ++i) h2[i] = __floats2bfloat162_rn(o[j + 2 * i], o[j + 2 * i + 1]);
+            *reinterpret_cast<uint4*>(c + j) = q;
+        }
+    } else {
+        for (int j = 0; j < 32 && n + j < p.N; ++j) c[j] = __float2bfloat16_rn(o[j]);
+    }
+}
+
+template <int EPI, bool DUAL, bool GROUPED>
+__global__ void __launch_bounds__(NUM_THREADS, 1) gemm_bf16_tc(const __grid_constant__ GemmParams p) {
+    extern __shared__ uint8_t smem_raw[];
+    const uint32_t raw = smem_u32(smem_raw);
+    const uint32_t base = (raw + 1023u) & ~1023u;
+    uint8_t* gbase = smem_raw + (base - raw);
+    const uint32_t bar0 = base + STAGES * STAGE_BYTES;
+    // barrier layout: full[S], empty[S], tfull[2], tempty[2], done; then tmem base word
+    auto full_bar = [&](int s) { return bar0 + 8u * s; };
+    auto empty_bar = [&](int s) { return bar0 + 8u * (STAGES + s); };
+    auto tfull_bar = [&](int b) { return bar0 + 8u * (2 * STAGES + b); };
+    auto tempty_bar = [&](int b) { return bar0 + 8u * (2 * STAGES + 2 + b); };
+    const uint32_t done_bar = bar0 + 8u * (2 * STAGES + 4);
+    uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(gbase + STAGES * STAGE_BYTES + 8 * (2 * STAGES + 5));
+    __shared__ int s_mt_prefix[MAX_GROUPS + 1];
+    __shared__ volatile int s_abort;
+
+    const int warp = threadIdx.x >> 5;
+    const int lane = threadIdx.x & 31;
+
+    if (threadIdx.x == 0) {
+        s_abort = 0;
+        for (int s = 0; s < STAGES; ++s) {
+            mbar_init(full_bar(s), 1);
+            mbar_init(empty_bar(s), 1);
+        }
+        for (int b = 0; b < 2; ++b) {
+            mbar_init(tfull_bar(b), 1);
+            mbar_init(tempty_bar(b), 128);
+        }
+        mbar_init(done_bar, 1);
+        asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
+        asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
+    }
+    if (GROUPED && threadIdx.x == 32) {
+        int acc = 0;
+        for (int g = 0; g < p.n_groups; ++g) {
+            s_mt_prefix[g] = acc;
+            int rows = p.group_bounds[g + 1] - p.group_bounds[g];
+            acc += (rows + BM - 1) / BM;
+        }
+        s_mt_prefix[p.n_groups] = acc;
+    }
+    if (warp == 1) {
+        tmem_alloc(smem_u32(tmem_slot), 512);
+        tmem_relinquish();
+    }
+    tc_fence_before();
+    __syncthreads();
+    tc_fence_after();
+    const uint32_t tmem_base = *tmem_slot;
+
+    int num_tiles = p.num_tiles;
+    if (GROUPED) num_tiles = s_mt_prefix[p.n_groups] * p.num_n_tiles;
+    const int kb_n = p.num_k_blocks;
+
+    if (warp == 0) {
+        // ------------------------------------------------------------ TMA producer
+        if (lane == 0) {
+            tma_prefetch_desc(&p.tmA);
+            tma_prefetch_desc(&p.tmB);
+            bool ok = true;
+            if (p.ready) {  // the weights this GEMM reads arrive through a ready word
+                const uint64_t t0 = globaltimer_ns();
+                while (ld_acquire_gpu(p.ready) != p.epoch) {
+                    if (*(volatile uint32_t*)p.err || globaltimer_ns() - t0 > p.wait_ns) {
+                        raise_error(p.err, p.wait_code);
+                        break;
+                    }
+                    __nanosleep(64);
+                }
+                asm volatile("fence.proxy.async.global;" ::: "memory");
+            }
+            int it = 0;
+            uint32_t issued_mask = 0;
+            for (int t = blockIdx.x; t < num_tiles && ok; t += gridDim.x) {
+                const Tile tl = tile_of<GROUPED, DUAL>(p, t, s_mt_prefix);
+                for (int kb = 0; kb < kb_n; ++kb, ++it) {
+                    const int s = it % STAGES;
+                    const uint32_t ph = (uint32_t)(it / STAGES) & 1u;
+                    if (!mbar_wait(empty_bar(s), ph ^ 1u, p.err, 1, p.mbar_limit_ns) || s_abort) {
+                        ok = false;
+                        s_abort = 1;
+                        break;
+                    }
+                    const uint32_t sa = base + s * STAGE_BYTES;
+                    const uint32_t sb = sa + A_BYTES;
+                    mbar_expect_tx(full_bar(s), STAGE_BYTES);
+                    tma_load_2d(sa, &p.tmA, full_bar(s), kb * BK, tl.a_row);
+                    if (DUAL) {
+                        tma_load_2d(sb, &p.tmB, full_bar(s), kb * BK, tl.b_row);
+                        tma_load_2d(sb + B_BYTES / 2, &p.tmB, full_bar(s), kb * BK,
+                                    tl.b_row + p.b2_row_off);
+                    } else {
+                        tma_load_2d(sb, &p.tmB, full_bar(s), kb * BK, tl.b_row);
+                    }
+                    issued_mask |= 1u << s;
+                }
+            }
+            // drain: every stage's last armed phase must have landed before exit
+            for (int s = 0; s < STAGES; ++s) {
+                if (!(issued_mask & (1u << s))) continue;
+                // the last issue on stage s had index <= it-1 with (index % STAGES) == s
+                int last = it - 1 - ((it - 1 - s) % STAGES + STAGES) % STAGES;
+                mbar_wait(full_bar(s), (uint32_t)(last / STAGES) & 1u, p.err, 5, p.mbar_limit_ns);
+            }
+        }
+    } else if (warp == 1) {
+        // ------------------------------------------------------------ MMA issuer
+        if (lane == 0) {
+            constexpr uint32_t IDESC = DUAL ? make_idesc(BM, ACC_COLS / 2) : make_idesc(BM, ACC_COLS);
+            int it = 0, tcount = 0;
+            bool ok = true;
+            for (int t = blockIdx.x; t < num_tiles && ok; t += gridDim.x, ++tcount) {
+                const int buf = tcount & 1;
+                const uint32_t tph = (uint32_t)(tcount >> 1) & 1u;
+                if (!mbar_wait(tempty_bar(buf), tph ^ 1u, p.err, 2, p.mbar_limit_ns) || s_abort) {
+                    s_abort = 1;
+                    break;
+                }
+                tc_fence_after();
+                const uint32_t d = tmem_base + (uint32_t)(buf * ACC_COLS);
+                for (int kb = 0; kb < kb_n; ++kb, ++it) {
+                    const int s = it % STAGES;
+                    const uint32_t ph = (uint32_t)(it / STAGES) & 1u;
+                    if (!mbar_wait(full_bar(s), ph, p.err, 3, p.mbar_limit_ns) || s_abort) {
+                        ok = false;
+                        s_abort = 1;
+                        break;
+                    }
+                    tc_fence_after();
+                    const uint32_t sa = base + s * STAGE_BYTES;
+                    const uint32_t sb = sa + A_BYTES;
+#pragma unroll
+                    for (int kk = 0; kk < BK / 16; ++kk) {
+                        const uint64_t ad = make_sdesc(sa + kk * 32);
+                        const uint32_t acc = (kb > 0 || kk > 0) ? 1u : 0u;
+                        if (DUAL) {
+                            umma_bf16(d, ad, make_sdesc(sb + kk * 32), IDESC, acc);
+                            umma_bf16(d + ACC_COLS / 2, ad, make_sdesc(sb + B_BYTES / 2 + kk * 32), IDESC, acc);
+                        } else {
+                            umma_bf16(d, ad, make_sdesc(sb + kk * 32), IDESC, acc);
+                        }
+                    }
+                    umma_commit(empty_bar(s));
+                }
+                if (ok) umma_commit(tfull_bar(buf));
+            }
+            // every MMA issued by this thread has completed once done_bar flips
+            umma_commit(done_bar);
+            mbar_wait(done_bar, 0, p.err, 6, p.mbar_limit_ns);
+        }
+    } else {
+        // ------------------------------------------------------------ epilogue (warps 2..5)
+        const int q = warp & 3;                 // TMEM lane quarter this warp may read
+        const int row_in_tile = q * 32 + lane;
+        int tcount = 0;
+        for (int t = blockIdx.x; t < num_tiles; t += gridDim.x, ++tcount) {
+            const int buf = tcount & 1;
+            const uint32_t tph = (uint32_t)(tcount >> 1) & 1u;
+            if (!mbar_wait(tfull_bar(buf), tph, p.err, 4, p.mbar_limit_ns) || s_abort) {
+                s_abort = 1;
+                break;
+            }
+            tc_fence_after();
+            const Tile tl = tile_of<GROUPED, DUAL>(p, t, s_mt_prefix);
+            const int row = tl.a_row + row_in_tile;
+            const bool valid = row < tl.row_end && row < p.M;
+            const uint32_t tbase = tmem_base + ((uint32_t)(q * 32) << 16) + (uint32_t)(buf * ACC_COLS);
+            constexpr int CHUNKS = DUAL ? ACC_COLS / 64 : ACC_COLS / 32;
+#pragma unroll 1
+            for (int c = 0; c < CHUNKS; ++c) {
+                uint32_t r[32], r2[32];
+                tmem_ld32(tbase + c * 32, r);
+                if (DUAL) tmem_ld32(tbase + ACC_COLS / 2 + c * 32, r2);
+                tmem_ld_wait();
+                const int n = tl.n0 + c * 32;
+                if (valid && n < p.N) {
+                    float v[32], u[32];
+#pragma unroll
+                    for (int j = 0; j < 32; ++j) {
+                        v[j] = __uint_as_float(r[j]);
+                        u[j] = DUAL ? __uint_as_float(r2[j]) : 0.f;
+                    }
+                    epilogue_chunk<EPI>(p, row, n, v, u, row);
+                }
+            }
+            tc_fence_before();
+            mbar_arrive(tempty_bar(buf));
+        }
+    }
+    tc_fence_before();
+    __syncthreads();
+    if (warp == 1) {
+        tc_fence_after();
+        tmem_dealloc(tmem_base, 512);
+    }
+}
+
+// ------------------------------------------------------------------ host side
+typedef CUresult (*EncodeTiledFn)(CUtensorMap*, CUtensorMapDataType, cuuint32_t, void*, const cuuint64_t*,
+                                  const cuuint64_t*, const cuuint32_t*, const cuuint32_t*,
+                                  CUtensorMapInterleave, CUtensorMapSwizzle, CUtensorMapL2promotion,
+                                  CUtensorMapFloatOOBfill);
+
+EncodeTiledFn encode_fn() {
+    static EncodeTiledFn fn = nullptr;
+    static std::once_flag once;
+    std::call_once(once, [] {
+        void* p = nullptr;
+        cudaDriverEntryPointQueryResult q;
+        if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &p, 12000, cudaEnableDefault,
+                                             &q) == cudaSuccess &&
+            q == cudaDriverEntryPointSuccess)
+            fn = reinterpret_cast<EncodeTiledFn>(p);
+    });
+    return fn;
+}
+
+// 2-D bf16 view [rows, cols] with row stride ld (elements); box = 64 x box_rows, 128-byte swizzle.
+bool make_tmap(CUtensorMap* m, const void* ptr, int64_t rows, int64_t cols, int64_t ld, int box_rows) {
+    EncodeTiledFn fn = encode_fn();
+    if (!fn) return false;
+    cuuint64_t dims[2] = {(cuuint64_t)cols, (cuuint64_t)rows};
+    cuuint64_t strides[1] = {(cuuint64_t)(ld * 2)};
+    cuuint32_t box[2] = {(cuuint32_t)BK, (cuuint32_t)box_rows};
+    cuuint32_t estr[2] = {1, 1};
+    CUresult r = fn(m, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, const_cast<void*>(ptr), dims, strides, box,
+                    estr, CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
+                    CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+    return r == CUDA_SUCCESS;
+}
+
+struct MapKey {
+    const void* p;
+    int64_t rows, cols, ld;
+    int box;
+    bool operator==(const MapKey& o) const {
+        return p == o.p && rows == o.rows && cols == o.cols && ld == o.ld && box == o.box;
+    }
+};
+struct MapKeyHash {
+    size_t operator()(const MapKey& k) const {
+        size_t h = std::hash<const void*>()(k.p);
+        h ^= std::hash<int64_t>()(k.rows * 1000003 + k.cols * 31 + k.ld) + 0x9e3779b9 + (h << 6) + (h >> 2);
+        return h ^ (size_t)k.box;
+    }
+};
+
+bool cached_tmap(CUtensorMap* out, const void* ptr, int64_t rows, int64_t cols, int64_t ld, int box) {
+    static std::mutex mu;
+    static std::unordered_map<MapKey, CUtensorMap, MapKeyHash> cache;
+    MapKey k{ptr, rows, cols, ld, box};
+    std::lock_guard<std::mutex> g(mu);
+    auto it = cache.find(k);
+    if (it != cache.end()) {
+        *out = it->second;
+        return true;
+    }
+    if (!make_tmap(out, ptr, rows, cols, ld, box)) return false;
+    if (cache.size() > 4096) cache.clear();
+    cache.emplace(k, *out);
+    return true;
+}
+
+template <int EPI, bool DUAL, bool GROUPED>
+cudaError_t launch_t(const GemmParams& p, int grid, cudaStream_t s) {
+    auto kern = gemm_bf16_tc<EPI, DUAL, GROUPED>;
+    static bool attr_set = false;
+    if (!attr_set) {
+        cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, SMEM_BYTES);
+        if (e != cudaSuccess) return e;
+        attr_set = true;
+    }
+    kern<<<grid, NUM_THREADS, SMEM_BYTES, s>>>(p);
+    return cudaGetLastError();
+}
+
+}  // namespace
+
+int gemm_num_sms() {
+    static int n = 0;
+    if (!n) {
+        int dev = 0;
+        cudaGetDevice(&dev);
+        cudaDeviceGetAttribute(&n, cudaDevAttrMultiProcessorCount, dev);
+        if (n <= 0) n = 1;
+    }
+    return n;
+}
+
+cudaError_t launch_gemm_bf16(const GemmDesc& d, int max_ctas, cudaStream_t s) {
+    const bool dual = d.epi == EPI_SWIGLU;
+    const bool grouped = d.group_bounds != nullptr;
+    if (d.M < 0 || d.N <= 0 || d.K <= 0 || (d.K % 8) || (d.N % 8) || (d.lda % 8) || (d.ldb % 8) ||
+        (reinterpret_cast<uintptr_t>(d.A) & 15) || (reinterpret_cast<uintptr_t>(d.B) & 15))
+        return cudaErrorInvalidValue;
+    if (d.epi != EPI_SCALE_F32 && ((d.ldc % 8) || (reinterpret_cast<uintptr_t>(d.C) & 15)))
+        return cudaErrorInvalidValue;
+    if ((d.epi == EPI_BIAS_RESID || d.epi == EPI_RESID) &&
+        ((d.ldr % 8) || (reinterpret_cast<uintptr_t>(d.resid) & 15)))
+        return cudaErrorInvalidValue;
+    if (grouped && (d.n_groups < 1 || d.n_groups > MAX_GROUPS)) return cudaErrorInvalidValue;
+    if (d.M == 0) return cudaSuccess;
+    GemmParams p;
+    memset(&p, 0, sizeof(p));
+    const int BN = dual ? ACC_COLS / 2 : ACC_COLS;
+    if (!cached_tmap(&p.tmA, d.A, d.a_rows > 0 ? d.a_rows : d.M, d.K, d.lda, BM)) return cudaErrorInvalidValue;
+    if (!cached_tmap(&p.tmB, d.B, d.b_rows > 0 ? d.b_rows : d.N, d.K, d.ldb, BN)) return cudaErrorInvalidValue;
+    p.M = d.M;
+    p.N = d.N;
+    p.K = d.K;
+    p.num_m_tiles = (d.M + BM - 1) / BM;
+    p.num_n_tiles = (d.N + BN - 1) / BN;
+    p.num_k_blocks = (d.K + BK - 1) / BK;
+    p.num_tiles = p.num_m_tiles * p.num_n_tiles;
+    p.b2_row_off = d.b2_row_off;
+    p.bias = reinterpret_cast<const __nv_bfloat16*>(d.bias);
+    p.resid = reinterpret_cast<const __nv_bfloat16*>(d.resid);
+    p.ldr = d.ldr;
+    p.C = d.C;
+    p.ldc = d.ldc;
+    p.group_bounds = d.group_bounds;
+    p.n_groups = d.n_groups;
+    p.b_group_stride_rows = d.b_group_stride_rows;
+    p.b_base_row = d.b_base_row;
+    p.row_table = d.row_table;
+    p.row_weight = d.row_weight;
+    p.ready = d.ready;
+    p.epoch = d.epoch;
+    p.wait_ns = d.wait_ns;
+    p.err = d.err_word;
+    p.wait_code = d.wait_code;
+    p.mbar_limit_ns = MBAR_LIMIT_NS + (d.ready ? d.wait_ns : 0);
+    int tiles = p.num_tiles;
+    if (grouped) {
+        // sum over groups of ceil(rows/BM) <= M/BM + n_groups
+        tiles = (p.num_m_tiles + d.n_groups) * p.num_n_tiles;
+        if (d.max_tiles_hint > 0 && d.max_tiles_hint < tiles) tiles = d.max_tiles_hint;
+    }
+    int sms = gemm_num_sms();
+    int grid = max_ctas > 0 ? (max_ctas < sms ? max_ctas : sms) : sms;
+    if (grid > tiles) grid = tiles;
+    if (grid < 1) grid = 1;
+    switch (d.epi) {
+        case EPI_STORE:
+            return grouped ? cudaErrorInvalidValue : launch_t<EPI_STORE, false, false>(p, grid, s);
+        case EPI_BIAS_GELU:
+            return grouped ? cudaErrorInvalidValue : launch_t<EPI_BIAS_GELU, false, false>(p, grid, s);
+        case EPI_BIAS_RESID:
+            return grouped ? cudaErrorInvalidValue : launch_t<EPI_BIAS_RESID, false, false>(p, grid, s);
+        case EPI_RESID:
+            return grouped ? cudaErrorInvalidValue : launch_t<EPI_RESID, false, false>(p, grid, s);
+        case EPI_SWIGLU:
+            return grouped ? launch_t<EPI_SWIGLU, true, true>(p, grid, s)
+                           : launch_t<EPI_SWIGLU, true, false>(p, grid, s);
+        case EPI_SCALE_F32:
+            return grouped ? launch_t<EPI_SCALE_F32, false, true>(p, grid, s) : cudaErrorInvalidValue;
+    }
+    return cudaErrorInvalidValue;
+}
+
+}  // namespace ls

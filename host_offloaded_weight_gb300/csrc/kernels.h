@@ -1,0 +1,86 @@
+// Internal kernel launchers of the layer-streaming library (not part of the C ABI).
+#pragma once
+#include <cuda_runtime.h>
+#include <stdint.h>
+
+namespace ls {
+
+// ---------------------------------------------------------------- copy path
+struct CopyRange {
+    const void* src;      // device-visible address of mapped pinned host memory
+    int64_t dst_off;      // byte offset inside the destination slot
+    int64_t n16;          // whole 16-byte units
+    int64_t chunk_begin;  // first chunk index of this range in the launch
+    int32_t tail;         // trailing bytes (< 16)
+    int32_t pad;
+};
+int64_t copy_chunks_for(int64_t n16);
+cudaError_t launch_copy_h2slot(const CopyRange* ranges_dev, int n_ranges, int64_t n_chunks,
+                               void* dst_base, const uint8_t* group_mask_dev, int ranges_per_group, uint32_t* ready,
+                               uint32_t* ticket, uint32_t epoch, bool publish, int ctas,
+                               cudaStream_t s);
+cudaError_t launch_publish(uint32_t* ready, uint32_t epoch, bool publish, cudaStream_t s);
+cudaError_t launch_wait_ready(const uint32_t* ready, uint32_t epoch, uint64_t limit_ns,
+                              uint32_t* err_word, uint32_t code, cudaStream_t s);
+
+// ---------------------------------------------------------------- fp32 linear + GELU
+cudaError_t launch_linear_gelu_f32(const float* x, const float* w, const float* b, float* y, int T,
+                                   int H, int F, cudaStream_t s);
+
+// ---------------------------------------------------------------- tcgen05 GEMM
+enum GemmEpilogue : int {
+    EPI_STORE = 0,      // C = acc                          -> bf16
+    EPI_BIAS_GELU = 1,  // C = GELU(acc + bias)             -> bf16
+    EPI_BIAS_RESID = 2, // C = acc + bias + R               -> bf16
+    EPI_SWIGLU = 3,     // dual B: C = SiLU(acc_g) * acc_u  -> bf16
+    EPI_RESID = 4,      // C = acc + R                      -> bf16
+    EPI_SCALE_F32 = 5,  // grouped: Y[row_table[i]] = w[row_table[i]] * acc -> fp32
+};
+
+struct GemmDesc {
+    int epi = EPI_STORE;
+    // A: [M, K] bf16 row-major (lda elements); B: [rows, K] bf16 row-major (ldb elements)
+    const void* A = nullptr;
+    int64_t lda = 0;
+    int64_t a_rows = 0;          // rows addressable through A (>= M)
+    const void* B = nullptr;
+    int64_t ldb = 0;
+    int64_t b_rows = 0;          // rows addressable through B
+    int M = 0, N = 0, K = 0;
+    int b2_row_off = 0;          // dual: second B matrix starts this many rows after the first
+    const void* bias = nullptr;  // [N] bf16
+    const void* resid = nullptr; // [M, ldr] bf16
+    int64_t ldr = 0;
+    void* C = nullptr;
+    int64_t ldc = 0;
+    // grouped (expert) mode: M is the total row count; groups split it
+    const int* group_bounds = nullptr;  // [n_groups + 1], device
+    int n_groups = 0;
+    int b_group_stride_rows = 0;        // B rows between consecutive groups' matrices
+    int b_base_row = 0;                 // B row of group 0's matrix
+    const int* row_table = nullptr;     // EPI_SCALE_F32: destination row of sorted row i
+    const float* row_weight = nullptr;  // EPI_SCALE_F32: weight by destination row
+    int max_tiles_hint = 0;             // grouped: upper bound of tiles (grid sizing)
+    // fused ready-word wait before the first weight load (optional)
+    const uint32_t* ready = nullptr;
+    uint32_t epoch = 0;
+    uint64_t wait_ns = 0;
+    uint32_t* err_word = nullptr;       // mapped host word for timeouts
+    uint32_t wait_code = 0;
+};
+
+// max_ctas <= 0: one CTA per SM.
+cudaError_t launch_gemm_bf16(const GemmDesc& d, int max_ctas, cudaStream_t s);
+int gemm_num_sms();
+
+// ---------------------------------------------------------------- MoE
+cudaError_t launch_moe_route(const float* logits, int n_layers, int T, int E, int k, int* sel,
+                             float* weight, cudaStream_t s);
+cudaError_t launch_moe_group(const int* sel, int n_layers, int T, int E, int k, int* row_table,
+                             int* group_bounds, uint8_t* expert_used, cudaStream_t s);
+cudaError_t launch_moe_gather(const void* x, const int* row_table, int rows, int k, int H,
+                              void* x_sorted, cudaStream_t s);
+cudaError_t launch_moe_combine(const void* x, const float* y, int T, int k, int H, void* out,
+                               cudaStream_t s);
+
+}  // namespace ls

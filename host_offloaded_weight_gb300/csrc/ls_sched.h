@@ -1,0 +1,100 @@
+// Streaming scheduler: slot plan, prefetch window, resident prefix, pool
+// degradation, synchronous fallback, eviction. Host-only integer logic.
+//
+// Rules ("feat: prefetch streamed layers during compute", Summary and Effective
+// behavior table; "feat: pool VRAM for streamed layer", Summary and pool
+// behavior table):
+//   S  = largest 256-byte-aligned private footprint of a segment.
+//   max_vram_bytes == 0: segmentation off, every segment resident.
+//   otherwise avail = floor((budget - shared) / S); below one slot the single
+//   mandatory slot is taken with a warning and nothing else (no residents, no
+//   prefetch).
+//   Depth first: the largest depth <= requested whose ring fits with no
+//   residents; then the longest resident prefix <= cap that still fits.
+//   Ring Q = min(d + 1, N - R); pool P = R + Q. Load j of a run goes to slot
+//   R + (j mod Q); resident i lives in slot i.
+//   Per step k: queue prefetches until the loads issued reach (streamed
+//   segments <= k) + d; load k synchronously if it was not queued; activate k.
+//   A failing pool is retried with fewer slots of the same size (re-planned
+//   for that many); pool off, a failing load first evicts the last resident
+//   already computed in this run, a failing prefetch then falls back to
+//   synchronous loads for good, a failing synchronous load fails the run.
+#pragma once
+#include <cstdint>
+#include <vector>
+
+#include "ls_api.h"
+
+namespace ls {
+
+struct Plan {
+    int N = 0;
+    int64_t S = 0;
+    int64_t shared_total = 0;
+    int avail = 0;
+    int d_fit = 0;   // depth that fits, before capping by the streamed count
+    int R = 0;
+    int Q = 0;
+    int P = 0;
+    bool mandatory = false;
+};
+
+Plan make_plan(int N, int64_t S, int64_t shared_total, int depth, int resident, int64_t max_vram,
+               int slot_cap /* < 0: none */);
+
+// What the scheduler asks of the device side. Every call is made in schedule
+// order; a false return from an allocation means the memory is not available.
+struct Executor {
+    virtual ~Executor() {}
+    virtual bool alloc_shared(int64_t bytes) = 0;
+    virtual bool alloc_pool(int slots, int64_t slot_bytes) = 0;
+    virtual bool alloc_segment(int seg, int64_t bytes) = 0;   // pool off: one buffer per load/resident
+    virtual void free_segment(int seg) = 0;                    // ordered after the segment's compute
+    virtual void begin_run(int run) = 0;
+    virtual void load_shared(int shared_id) = 0;
+    virtual void load(int seg, int slot, int kind, int64_t bytes) = 0;   // kind = LS_EV_*
+    virtual void activate(int seg, int slot, bool via_copy_queue) = 0;
+    virtual void evict(int seg, int slot) = 0;
+};
+
+class Scheduler {
+public:
+    // seg_slot: aligned private footprint per segment; shared: (id, bytes) distinct ids.
+    void configure(const ls_params& p, const std::vector<int64_t>& seg_slot,
+                   const std::vector<std::pair<int, int64_t>>& shared);
+    ls_status register_memory(Executor& ex);                 // plan + shared region + pool
+    ls_status run(Executor& ex, const int64_t* load_bytes);  // one pass; load_bytes[N] or null
+    const Plan& plan() const { return plan_; }
+    const std::vector<ls_sched_event>& log() const { return log_; }
+    void fill_stats(ls_stats& s) const;
+    int residents() const { return R_; }
+    int depth() const { return d_; }
+    int runs() const { return run_; }
+    int64_t live_bytes() const { return live_; }
+
+private:
+    bool alloc_bytes(int64_t bytes) {
+        if (cap_ > 0 && live_ + bytes > cap_) return false;
+        live_ += bytes;
+        return true;
+    }
+    bool alloc_seg_evicting(Executor& ex, int seg, int step, int& cur_R);
+    void emit(int step, int kind, int seg, int slot, int64_t bytes);
+    void fallback();
+
+    ls_params prm_{};
+    std::vector<int64_t> seg_slot_;
+    std::vector<std::pair<int, int64_t>> shared_;
+    Plan plan_;
+    int R_ = 0, d_ = 0, run_ = 0;
+    bool async_ok_ = true, fail_async_ = false;
+    int64_t cap_ = 0, live_ = 0;
+    std::vector<ls_sched_event> log_;
+
+public:
+    int64_t n_prefetch = 0, n_prefetch_activated = 0, n_sync = 0, n_resident = 0,
+            n_shared = 0, n_evict = 0, n_fallback = 0, n_degrade = 0, bytes_loaded = 0;
+    int warnings = 0;
+};
+
+}  // namespace ls

@@ -1,0 +1,1238 @@
+// Layer-streaming runtime: contexts, registration, the GPU executor and the C ABI.
+//
+// The scheduler (ls_sched.h) decides what happens at each step; the executor here
+// turns each decision into device work:
+//   load (prefetch)  copy stream: wait until the slot's previous occupant has
+//                    computed (event), then the host-to-slot copy, whose last
+//                    CTA raises the slot's ready word to a fresh epoch.
+//   load (sync)      the same copy on the compute stream (stream order is the
+//                    hand-off; the ready word is raised too).
+//   activate         compute stream: the segment's kernels; the first kernel
+//                    that reads streamed weights waits for the ready word
+//                    (bounded), then "slot free" is recorded for the copy stream.
+// No host synchronisation happens inside a pass; ls_run synchronises once at the
+// end and then reads the error word the bounded waits write on timeout
+// ("layer split: overlap the stages' hand-off", Changes since #936).
+#include <cuda_runtime.h>
+
+#include <algorithm>
+#include <cstdarg>
+#include <cstdio>
+#include <cstring>
+#include <map>
+#include <string>
+#include <vector>
+
+#include "common.cuh"
+#include "kernels.h"
+#include "ls_api.h"
+#include "ls_sched.h"
+
+using namespace ls;
+
+namespace {
+
+constexpr size_t MIN_PARAMS_SIZE = offsetof(ls_params, use_pool) + sizeof(int32_t);
+constexpr int64_t ALIGN = 256;
+inline int64_t align_up(int64_t n) { return (n + ALIGN - 1) / ALIGN * ALIGN; }
+
+struct TensorRec {
+    const void* host = nullptr;
+    const void* dev = nullptr;  // device-visible address of the host memory
+    uint64_t bytes = 0;
+    int dtype = 0, ndim = 0;
+    int64_t shape[2] = {0, 0};
+    int64_t off = 0;            // offset in the slot (private) or in the shared region (shared)
+    int shared_id = -1;
+};
+
+struct SegRec {
+    std::vector<TensorRec> t;
+    int64_t slot_bytes = 0;     // aligned private footprint
+    int64_t load_bytes = 0;     // exact private bytes
+    bool kernel_ok = true;      // all sources 16-byte aligned
+    CopyRange* ranges_dev = nullptr;
+    int n_ranges = 0;
+    int64_t n_chunks = 0;
+};
+
+struct SharedRec {
+    int id;
+    const void* host;
+    const void* dev;
+    uint64_t bytes;
+    int64_t off;
+};
+
+}  // namespace
+
+struct ls_ctx {
+    ls_params prm{};
+    int device = 0;
+    std::string err;
+    bool registered = false;
+    int kind = -1;
+    int N = 0, H = 0, F = 0, E = 0;
+    std::vector<SegRec> segs;
+    std::vector<SharedRec> shared;
+    std::vector<std::pair<void*, size_t>> host_registered;
+    Scheduler sched;
+    // device memory
+    void* shared_dev = nullptr;
+    void* pool = nullptr;
+    int64_t pool_bytes = 0;
+    std::vector<void*> seg_buf;          // pool off: current buffer of each segment
+    uint32_t* ready = nullptr;           // [P] ready words
+    uint32_t* tickets = nullptr;         // [P] last-CTA tickets
+    std::vector<uint32_t> slot_epoch;
+    std::vector<cudaEvent_t> slot_free;
+    uint32_t* err_word = nullptr;        // mapped pinned host
+    uint32_t* err_word_dev = nullptr;
+    cudaStream_t copy_stream = nullptr;
+    cudaStream_t own_stream = nullptr;
+    cudaEvent_t alloc_event = nullptr;
+    cudaEvent_t run_done = nullptr;          // end of the last queued pass
+    std::vector<cudaStream_t> pending;       // streams with queued passes
+    int copy_path = LS_COPY_ENGINE;
+    int copy_ctas = 0;
+    int reserve_sms = 0;
+    double gbs_kernel = 0, gbs_engine = 0;
+    int64_t publishes = 0;
+    // per-run segment state
+    std::vector<uint32_t> seg_epoch;
+    std::vector<void*> seg_ptr;
+    std::vector<int> seg_slot;
+    // workspaces
+    int64_t ws_tokens = 0;
+    void* act[2] = {nullptr, nullptr};
+    void* hbuf = nullptr;
+    void* ubuf = nullptr;
+    // MoE workspaces
+    int top_k = 0;
+    int* moe_sel = nullptr;
+    float* moe_w = nullptr;
+    int* moe_table = nullptr;
+    int* moe_bounds = nullptr;
+    uint8_t* moe_used = nullptr;
+    uint8_t* moe_used_host = nullptr;
+    void* moe_xs = nullptr;
+    void* moe_hs = nullptr;
+    float* moe_y = nullptr;
+    // host-buffer entry point staging
+    void* stage_x = nullptr;
+    void* stage_y = nullptr;
+    float* stage_logits = nullptr;
+    int64_t stage_tokens = 0;
+    cudaError_t cuda_err = cudaSuccess;
+    // kernel timing (params.kernel_timing)
+    struct TimerClass {
+        std::string name;
+        int64_t launches = 0;
+        double total_ms = 0;
+    };
+    std::vector<TimerClass> tclass;
+    std::vector<std::pair<cudaEvent_t, cudaEvent_t>> tev;  // event pool
+    std::vector<int> tev_class;                              // class of each used pair
+    size_t tev_used = 0;
+};
+
+namespace {
+
+void set_err(ls_ctx* c, const char* fmt, ...) {
+    char buf[512];
+    va_list ap;
+    va_start(ap, fmt);
+    vsnprintf(buf, sizeof(buf), fmt, ap);
+    va_end(ap);
+    c->err = buf;
+}
+
+#define CK(call)                                                                      \
+    do {                                                                              \
+        cudaError_t e_ = (call);                                                      \
+        if (e_ != cudaSuccess) {                                                      \
+            set_err(c, "%s failed: %s", #call, cudaGetErrorString(e_));               \
+            return LS_ERR_CUDA;                                                       \
+        }                                                                             \
+    } while (0)
+
+void* dev_alloc(ls_ctx* c, size_t bytes, cudaStream_t s) {
+    if (bytes == 0) return nullptr;
+    if (c->prm.alloc_fn) return c->prm.alloc_fn(c->prm.alloc_user, bytes, s);
+    void* p = nullptr;
+    if (cudaMallocAsync(&p, bytes, s) != cudaSuccess) {
+        cudaGetLastError();
+        return nullptr;
+    }
+    return p;
+}
+
+void dev_free(ls_ctx* c, void* p, size_t bytes, cudaStream_t s) {
+    if (!p) return;
+    if (c->prm.free_fn) {
+        c->prm.free_fn(c->prm.alloc_user, p, bytes, s);
+        return;
+    }
+    cudaFreeAsync(p, s);
+}
+
+inline void track(ls_ctx* c, cudaError_t e) {
+    if (e != cudaSuccess && c->cuda_err == cudaSuccess) c->cuda_err = e;
+}
+
+// Bracket one launch with events on its own stream (only with kernel_timing on).
+struct KTime {
+    ls_ctx* c;
+    cudaStream_t s;
+    size_t idx = (size_t)-1;
+    KTime(ls_ctx* ctx, const char* name, cudaStream_t st) : c(ctx), s(st) {
+        if (!c->prm.kernel_timing) return;
+        int cls = -1;
+        for (size_t i = 0; i < c->tclass.size(); ++i)
+            if (c->tclass[i].name == name) cls = (int)i;
+        if (cls < 0) {
+            c->tclass.push_back({name, 0, 0});
+            cls = (int)c->tclass.size() - 1;
+        }
+        if (c->tev_used == c->tev.size()) {
+            cudaEvent_t a, b;
+            if (cudaEventCreate(&a) != cudaSuccess || cudaEventCreate(&b) != cudaSuccess) return;
+            c->tev.push_back({a, b});
+            c->tev_class.push_back(cls);
+        }
+        idx = c->tev_used++;
+        c->tev_class[idx] = cls;
+        track(c, cudaEventRecord(c->tev[idx].first, s));
+    }
+    ~KTime() {
+        if (idx != (size_t)-1) track(c, cudaEventRecord(c->tev[idx].second, s));
+    }
+};
+
+// After the run's final synchronisation: fold the recorded pairs into the classes.
+void collect_times(ls_ctx* c) {
+    for (size_t i = 0; i < c->tev_used; ++i) {
+        float ms = 0;
+        if (cudaEventElapsedTime(&ms, c->tev[i].first, c->tev[i].second) == cudaSuccess) {
+            c->tclass[c->tev_class[i]].launches += 1;
+            c->tclass[c->tev_class[i]].total_ms += ms;
+        } else {
+            cudaGetLastError();
+        }
+    }
+    c->tev_used = 0;
+}
+
+// --------------------------------------------------------------------------- copies
+void issue_copy(ls_ctx* c, int seg, void* dst, int slot, uint32_t epoch, cudaStream_t s, bool use_kernel,
+                const uint8_t* expert_mask) {
+    SegRec& sr = c->segs[seg];
+    const bool publish = !(c->prm.test_drop_publish > 0 && ++c->publishes == c->prm.test_drop_publish);
+    if (use_kernel && sr.kernel_ok) {
+        KTime kt(c, "copy_h2slot", s);
+        track(c, launch_copy_h2slot(sr.ranges_dev, sr.n_ranges, sr.n_chunks, dst, expert_mask,
+                                    expert_mask ? 3 : 1, c->ready + slot, c->tickets + slot, epoch,
+                                    publish, c->copy_ctas, s));
+        return;
+    }
+    // copy engine: one copy per tensor (contiguous neighbours merged), then publish
+    KTime kt(c, "copy_engine", s);
+    const bool moe = c->kind == LS_KIND_MOE_SWIGLU_BF16;
+    int64_t run_dst = 0, run_len = 0;
+    const uint8_t* host_src0 = nullptr;
+    auto flush = [&]() {
+        if (run_len > 0)
+            track(c, cudaMemcpyAsync((uint8_t*)dst + run_dst, host_src0, run_len, cudaMemcpyHostToDevice, s));
+        run_len = 0;
+    };
+    for (size_t i = 0; i < sr.t.size(); ++i) {
+        const TensorRec& t = sr.t[i];
+        if (t.shared_id >= 0) continue;
+        if (moe && c->moe_used_host && !c->moe_used_host[(int64_t)seg * c->E + i / 3]) {
+            flush();
+            continue;
+        }
+        const uint8_t* src = (const uint8_t*)t.host;
+        if (run_len > 0 && src == host_src0 + run_len && t.off == run_dst + run_len) {
+            run_len += (int64_t)t.bytes;
+        } else {
+            flush();
+            host_src0 = src;
+            run_dst = t.off;
+            run_len = (int64_t)t.bytes;
+        }
+    }
+    flush();
+    track(c, launch_publish(c->ready + slot, epoch, publish, s));
+}
+
+// --------------------------------------------------------------------------- compute
+const void* tptr(ls_ctx* c, int seg, int i) {
+    const TensorRec& t = c->segs[seg].t[i];
+    if (t.shared_id >= 0) return (const uint8_t*)c->shared_dev + t.off;
+    return (const uint8_t*)c->seg_ptr[seg] + t.off;
+}
+
+int gemm_ctas(ls_ctx* c) {
+    int sms = gemm_num_sms();
+    int r = c->reserve_sms;
+    if (r < 0) r = 0;
+    return std::max(1, sms - r);
+}
+
+struct RunCtx {
+    const void* x;
+    void* y;
+    int64_t T;
+    cudaStream_t s;
+    uint64_t wait_ns;
+};
+
+void compute_segment(ls_ctx* c, const RunCtx& rc, int seg, bool wait) {
+    const int N = c->N;
+    const void* xin = seg == 0 ? rc.x : c->act[(seg - 1) & 1];
+    void* xout = seg == N - 1 ? rc.y : c->act[seg & 1];
+    const int T = (int)rc.T, H = c->H, F = c->F;
+    const int slot = c->seg_slot[seg];
+    const uint32_t epoch = c->seg_epoch[seg];
+    const uint32_t code = DERR_HANDOFF_TIMEOUT | ((uint32_t)slot << 8);
+    GemmDesc w0;  // fused wait for the first kernel reading streamed weights
+    if (wait) {
+        w0.ready = c->ready + slot;
+        w0.epoch = epoch;
+        w0.wait_ns = rc.wait_ns;
+        w0.err_word = c->err_word_dev;
+        w0.wait_code = code;
+    }
+    const int ctas = gemm_ctas(c);
+    switch (c->kind) {
+        case LS_KIND_LINEAR_GELU_F32: {
+            if (wait) {
+                KTime kt(c, "wait_ready", rc.s);
+                track(c, launch_wait_ready(c->ready + slot, epoch, rc.wait_ns, c->err_word_dev, code, rc.s));
+            }
+            KTime kt(c, "linear_gelu_f32", rc.s);
+            track(c, launch_linear_gelu_f32((const float*)xin, (const float*)tptr(c, seg, 0),
+                                            (const float*)tptr(c, seg, 1), (float*)xout, T, H, F, rc.s));
+            break;
+        }
+        case LS_KIND_FFN_GELU_BF16:
+        case LS_KIND_FFN_GELU_SHARED_BF16: {
+            const bool proj = c->kind == LS_KIND_FFN_GELU_SHARED_BF16;
+            const int o = proj ? 1 : 0;
+            const void* a1 = xin;
+            if (proj) {
+                GemmDesc g;
+                g.epi = EPI_STORE;
+                g.A = xin; g.lda = H; g.a_rows = T;
+                g.B = tptr(c, seg, 0); g.ldb = H; g.b_rows = H;
+                g.M = T; g.N = H; g.K = H;
+                g.C = c->ubuf; g.ldc = H;
+                KTime kt(c, "gemm_proj", rc.s);
+                track(c, launch_gemm_bf16(g, ctas, rc.s));
+                a1 = c->ubuf;
+            }
+            GemmDesc g1 = w0;
+            g1.epi = EPI_BIAS_GELU;
+            g1.A = a1; g1.lda = H; g1.a_rows = T;
+            g1.B = tptr(c, seg, o + 0); g1.ldb = H; g1.b_rows = F;
+            g1.bias = tptr(c, seg, o + 1);
+            g1.M = T; g1.N = F; g1.K = H;
+            g1.C = c->hbuf; g1.ldc = F;
+            {
+                KTime kt(c, "gemm_up", rc.s);
+                track(c, launch_gemm_bf16(g1, ctas, rc.s));
+            }
+            GemmDesc g2;
+            g2.epi = EPI_BIAS_RESID;
+            g2.A = c->hbuf; g2.lda = F; g2.a_rows = T;
+            g2.B = tptr(c, seg, o + 2); g2.ldb = F; g2.b_rows = H;
+            g2.bias = tptr(c, seg, o + 3);
+            g2.resid = xin; g2.ldr = H;
+            g2.M = T; g2.N = H; g2.K = F;
+            g2.C = xout; g2.ldc = H;
+            KTime kt(c, "gemm_down", rc.s);
+            track(c, launch_gemm_bf16(g2, ctas, rc.s));
+            break;
+        }
+        case LS_KIND_SWIGLU_BF16: {
+            GemmDesc g1 = w0;
+            g1.epi = EPI_SWIGLU;
+            g1.A = xin; g1.lda = H; g1.a_rows = T;
+            g1.B = tptr(c, seg, 0); g1.ldb = H; g1.b_rows = 2 * (int64_t)F;
+            g1.b2_row_off = F;
+            g1.M = T; g1.N = F; g1.K = H;
+            g1.C = c->hbuf; g1.ldc = F;
+            {
+                KTime kt(c, "gemm_up", rc.s);
+                track(c, launch_gemm_bf16(g1, ctas, rc.s));
+            }
+            GemmDesc g2;
+            g2.epi = EPI_RESID;
+            g2.A = c->hbuf; g2.lda = F; g2.a_rows = T;
+            g2.B = tptr(c, seg, 2); g2.ldb = F; g2.b_rows = H;
+            g2.resid = xin; g2.ldr = H;
+            g2.M = T; g2.N = H; g2.K = F;
+            g2.C = xout; g2.ldc = H;
+            KTime kt(c, "gemm_down", rc.s);
+            track(c, launch_gemm_bf16(g2, ctas, rc.s));
+            break;
+        }
+        case LS_KIND_MOE_SWIGLU_BF16: {
+            const int k = c->top_k, E = c->E;
+            const int rows = T * k;
+            const int* table = c->moe_table + (int64_t)seg * rows;
+            const int* bounds = c->moe_bounds + (int64_t)seg * (E + 1);
+            {
+                KTime kt(c, "moe_gather", rc.s);
+                track(c, launch_moe_gather(xin, table, rows, k, H, c->moe_xs, rc.s));
+            }
+            const int64_t eb = c->segs[seg].slot_bytes / E;  // bytes per expert (G, U, D packed)
+            const void* base = c->seg_ptr[seg];
+            GemmDesc g1 = w0;
+            g1.epi = EPI_SWIGLU;
+            g1.A = c->moe_xs; g1.lda = H; g1.a_rows = rows;
+            g1.B = base; g1.ldb = H; g1.b_rows = c->segs[seg].slot_bytes / (2 * (int64_t)H);
+            g1.b2_row_off = F;
+            g1.M = rows; g1.N = F; g1.K = H;
+            g1.C = c->moe_hs; g1.ldc = F;
+            g1.group_bounds = bounds; g1.n_groups = E;
+            g1.b_group_stride_rows = (int)(eb / (2 * (int64_t)H));
+            g1.b_base_row = 0;
+            {
+                KTime kt(c, "gemm_up", rc.s);
+                track(c, launch_gemm_bf16(g1, ctas, rc.s));
+            }
+            GemmDesc g2;
+            g2.epi = EPI_SCALE_F32;
+            g2.A = c->moe_hs; g2.lda = F; g2.a_rows = rows;
+            g2.B = base; g2.ldb = F; g2.b_rows = c->segs[seg].slot_bytes / (2 * (int64_t)F);
+            g2.M = rows; g2.N = H; g2.K = F;
+            g2.C = c->moe_y; g2.ldc = H;
+            g2.group_bounds = bounds; g2.n_groups = E;
+            g2.b_group_stride_rows = (int)(eb / (2 * (int64_t)F));
+            g2.b_base_row = (int)(2 * (int64_t)F * H * 2 / (2 * (int64_t)F));
+            g2.row_table = table;
+            g2.row_weight = c->moe_w + (int64_t)seg * rows;
+            {
+                KTime kt(c, "gemm_down", rc.s);
+                track(c, launch_gemm_bf16(g2, ctas, rc.s));
+            }
+            KTime kt(c, "moe_combine", rc.s);
+            track(c, launch_moe_combine(xin, c->moe_y, T, k, H, xout, rc.s));
+            break;
+        }
+    }
+}
+
+// --------------------------------------------------------------------------- executors
+struct GpuExec : Executor {
+    ls_ctx* c;
+    RunCtx rc;
+    explicit GpuExec(ls_ctx* ctx) : c(ctx) { rc = RunCtx{nullptr, nullptr, 0, nullptr, 0}; }
+
+    bool alloc_shared(int64_t bytes) override {
+        c->shared_dev = dev_alloc(c, (size_t)bytes, c->copy_stream);
+        return c->shared_dev != nullptr;
+    }
+    bool alloc_pool(int slots, int64_t slot_bytes) override {
+        c->pool = dev_alloc(c, (size_t)(slots * slot_bytes), c->copy_stream);
+        c->pool_bytes = slots * slot_bytes;
+        return c->pool != nullptr;
+    }
+    bool alloc_segment(int seg, int64_t bytes) override {
+        c->seg_buf[seg] = dev_alloc(c, (size_t)bytes, rc.s);
+        return c->seg_buf[seg] != nullptr;
+    }
+    void free_segment(int seg) override {
+        dev_free(c, c->seg_buf[seg], (size_t)c->segs[seg].slot_bytes, rc.s);
+        c->seg_buf[seg] = nullptr;
+    }
+    void begin_run(int) override {}
+    void load_shared(int id) override {
+        for (auto& s : c->shared)
+            if (s.id == id)
+                track(c, cudaMemcpyAsync((uint8_t*)c->shared_dev + s.off, s.host, s.bytes,
+                                         cudaMemcpyHostToDevice, rc.s));
+    }
+    void load(int seg, int slot, int kind, int64_t) override {
+        void* dst = c->prm.use_pool ? (uint8_t*)c->pool + (int64_t)slot * c->sched.plan().S : c->seg_buf[seg];
+        const uint32_t epoch = ++c->slot_epoch[slot];
+        c->seg_epoch[seg] = epoch;
+        c->seg_ptr[seg] = dst;
+        c->seg_slot[seg] = slot;
+        const uint8_t* mask =
+            c->kind == LS_KIND_MOE_SWIGLU_BF16 ? c->moe_used + (int64_t)seg * c->E : nullptr;
+        const bool kern = c->copy_path == LS_COPY_KERNEL;
+        if (kind == LS_EV_PREFETCH) {
+            track(c, cudaStreamWaitEvent(c->copy_stream, c->slot_free[slot], 0));
+            if (!c->prm.use_pool) {  // the buffer was allocated in compute-stream order
+                track(c, cudaEventRecord(c->alloc_event, rc.s));
+                track(c, cudaStreamWaitEvent(c->copy_stream, c->alloc_event, 0));
+            }
+            issue_copy(c, seg, dst, slot, epoch, c->copy_stream, kern, mask);
+        } else {
+            issue_copy(c, seg, dst, slot, epoch, rc.s, kern, mask);
+        }
+    }
+    void activate(int seg, int slot, bool via_queue) override {
+        compute_segment(c, rc, seg, via_queue);
+        track(c, cudaEventRecord(c->slot_free[slot], rc.s));
+    }
+    void evict(int seg, int) override {
+        dev_free(c, c->seg_buf[seg], (size_t)c->segs[seg].slot_bytes, rc.s);
+        c->seg_buf[seg] = nullptr;
+    }
+};
+
+struct DryExec : Executor {
+    bool alloc_shared(int64_t) override { return true; }
+    bool alloc_pool(int, int64_t) override { return true; }
+    bool alloc_segment(int, int64_t) override { return true; }
+    void free_segment(int) override {}
+    void begin_run(int) override {}
+    void load_shared(int) override {}
+    void load(int, int, int, int64_t) override {}
+    void activate(int, int, bool) override {}
+    void evict(int, int) override {}
+};
+
+ls_status check_params(const ls_params* p, ls_params* out, std::string* why) {
+    if (!p) {
+        *why = "params is NULL";
+        return LS_ERR_INVALID_ARG;
+    }
+    if (p->version != LS_PARAMS_VERSION) {
+        *why = "unknown params version";
+        return LS_ERR_VERSION;
+    }
+    if (p->struct_size < MIN_PARAMS_SIZE) {
+        *why = "params struct_size below the minimum";
+        return LS_ERR_VERSION;
+    }
+    ls_params d;
+    ls_params_init(&d);
+    size_t n = std::min<size_t>(p->struct_size, sizeof(ls_params));
+    memcpy(&d, p, n);
+    d.struct_size = sizeof(ls_params);
+    if (d.prefetch_depth < 0) { *why = "prefetch_depth < 0"; return LS_ERR_INVALID_ARG; }
+    if (d.resident_layers < -1) { *why = "resident_layers < -1"; return LS_ERR_INVALID_ARG; }
+    if (d.max_vram_bytes < 0) { *why = "max_vram_bytes < 0"; return LS_ERR_INVALID_ARG; }
+    if (d.use_pool != 0 && d.use_pool != 1) { *why = "use_pool must be 0 or 1"; return LS_ERR_INVALID_ARG; }
+    if (d.wait_limit_ms < 1 || d.wait_limit_ms > 600000) {
+        *why = "wait_limit_ms must be in 1..600000 (device waits are always bounded)";
+        return LS_ERR_INVALID_ARG;
+    }
+    if (d.copy_path < LS_COPY_AUTO || d.copy_path > LS_COPY_ENGINE) { *why = "bad copy_path"; return LS_ERR_INVALID_ARG; }
+    if (d.copy_ctas < 0 || d.test_alloc_cap_bytes < 0 || d.test_drop_publish < 0) {
+        *why = "negative count";
+        return LS_ERR_INVALID_ARG;
+    }
+    if ((d.alloc_fn == nullptr) != (d.free_fn == nullptr)) { *why = "alloc_fn and free_fn go together"; return LS_ERR_INVALID_ARG; }
+    *out = d;
+    return LS_OK;
+}
+
+// Pin and map every host range that is not pinned yet (merged by page).
+ls_status pin_host(ls_ctx* c, std::vector<std::pair<const void*, uint64_t>>& ranges) {
+    const uintptr_t PG = 4096;
+    std::vector<std::pair<uintptr_t, uintptr_t>> todo;
+    for (auto& r : ranges) {
+        if (!r.first || !r.second) continue;
+        cudaPointerAttributes a;
+        if (cudaPointerGetAttributes(&a, r.first) == cudaSuccess && a.type == cudaMemoryTypeHost) continue;
+        cudaGetLastError();
+        uintptr_t b = (uintptr_t)r.first & ~(PG - 1);
+        uintptr_t e = ((uintptr_t)r.first + r.second + PG - 1) & ~(PG - 1);
+        todo.push_back({b, e});
+    }
+    std::sort(todo.begin(), todo.end());
+    std::vector<std::pair<uintptr_t, uintptr_t>> merged;
+    for (auto& r : todo) {
+        if (!merged.empty() && r.first <= merged.back().second)
+            merged.back().second = std::max(merged.back().second, r.second);
+        else
+            merged.push_back(r);
+    }
+    for (auto& r : merged) {
+        cudaError_t e = cudaHostRegister((void*)r.first, r.second - r.first,
+                                         cudaHostRegisterMapped | cudaHostRegisterPortable);
+        if (e != cudaSuccess) {
+            cudaGetLastError();
+            set_err(c, "cudaHostRegister of %zu bytes failed: %s", (size_t)(r.second - r.first),
+                    cudaGetErrorString(e));
+            return LS_ERR_CUDA;
+        }
+        c->host_registered.push_back({(void*)r.first, r.second - r.first});
+    }
+    return LS_OK;
+}
+
+const void* mapped_ptr(const void* host) {
+    cudaPointerAttributes a;
+    if (cudaPointerGetAttributes(&a, host) != cudaSuccess) {
+        cudaGetLastError();
+        return nullptr;
+    }
+    return a.devicePointer;
+}
+
+ls_status validate_layout(ls_ctx* c) {
+    const int k = c->kind;
+    auto shape_is = [](const TensorRec& t, int64_t a, int64_t b) {
+        return b < 0 ? (t.ndim == 1 && t.shape[0] == a) : (t.ndim == 2 && t.shape[0] == a && t.shape[1] == b);
+    };
+    for (int s = 0; s < c->N; ++s) {
+        const auto& t = c->segs[s].t;
+        bool ok = true;
+        const int dt = k == LS_KIND_LINEAR_GELU_F32 ? LS_DTYPE_F32 : LS_DTYPE_BF16;
+        for (auto& x : t) {
+            ok &= x.dtype == dt;
+            ok &= x.bytes == (uint64_t)(x.shape[0] * (x.ndim == 2 ? x.shape[1] : 1) * (dt == LS_DTYPE_F32 ? 4 : 2));
+        }
+        if (k == LS_KIND_LINEAR_GELU_F32)
+            ok &= t.size() == 2 && t[0].ndim == 2 && shape_is(t[1], t[0].shape[0], -1);
+        else if (k == LS_KIND_FFN_GELU_BF16 || k == LS_KIND_FFN_GELU_SHARED_BF16) {
+            int o = k == LS_KIND_FFN_GELU_SHARED_BF16 ? 1 : 0;
+            ok &= (int)t.size() == 4 + o;
+            if (ok) {
+                int64_t Fh = t[o].shape[0], Hh = t[o].shape[1];
+                ok &= shape_is(t[o + 1], Fh, -1) && shape_is(t[o + 2], Hh, Fh) && shape_is(t[o + 3], Hh, -1);
+                if (o) ok &= shape_is(t[0], Hh, Hh) && t[0].shared_id >= 0;
+                for (int i = o; i < 4 + o; ++i) ok &= t[i].shared_id < 0;
+            }
+        } else if (k == LS_KIND_SWIGLU_BF16) {
+            ok &= t.size() == 3;
+            if (ok) {
+                int64_t Fh = t[0].shape[0], Hh = t[0].shape[1];
+                ok &= shape_is(t[1], Fh, Hh) && shape_is(t[2], Hh, Fh);
+                ok &= t[1].off == t[0].off + (int64_t)t[0].bytes;  // G and U adjacent: one [2F, H] view
+            }
+        } else if (k == LS_KIND_MOE_SWIGLU_BF16) {
+            ok &= t.size() % 3 == 0 && !t.empty() && t.size() / 3 <= 256;
+            if (ok) {
+                int64_t Fh = t[0].shape[0], Hh = t[0].shape[1];
+                int64_t eb = 3 * Fh * Hh * 2;
+                for (size_t e = 0; e < t.size() / 3 && ok; ++e) {
+                    ok &= shape_is(t[3 * e], Fh, Hh) && shape_is(t[3 * e + 1], Fh, Hh) && shape_is(t[3 * e + 2], Hh, Fh);
+                    ok &= t[3 * e].off == (int64_t)e * eb && t[3 * e + 1].off == t[3 * e].off + Fh * Hh * 2 &&
+                          t[3 * e + 2].off == t[3 * e].off + 2 * Fh * Hh * 2;
+                }
+            }
+        } else {
+            ok = false;
+        }
+        if (!ok) {
+            set_err(c, "segment %d: tensors do not match kind %d's layout", s, k);
+            return LS_ERR_UNSUPPORTED;
+        }
+    }
+    // dims of the stack
+    const auto& t0 = c->segs[0].t;
+    if (k == LS_KIND_LINEAR_GELU_F32) {
+        c->F = (int)t0[0].shape[0];
+        c->H = (int)t0[0].shape[1];
+        if (c->F != c->H) {
+            set_err(c, "fp32 linear stack: out features must equal in features");
+            return LS_ERR_UNSUPPORTED;
+        }
+    } else {
+        int o = k == LS_KIND_FFN_GELU_SHARED_BF16 ? 1 : 0;
+        c->F = (int)t0[o].shape[0];
+        c->H = (int)t0[o].shape[1];
+        if (k == LS_KIND_MOE_SWIGLU_BF16) c->E = (int)(t0.size() / 3);
+        if ((c->H % 8) || (c->F % 8)) {
+            set_err(c, "bf16 kinds need hidden and ffn sizes that are multiples of 8");
+            return LS_ERR_UNSUPPORTED;
+        }
+    }
+    for (int s = 1; s < c->N; ++s) {
+        int o = k == LS_KIND_FFN_GELU_SHARED_BF16 ? 1 : 0;
+        if (c->segs[s].t.size() != t0.size() || c->segs[s].t[o].shape[0] != t0[o].shape[0] ||
+            c->segs[s].t[o].shape[1] != t0[o].shape[1]) {
+            set_err(c, "segment %d has other dimensions than segment 0", s);
+            return LS_ERR_UNSUPPORTED;
+        }
+    }
+    return LS_OK;
+}
+
+ls_status build_ranges(ls_ctx* c, SegRec& sr) {
+    std::vector<CopyRange> v;
+    int64_t chunk = 0;
+    for (auto& t : sr.t) {
+        if (t.shared_id >= 0) continue;
+        if (((uintptr_t)t.dev & 15) != 0) sr.kernel_ok = false;
+        CopyRange r{};
+        r.src = t.dev;
+        r.dst_off = t.off;
+        r.n16 = (int64_t)(t.bytes / 16);
+        r.tail = (int32_t)(t.bytes % 16);
+        r.chunk_begin = chunk;
+        chunk += std::max<int64_t>(1, copy_chunks_for(r.n16));
+        v.push_back(r);
+    }
+    sr.n_ranges = (int)v.size();
+    sr.n_chunks = chunk;
+    if (v.empty()) return LS_OK;
+    CK(cudaMalloc(&sr.ranges_dev, v.size() * sizeof(CopyRange)));
+    CK(cudaMemcpy(sr.ranges_dev, v.data(), v.size() * sizeof(CopyRange), cudaMemcpyHostToDevice));
+    return LS_OK;
+}
+
+// Time both copy paths on one segment's load (copy stream, into the first slot or a scratch buffer).
+ls_status autotune_copy(ls_ctx* c) {
+    const Plan& p = c->sched.plan();
+    const int M = p.N - p.R;
+    const int forced = c->prm.copy_path;
+    const int seg = p.N - 1;
+    if (M <= 0 || !c->segs[seg].kernel_ok) {  // nothing streamed, or sources not 16-byte aligned
+        c->copy_path = (forced == LS_COPY_KERNEL && c->segs[seg].kernel_ok) ? LS_COPY_KERNEL : LS_COPY_ENGINE;
+        return LS_OK;
+    }
+    void* dst = c->pool;
+    void* scratch = nullptr;
+    if (!dst) {
+        CK(cudaMalloc(&scratch, (size_t)c->segs[seg].slot_bytes));
+        dst = scratch;
+    }
+    if (c->kind == LS_KIND_MOE_SWIGLU_BF16) {  // time with every expert routed
+        CK(cudaMemset(c->moe_used + (int64_t)seg * c->E, 1, c->E));
+        memset(c->moe_used_host + (int64_t)seg * c->E, 1, c->E);
+    }
+    cudaEvent_t e0, e1;
+    CK(cudaEventCreate(&e0));
+    CK(cudaEventCreate(&e1));
+    const uint8_t* mask = c->kind == LS_KIND_MOE_SWIGLU_BF16 ? c->moe_used + (int64_t)seg * c->E : nullptr;
+    double best[2] = {1e30, 1e30};
+    const int saved_drop = c->prm.test_drop_publish;
+    const int saved_timing = c->prm.kernel_timing;
+    c->prm.test_drop_publish = 0;
+    c->prm.kernel_timing = 0;
+    for (int path = 0; path < 2; ++path) {
+        for (int rep = 0; rep < 4; ++rep) {
+            CK(cudaEventRecord(e0, c->copy_stream));
+            issue_copy(c, seg, dst, 0, 0x80000000u + rep, c->copy_stream, path == 0, mask);
+            CK(cudaEventRecord(e1, c->copy_stream));
+            CK(cudaEventSynchronize(e1));
+            float ms = 0;
+            CK(cudaEventElapsedTime(&ms, e0, e1));
+            if (rep > 0) best[path] = std::min(best[path], (double)ms);
+        }
+    }
+    c->prm.test_drop_publish = saved_drop;
+    c->prm.kernel_timing = saved_timing;
+    CK(c->cuda_err);
+    CK(cudaMemsetAsync(c->ready, 0, sizeof(uint32_t) * std::max(1, p.P), c->copy_stream));
+    CK(cudaStreamSynchronize(c->copy_stream));
+    cudaEventDestroy(e0);
+    cudaEventDestroy(e1);
+    if (scratch) cudaFree(scratch);
+    const double bytes = (double)c->segs[seg].load_bytes;
+    c->gbs_kernel = bytes / (best[0] * 1e-3) / 1e9;
+    c->gbs_engine = bytes / (best[1] * 1e-3) / 1e9;
+    c->copy_path = forced != LS_COPY_AUTO ? forced : (best[0] <= best[1] ? LS_COPY_KERNEL : LS_COPY_ENGINE);
+    return LS_OK;
+}
+
+ls_status ensure_workspace(ls_ctx* c, int64_t T) {
+    if (T <= c->ws_tokens) return LS_OK;
+    cudaDeviceSynchronize();
+    for (void** p : {&c->act[0], &c->act[1], &c->hbuf, &c->ubuf, &c->moe_xs, &c->moe_hs})
+        if (*p) { cudaFree(*p); *p = nullptr; }
+    for (void* p : {(void*)c->moe_sel, (void*)c->moe_w, (void*)c->moe_table, (void*)c->moe_y})
+        if (p) cudaFree(p);
+    c->moe_sel = nullptr; c->moe_w = nullptr; c->moe_table = nullptr; c->moe_y = nullptr;
+    const size_t es = c->kind == LS_KIND_LINEAR_GELU_F32 ? 4 : 2;
+    if (c->N > 1) {
+        CK(cudaMalloc(&c->act[0], (size_t)T * c->H * es));
+        CK(cudaMalloc(&c->act[1], (size_t)T * c->H * es));
+    }
+    if (c->kind == LS_KIND_FFN_GELU_BF16 || c->kind == LS_KIND_FFN_GELU_SHARED_BF16 || c->kind == LS_KIND_SWIGLU_BF16)
+        CK(cudaMalloc(&c->hbuf, (size_t)T * c->F * 2));
+    if (c->kind == LS_KIND_FFN_GELU_SHARED_BF16) CK(cudaMalloc(&c->ubuf, (size_t)T * c->H * 2));
+    if (c->kind == LS_KIND_MOE_SWIGLU_BF16) {
+        const int64_t rows = T * 8;
+        CK(cudaMalloc(&c->moe_sel, (size_t)c->N * rows * sizeof(int)));
+        CK(cudaMalloc(&c->moe_w, (size_t)c->N * rows * sizeof(float)));
+        CK(cudaMalloc(&c->moe_table, (size_t)c->N * rows * sizeof(int)));
+        CK(cudaMalloc(&c->moe_xs, (size_t)rows * c->H * 2));
+        CK(cudaMalloc(&c->moe_hs, (size_t)rows * c->F * 2));
+        CK(cudaMalloc(&c->moe_y, (size_t)rows * c->H * sizeof(float)));
+    }
+    c->ws_tokens = T;
+    return LS_OK;
+}
+
+}  // namespace
+
+// =========================================================================== C ABI
+extern "C" {
+
+void ls_params_init(ls_params* p) {
+    if (!p) return;
+    memset(p, 0, sizeof(*p));
+    p->struct_size = sizeof(ls_params);
+    p->version = LS_PARAMS_VERSION;
+    p->prefetch_depth = 0;
+    p->resident_layers = -1;
+    p->max_vram_bytes = 0;
+    p->use_pool = 0;
+    p->wait_limit_ms = 30000;
+    p->copy_path = LS_COPY_AUTO;
+    p->copy_ctas = 0;
+    p->reserve_sms = -1;
+    p->device = -1;
+}
+
+const char* ls_status_string(ls_status s) {
+    switch (s) {
+        case LS_OK: return "ok";
+        case LS_WARN_MANDATORY_SLOT: return "warning: budget below one slot, mandatory one-slot pool used";
+        case LS_WARN_SYNC_FALLBACK: return "warning: asynchronous prefetch unavailable, continued synchronously";
+        case LS_ERR_INVALID_ARG: return "invalid argument";
+        case LS_ERR_VERSION: return "unsupported params version or struct size";
+        case LS_ERR_OOM: return "out of device memory (not even one slot)";
+        case LS_ERR_HANDOFF_TIMEOUT: return "hand-off wait timed out (ready word stayed down)";
+        case LS_ERR_CUDA: return "CUDA error";
+        case LS_ERR_STATE: return "call out of order";
+        case LS_ERR_UNSUPPORTED: return "unsupported shape, kind or alignment";
+    }
+    return "unknown status";
+}
+
+const char* ls_last_error(const ls_ctx* ctx) { return ctx ? ctx->err.c_str() : "null context"; }
+
+ls_status ls_ctx_create(const ls_params* params, ls_ctx** out) {
+    if (!out) return LS_ERR_INVALID_ARG;
+    *out = nullptr;
+    ls_params p;
+    std::string why;
+    ls_status st = check_params(params, &p, &why);
+    if (st != LS_OK) return st;
+    ls_ctx* c = new ls_ctx();
+    c->prm = p;
+    *out = c;
+    return LS_OK;
+}
+
+ls_status ls_register_segments(ls_ctx* c, const ls_segment_desc* segs, int32_t n, const ls_shared_ref* shared_map,
+                               int32_t n_shared) {
+    if (!c) return LS_ERR_INVALID_ARG;
+    if (c->registered) {
+        set_err(c, "segments are already registered");
+        return LS_ERR_STATE;
+    }
+    if (!segs || n < 1 || (n_shared > 0 && !shared_map) || n_shared < 0) {
+        set_err(c, "bad segment list");
+        return LS_ERR_INVALID_ARG;
+    }
+    if (c->prm.device >= 0) CK(cudaSetDevice(c->prm.device));
+    CK(cudaGetDevice(&c->device));
+    c->N = n;
+    c->kind = segs[0].kind;
+    c->segs.assign(n, SegRec());
+    std::vector<std::pair<const void*, uint64_t>> host_ranges;
+    for (int s = 0; s < n; ++s) {
+        if (segs[s].kind != c->kind || segs[s].n_tensors < 1 || !segs[s].tensors) {
+            set_err(c, "segment %d: bad kind or tensor list", s);
+            return LS_ERR_INVALID_ARG;
+        }
+        for (int i = 0; i < segs[s].n_tensors; ++i) {
+            const ls_tensor_desc& d = segs[s].tensors[i];
+            if (!d.host_ptr || d.bytes == 0 || d.ndim < 1 || d.ndim > 2) {
+                set_err(c, "segment %d tensor %d: bad descriptor", s, i);
+                return LS_ERR_INVALID_ARG;
+            }
+            TensorRec t;
+            t.host = d.host_ptr;
+            t.bytes = d.bytes;
+            t.dtype = d.dtype;
+            t.ndim = d.ndim;
+            t.shape[0] = d.shape[0];
+            t.shape[1] = d.ndim == 2 ? d.shape[1] : 1;
+            c->segs[s].t.push_back(t);
+            host_ranges.push_back({d.host_ptr, d.bytes});
+        }
+    }
+    for (int i = 0; i < n_shared; ++i) {
+        const ls_shared_ref& r = shared_map[i];
+        if (r.segment < 0 || r.segment >= n || r.tensor_index < 0 ||
+            r.tensor_index >= (int)c->segs[r.segment].t.size() || r.shared_id < 0) {
+            set_err(c, "shared map entry %d out of range", i);
+            return LS_ERR_INVALID_ARG;
+        }
+        c->segs[r.segment].t[r.tensor_index].shared_id = r.shared_id;
+    }
+    // dedup shared tensors by id (the first occurrence is the copy that is loaded)
+    std::map<int, SharedRec> sh;
+    for (int s = 0; s < n; ++s)
+        for (auto& t : c->segs[s].t) {
+            if (t.shared_id < 0) continue;
+            auto it = sh.find(t.shared_id);
+            if (it == sh.end()) {
+                sh[t.shared_id] = SharedRec{t.shared_id, t.host, nullptr, t.bytes, 0};
+            } else if (it->second.bytes != t.bytes) {
+                set_err(c, "shared id %d registered with two sizes", t.shared_id);
+                return LS_ERR_INVALID_ARG;
+            }
+        }
+    int64_t off = 0;
+    for (auto& kv : sh) {
+        kv.second.off = off;
+        off += align_up((int64_t)kv.second.bytes);
+        c->shared.push_back(kv.second);
+    }
+    for (int s = 0; s < n; ++s) {
+        int64_t o = 0, lb = 0;
+        for (auto& t : c->segs[s].t) {
+            if (t.shared_id >= 0) {
+                t.off = sh[t.shared_id].off;
+                continue;
+            }
+            t.off = o;
+            o += align_up((int64_t)t.bytes);
+            lb += (int64_t)t.bytes;
+        }
+        c->segs[s].slot_bytes = o;
+        c->segs[s].load_bytes = lb;
+        if (o == 0) {
+            set_err(c, "segment %d has no private parameters", s);
+            return LS_ERR_INVALID_ARG;
+        }
+    }
+    ls_status st = validate_layout(c);
+    if (st != LS_OK) return st;
+    st = pin_host(c, host_ranges);
+    if (st != LS_OK) return st;
+    for (int s = 0; s < n; ++s)
+        for (auto& t : c->segs[s].t) {
+            t.dev = mapped_ptr(t.host);
+            if (!t.dev) {
+                set_err(c, "segment %d: host memory is not device-mapped", s);
+                return LS_ERR_CUDA;
+            }
+        }
+    for (auto& s : c->shared) s.dev = mapped_ptr(s.host);
+    for (auto& s : c->segs) {
+        st = build_ranges(c, s);
+        if (st != LS_OK) return st;
+    }
+    // streams, words, events
+    CK(cudaStreamCreateWithFlags(&c->copy_stream, cudaStreamNonBlocking));
+    CK(cudaEventCreateWithFlags(&c->alloc_event, cudaEventDisableTiming));
+    CK(cudaEventCreateWithFlags(&c->run_done, cudaEventDisableTiming));
+    CK(cudaHostAlloc((void**)&c->err_word, sizeof(uint32_t), cudaHostAllocMapped | cudaHostAllocPortable));
+    *c->err_word = 0;
+    CK(cudaHostGetDevicePointer((void**)&c->err_word_dev, c->err_word, 0));
+    std::vector<int64_t> seg_slot(n);
+    for (int s = 0; s < n; ++s) seg_slot[s] = c->segs[s].slot_bytes;
+    std::vector<std::pair<int, int64_t>> shared_bytes;
+    for (auto& s : c->shared) shared_bytes.push_back({s.id, (int64_t)s.bytes});
+    c->sched.configure(c->prm, seg_slot, shared_bytes);
+    GpuExec ex(c);
+    ls_status plan_st = c->sched.register_memory(ex);
+    if (plan_st < 0) {
+        set_err(c, "could not allocate the parameter memory (not even one slot)");
+        return plan_st;
+    }
+    const Plan& p = c->sched.plan();
+    const int P = std::max(1, p.P);
+    CK(cudaMalloc(&c->ready, sizeof(uint32_t) * P));
+    CK(cudaMalloc(&c->tickets, sizeof(uint32_t) * P));
+    CK(cudaMemset(c->ready, 0, sizeof(uint32_t) * P));
+    CK(cudaMemset(c->tickets, 0, sizeof(uint32_t) * P));
+    c->slot_epoch.assign(P, 0);
+    c->slot_free.assign(P, nullptr);
+    for (int i = 0; i < P; ++i) CK(cudaEventCreateWithFlags(&c->slot_free[i], cudaEventDisableTiming));
+    c->seg_buf.assign(n, nullptr);
+    c->seg_epoch.assign(n, 0);
+    c->seg_ptr.assign(n, nullptr);
+    c->seg_slot.assign(n, 0);
+    if (c->kind == LS_KIND_MOE_SWIGLU_BF16) {
+        CK(cudaMalloc(&c->moe_bounds, sizeof(int) * (size_t)n * (c->E + 1)));
+        CK(cudaMalloc(&c->moe_used, (size_t)n * c->E));
+        CK(cudaHostAlloc((void**)&c->moe_used_host, (size_t)n * c->E, cudaHostAllocDefault));
+        memset(c->moe_used_host, 1, (size_t)n * c->E);
+    }
+    const int sms = gemm_num_sms();
+    c->copy_ctas = c->prm.copy_ctas > 0 ? c->prm.copy_ctas : sms;
+    c->reserve_sms = c->prm.reserve_sms >= 0 ? c->prm.reserve_sms : 0;
+    CK(cudaStreamSynchronize(c->copy_stream));
+    st = autotune_copy(c);
+    if (st != LS_OK) return st;
+    if (c->cuda_err != cudaSuccess) {
+        set_err(c, "registration: %s", cudaGetErrorString(c->cuda_err));
+        return LS_ERR_CUDA;
+    }
+    c->registered = true;
+    return plan_st;
+}
+
+ls_status ls_run_async(ls_ctx* c, const void* x_dev, void* y_dev, int64_t tokens, void* stream,
+                       const ls_moe_routing* routing) {
+    if (!c) return LS_ERR_INVALID_ARG;
+    if (!c->registered) {
+        set_err(c, "ls_run before ls_register_segments");
+        return LS_ERR_STATE;
+    }
+    if (!x_dev || !y_dev || tokens < 1 || tokens > (1 << 24) || x_dev == y_dev) {
+        set_err(c, "bad run arguments");
+        return LS_ERR_INVALID_ARG;
+    }
+    const bool moe = c->kind == LS_KIND_MOE_SWIGLU_BF16;
+    if (moe && (!routing || !routing->logits || routing->top_k < 1 || routing->top_k > 8 ||
+                routing->top_k > c->E)) {
+        set_err(c, "the MoE kind needs routing logits and 1 <= top_k <= min(8, experts)");
+        return LS_ERR_INVALID_ARG;
+    }
+    if ((int64_t)tokens * (moe ? routing->top_k : 1) > (int64_t)INT32_MAX / 4) {
+        set_err(c, "too many tokens");
+        return LS_ERR_INVALID_ARG;
+    }
+    CK(cudaSetDevice(c->device));
+    cudaStream_t s = (cudaStream_t)stream;
+    if (tokens > c->ws_tokens) {
+        ls_status sy = ls_sync(c);  // workspaces are about to be replaced
+        if (sy < 0) return sy;
+    }
+    ls_status st = ensure_workspace(c, tokens);
+    if (st != LS_OK) return st;
+    if (std::find(c->pending.begin(), c->pending.end(), s) == c->pending.end()) c->pending.push_back(s);
+    CK(cudaStreamWaitEvent(s, c->run_done, 0));  // passes share workspaces: keep them in order
+    std::vector<int64_t> load_bytes(c->N);
+    for (int i = 0; i < c->N; ++i) load_bytes[i] = c->segs[i].load_bytes;
+    if (moe) {
+        c->top_k = routing->top_k;
+        const int E = c->E, k = c->top_k;
+        {
+            KTime kt(c, "moe_route_group", s);
+            CK(launch_moe_route(routing->logits, c->N, (int)tokens, E, k, c->moe_sel, c->moe_w, s));
+            CK(launch_moe_group(c->moe_sel, c->N, (int)tokens, E, k, c->moe_table, c->moe_bounds, c->moe_used, s));
+        }
+        CK(cudaMemcpyAsync(c->moe_used_host, c->moe_used, (size_t)c->N * E, cudaMemcpyDeviceToHost, s));
+        CK(cudaStreamSynchronize(s));
+        const int64_t eb = c->segs[0].slot_bytes / E;
+        for (int l = 0; l < c->N; ++l) {
+            int64_t used = 0;
+            for (int e = 0; e < E; ++e) used += c->moe_used_host[(int64_t)l * E + e];
+            load_bytes[l] = used * eb;
+        }
+    }
+    GpuExec ex(c);
+    ex.rc = RunCtx{x_dev, y_dev, tokens, s, (uint64_t)c->prm.wait_limit_ms * 1000000ull};
+    ls_status rs = c->sched.run(ex, load_bytes.data());
+    track(c, cudaEventRecord(c->run_done, s));
+    if (rs < 0) set_err(c, "run %d: %s", c->sched.runs() - 1, ls_status_string(rs));
+    return rs;
+}
+
+ls_status ls_sync(ls_ctx* c) {
+    if (!c) return LS_ERR_INVALID_ARG;
+    if (!c->registered) return LS_OK;
+    CK(cudaSetDevice(c->device));
+    cudaError_t e = cudaSuccess;
+    for (cudaStream_t s : c->pending) {
+        cudaError_t e1 = cudaStreamSynchronize(s);
+        if (e == cudaSuccess) e = e1;
+    }
+    cudaError_t e2 = cudaStreamSynchronize(c->copy_stream);
+    if (e == cudaSuccess) e = e2;
+    c->pending.clear();
+    if (c->prm.kernel_timing) collect_times(c);
+    if (e == cudaSuccess) e = c->cuda_err;
+    c->cuda_err = cudaSuccess;
+    const uint32_t ew = *(volatile uint32_t*)c->err_word;
+    *(volatile uint32_t*)c->err_word = 0;
+    if (e != cudaSuccess) {
+        set_err(c, "run %d: %s", c->sched.runs() - 1, cudaGetErrorString(e));
+        return LS_ERR_CUDA;
+    }
+    if (ew != 0) {
+        if ((ew & 0xff) == DERR_HANDOFF_TIMEOUT) {
+            set_err(c, "run %d: the ready word of slot %u stayed down for %d ms", c->sched.runs() - 1, ew >> 8,
+                    c->prm.wait_limit_ms);
+            return LS_ERR_HANDOFF_TIMEOUT;
+        }
+        set_err(c, "run %d: device error word 0x%x", c->sched.runs() - 1, ew);
+        return LS_ERR_CUDA;
+    }
+    return LS_OK;
+}
+
+ls_status ls_run(ls_ctx* c, const void* x_dev, void* y_dev, int64_t tokens, void* stream,
+                 const ls_moe_routing* routing) {
+    ls_status st = ls_run_async(c, x_dev, y_dev, tokens, stream, routing);
+    ls_status sy = c ? ls_sync(c) : LS_ERR_INVALID_ARG;
+    if (st < 0) return st;
+    if (sy < 0) return sy;
+    return st;
+}
+
+ls_status ls_run_host(ls_ctx* c, const void* x_host, void* y_host, int64_t tokens, const ls_moe_routing* routing_host) {
+    if (!c) return LS_ERR_INVALID_ARG;
+    if (!c->registered) {
+        set_err(c, "ls_run_host before ls_register_segments");
+        return LS_ERR_STATE;
+    }
+    if (!x_host || !y_host || tokens < 1) {
+        set_err(c, "bad run arguments");
+        return LS_ERR_INVALID_ARG;
+    }
+    const bool moe = c->kind == LS_KIND_MOE_SWIGLU_BF16;
+    if (moe && (!routing_host || !routing_host->logits)) {
+        set_err(c, "the MoE kind needs routing logits");
+        return LS_ERR_INVALID_ARG;
+    }
+    CK(cudaSetDevice(c->device));
+    if (!c->own_stream) CK(cudaStreamCreateWithFlags(&c->own_stream, cudaStreamNonBlocking));
+    const size_t es = c->kind == LS_KIND_LINEAR_GELU_F32 ? 4 : 2;
+    const size_t xb = (size_t)tokens * c->H * es;
+    if (tokens > c->stage_tokens) {
+        ls_status sy = ls_sync(c);
+        if (sy < 0) return sy;
+        if (c->stage_x) cudaFree(c->stage_x);
+        if (c->stage_y) cudaFree(c->stage_y);
+        if (c->stage_logits) cudaFree(c->stage_logits);
+        c->stage_x = c->stage_y = nullptr;
+        c->stage_logits = nullptr;
+        CK(cudaMalloc(&c->stage_x, xb));
+        CK(cudaMalloc(&c->stage_y, xb));
+        if (moe) CK(cudaMalloc((void**)&c->stage_logits, (size_t)c->N * tokens * c->E * sizeof(float)));
+        c->stage_tokens = tokens;
+    }
+    CK(cudaMemcpyAsync(c->stage_x, x_host, xb, cudaMemcpyHostToDevice, c->own_stream));
+    ls_moe_routing r{};
+    if (moe) {
+        CK(cudaMemcpyAsync(c->stage_logits, routing_host->logits, (size_t)c->N * tokens * c->E * sizeof(float),
+                           cudaMemcpyHostToDevice, c->own_stream));
+        r.logits = c->stage_logits;
+        r.top_k = routing_host->top_k;
+    }
+    ls_status st = ls_run(c, c->stage_x, c->stage_y, tokens, c->own_stream, moe ? &r : nullptr);
+    if (st < 0) return st;
+    CK(cudaMemcpyAsync(y_host, c->stage_y, xb, cudaMemcpyDeviceToHost, c->own_stream));
+    CK(cudaStreamSynchronize(c->own_stream));
+    return st;
+}
+
+ls_status ls_get_schedule(ls_ctx* c, ls_sched_event* out, int64_t cap, int64_t* n_out) {
+    if (!c || !n_out || cap < 0 || (cap > 0 && !out)) return LS_ERR_INVALID_ARG;
+    const auto& log = c->sched.log();
+    *n_out = (int64_t)log.size();
+    const int64_t n = std::min<int64_t>(cap, (int64_t)log.size());
+    if (n > 0) memcpy(out, log.data(), sizeof(ls_sched_event) * n);
+    return LS_OK;
+}
+
+ls_status ls_get_stats(ls_ctx* c, ls_stats* out) {
+    if (!c || !out || out->struct_size < offsetof(ls_stats, slot_bytes)) return LS_ERR_INVALID_ARG;
+    ls_stats s;
+    memset(&s, 0, sizeof(s));
+    s.struct_size = sizeof(s);
+    if (c->registered || c->sched.plan().N > 0) c->sched.fill_stats(s);
+    s.copy_path = c->copy_path;
+    s.copy_kernel_gbs = c->gbs_kernel;
+    s.copy_engine_gbs = c->gbs_engine;
+    const uint32_t n = std::min<uint32_t>(out->struct_size, sizeof(s));
+    memcpy(out, &s, n);
+    out->struct_size = n;
+    return LS_OK;
+}
+
+ls_status ls_get_kernel_times(ls_ctx* c, ls_kernel_time* out, int32_t cap, int32_t* n_out, int32_t reset) {
+    if (!c || !n_out || cap < 0 || (cap > 0 && !out)) return LS_ERR_INVALID_ARG;
+    *n_out = (int32_t)c->tclass.size();
+    for (int32_t i = 0; i < cap && i < (int32_t)c->tclass.size(); ++i) {
+        memset(&out[i], 0, sizeof(out[i]));
+        snprintf(out[i].name, sizeof(out[i].name), "%s", c->tclass[i].name.c_str());
+        out[i].launches = c->tclass[i].launches;
+        out[i].total_ms = c->tclass[i].total_ms;
+    }
+    if (reset)
+        for (auto& t : c->tclass) {
+            t.launches = 0;
+            t.total_ms = 0;
+        }
+    return LS_OK;
+}
+
+void ls_ctx_destroy(ls_ctx* c) {
+    if (!c) return;
+    if (c->N > 0) {
+        cudaSetDevice(c->device);
+        cudaDeviceSynchronize();
+        for (int s = 0; s < (int)c->seg_buf.size(); ++s)
+            if (c->seg_buf[s]) dev_free(c, c->seg_buf[s], (size_t)c->segs[s].slot_bytes, c->copy_stream);
+        if (c->pool) dev_free(c, c->pool, (size_t)c->pool_bytes, c->copy_stream);
+        if (c->shared_dev) dev_free(c, c->shared_dev, 0, c->copy_stream);
+        if (c->copy_stream) cudaStreamSynchronize(c->copy_stream);
+        for (auto& sr : c->segs)
+            if (sr.ranges_dev) cudaFree(sr.ranges_dev);
+        for (void* p : {(void*)c->ready, (void*)c->tickets, c->act[0], c->act[1], c->hbuf, c->ubuf,
+                        (void*)c->moe_sel, (void*)c->moe_w, (void*)c->moe_table, (void*)c->moe_bounds,
+                        (void*)c->moe_used, c->moe_xs, c->moe_hs, (void*)c->moe_y, c->stage_x, c->stage_y,
+                        (void*)c->stage_logits})
+            if (p) cudaFree(p);
+        if (c->moe_used_host) cudaFreeHost(c->moe_used_host);
+        if (c->err_word) cudaFreeHost(c->err_word);
+        for (auto e : c->slot_free)
+            if (e) cudaEventDestroy(e);
+        for (auto& e : c->tev) {
+            cudaEventDestroy(e.first);
+            cudaEventDestroy(e.second);
+        }
+        if (c->alloc_event) cudaEventDestroy(c->alloc_event);
+        if (c->run_done) cudaEventDestroy(c->run_done);
+        if (c->copy_stream) cudaStreamDestroy(c->copy_stream);
+        if (c->own_stream) cudaStreamDestroy(c->own_stream);
+        for (auto& r : c->host_registered) cudaHostUnregister(r.first);
+        cudaGetLastError();
+    }
+    delete c;
+}
+
+ls_status ls_simulate(const ls_params* params, const int64_t* seg_slot_bytes, int32_t n, const int64_t* shared_bytes,
+                      const int32_t* shared_ids, int32_t n_shared, int32_t runs, const int64_t* load_bytes,
+                      ls_sched_event* events, int64_t cap, int64_t* n_events, ls_stats* stats,
+                      ls_status* run_status) {
+    ls_params p;
+    std::string why;
+    ls_status st = check_params(params, &p, &why);
+    if (st != LS_OK) return st;
+    if (!seg_slot_bytes || n < 1 || runs < 0 || (n_shared > 0 && (!shared_bytes || !shared_ids)) || !n_events ||
+        (cap > 0 && !events))
+        return LS_ERR_INVALID_ARG;
+    std::vector<int64_t> seg(seg_slot_bytes, seg_slot_bytes + n);
+    for (int64_t b : seg)
+        if (b <= 0) return LS_ERR_INVALID_ARG;
+    std::vector<std::pair<int, int64_t>> sh;
+    for (int i = 0; i < n_shared; ++i) sh.push_back({shared_ids[i], shared_bytes[i]});
+    Scheduler sched;
+    sched.configure(p, seg, sh);
+    DryExec ex;
+    ls_status reg = sched.register_memory(ex);
+    if (reg >= 0) {
+        for (int r = 0; r < runs; ++r) {
+            ls_status rs = sched.run(ex, load_bytes ? load_bytes + (int64_t)r * n : nullptr);
+            if (run_status) run_status[r] = rs;
+        }
+    }
+    const auto& log = sched.log();
+    *n_events = (int64_t)log.size();
+    const int64_t m = std::min<int64_t>(cap, (int64_t)log.size());
+    if (m > 0) memcpy(events, log.data(), sizeof(ls_sched_event) * m);
+    if (stats) {
+        if (stats->struct_size < offsetof(ls_stats, slot_bytes)) return LS_ERR_INVALID_ARG;
+        ls_stats s;
+        memset(&s, 0, sizeof(s));
+        if (reg >= 0) sched.fill_stats(s);
+        s.copy_path = LS_COPY_AUTO;
+        const uint32_t sz = std::min<uint32_t>(stats->struct_size, sizeof(s));
+        memcpy(stats, &s, sz);
+        stats->struct_size = sz;
+    }
+    return reg;
+}
+
+}  // extern "C"

@@ -1,0 +1,103 @@
+/*
+ * ls_kernels.h — the library's device kernels as standalone C entry points.
+ *
+ * ls_run drives these kernels itself; these entry points exist so that each
+ * kernel can be checked and timed alone, in the launch configuration ls_run
+ * uses. All pointers named *_dev are device memory on the current device;
+ * `stream` is a cudaStream_t passed as void* (NULL = legacy default stream).
+ * Calls are asynchronous: they return once the work is queued. Return values
+ * are ls_status codes from ls_api.h (LS_ERR_INVALID_ARG for shapes or
+ * alignments a kernel does not handle, LS_ERR_CUDA for a failed launch).
+ * A bounded wait that expires inside a kernel sets the library's device error
+ * word, read and cleared with lsk_device_error().
+ */
+#ifndef LS_KERNELS_H
+#define LS_KERNELS_H
+
+#include <stdint.h>
+
+#include "ls_api.h"
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+/* GEMM epilogues (C[M,N] = A[M,K] B[N,K]^T, fp32 accumulation, bf16 operands). */
+enum {
+    LSK_EPI_STORE = 0,      /* C = acc -> bf16 */
+    LSK_EPI_BIAS_GELU = 1,  /* C = GELU(acc + bias) -> bf16; GELU(z) = z Phi(z) */
+    LSK_EPI_BIAS_RESID = 2, /* C = acc + bias + R -> bf16 */
+    LSK_EPI_SWIGLU = 3,     /* two B matrices (rows b2_row_off apart): C = SiLU(A Bg^T) * (A Bu^T) -> bf16 */
+    LSK_EPI_RESID = 4,      /* C = acc + R -> bf16 */
+    LSK_EPI_SCALE_F32 = 5   /* grouped only: C[row_table[i]] = row_weight[row_table[i]] * acc -> fp32 */
+};
+
+/* Number of SMs of the current device (the default CTA count of the GEMMs). */
+int32_t lsk_num_sms(void);
+
+/* Read and clear the device error word of the standalone entry points (0 = none). */
+uint32_t lsk_device_error(void);
+
+/* Host-to-device copy with the copy kernel (16-byte loads of mapped pinned host
+ * memory), then ready_dev[0] = epoch after a system fence, raised by the last CTA.
+ * src_host must be pinned (page-locked and mapped) and 16-byte aligned; dst_dev
+ * 16-byte aligned. ticket_dev: one zeroed uint32 the CTAs count on (left at 0).
+ * ctas <= 0: one per SM. "layer split: overlap the stages' hand-off" (publish
+ * order); "prefill: a layer split's idle card streams a share of a one-chunk
+ * prompt's experts", What (16-byte copy kernel). */
+ls_status lsk_copy_h2slot(void* dst_dev, const void* src_host, uint64_t bytes, int32_t ctas,
+                          uint32_t* ready_dev, uint32_t* ticket_dev, uint32_t epoch, void* stream);
+
+/* One thread waits until ready_dev[0] == epoch, at most limit_ms; on expiry it
+ * writes err_host[0] (pinned, mapped host memory) = 1 | (slot << 8) and returns. */
+ls_status lsk_wait_ready(const uint32_t* ready_dev, uint32_t epoch, int32_t limit_ms, uint32_t* err_host,
+                         int32_t slot, void* stream);
+
+/* Dense tcgen05 GEMM with a fused epilogue. A_dev [M,K], B_dev [b_rows,K] (b_rows
+ * >= N, or >= b2_row_off + N for SWIGLU), bias [N], R [M,N], C [M,N]; all bf16
+ * row-major, dense. K and N multiples of 8, pointers 16-byte aligned.
+ * max_ctas <= 0: one CTA per SM. */
+ls_status lsk_gemm_bf16(int32_t epilogue, const void* A_dev, const void* B_dev, int64_t b_rows,
+                        int32_t b2_row_off, const void* bias_dev, const void* resid_dev, void* C_dev,
+                        int32_t M, int32_t N, int32_t K, int32_t max_ctas, void* stream);
+
+/* Grouped (expert) GEMM: rows of A_dev [M,K] are sorted by group;
+ * group g = rows [group_bounds[g], group_bounds[g+1]) multiplies B rows
+ * starting at b_base_row + g * b_group_stride_rows (SWIGLU: second matrix
+ * b2_row_off rows further). Epilogue SWIGLU (C bf16 [M,N], sorted rows) or
+ * SCALE_F32 (C fp32 [*,N] scattered through row_table with row_weight). */
+ls_status lsk_gemm_grouped_bf16(int32_t epilogue, const void* A_dev, const void* B_dev, int64_t b_rows,
+                                int32_t b_base_row, int32_t b_group_stride_rows, int32_t b2_row_off,
+                                const int32_t* group_bounds_dev, int32_t n_groups,
+                                const int32_t* row_table_dev, const float* row_weight_dev, void* C_dev,
+                                int32_t M, int32_t N, int32_t K, int32_t max_ctas, void* stream);
+
+/* y[T,F] = GELU(x[T,H] W[F,H]^T + b[F]), fp32. */
+ls_status lsk_linear_gelu_f32(const float* x_dev, const float* w_dev, const float* b_dev, float* y_dev,
+                              int32_t T, int32_t H, int32_t F, void* stream);
+
+/* Routing of n_layers x T tokens: sel [n_layers,T,k] = top-k expert ids of the
+ * fp32 logits [n_layers,T,E] (larger first, ties to the lower index); weight =
+ * softmax over the k chosen logits (fp32). E <= 256, k <= 8. */
+ls_status lsk_moe_route(const float* logits_dev, int32_t n_layers, int32_t T, int32_t E, int32_t k,
+                        int32_t* sel_dev, float* weight_dev, void* stream);
+
+/* Per layer: stable counting sort of the rows t*k+j by expert -> row_table
+ * [n_layers, T*k], group_bounds [n_layers, E+1], expert_used [n_layers, E]
+ * (may be NULL). */
+ls_status lsk_moe_group(const int32_t* sel_dev, int32_t n_layers, int32_t T, int32_t E, int32_t k,
+                        int32_t* row_table_dev, int32_t* group_bounds_dev, uint8_t* expert_used_dev,
+                        void* stream);
+
+/* x_sorted[i] = x[row_table[i] / k] for i < rows; bf16 rows of H (H % 8 == 0). */
+ls_status lsk_moe_gather(const void* x_dev, const int32_t* row_table_dev, int32_t rows, int32_t k, int32_t H,
+                         void* x_sorted_dev, void* stream);
+
+/* out[t] = x[t] + sum_{j<k} y[t*k + j] (fp32 sum in j order, one bf16 rounding). */
+ls_status lsk_moe_combine(const void* x_dev, const float* y_dev, int32_t T, int32_t k, int32_t H, void* out_dev,
+                          void* stream);
+
+#ifdef __cplusplus
+}
+#endif
+#endif /* LS_KERNELS_H */

@@ -260,3 +260,62 @@ def draw_expert(cfg: StackConfig, layer: int, expert: int):
     """The three tensors (G, U, D) of one expert of one MoE layer."""
     specs = segment_tensors(cfg)[3 * expert:3 * expert + 3]
     return [draw_tensor(cfg, layer, s) for s in specs]
+
+
+# ---------------------------------------------------------------- host layout
+class HostStack:
+    """A whole stack drawn into one page-aligned host buffer.
+
+    Each segment's private tensors sit at 256-byte aligned offsets in the
+    segment's region, in registration order (the same packing as a device
+    slot); the shared tensors follow the last segment. ``segments`` is a list of
+    (kind, [numpy views]) and ``shared_map`` a list of
+    (segment, tensor_index, shared_id), the shapes the C ABI registers.
+    bf16 tensors are uint16 views holding the bit patterns."""
+
+    def __init__(self, cfg: StackConfig, n_segments: int | None = None, threads: int = 0):
+        self.cfg = cfg
+        n = cfg.n_segments if n_segments is None else n_segments
+        specs = segment_tensors(cfg)
+        sh = shared_tensors(cfg)
+        seg_bytes = segment_slot_bytes(cfg)
+        sh_bytes = sum(align256(t.nbytes) for t in sh)
+        total = n * seg_bytes + sh_bytes
+        page = 4096
+        raw = np.empty(total + page, np.uint8)
+        off0 = (-raw.ctypes.data) % page
+        self.buffer = raw[off0:off0 + total]
+        self._raw = raw
+        self.shared_views = []
+        o = n * seg_bytes
+        for t in sh:
+            self.shared_views.append(self._view(o, t))
+            o += align256(t.nbytes)
+        self.seg_views = []
+        jobs = []
+        for s in range(n):
+            o = s * seg_bytes
+            views = []
+            for t in specs:
+                v = self._view(o, t)
+                views.append(v)
+                jobs.append((s, t, v))
+                o += align256(t.nbytes)
+            self.seg_views.append(views)
+        jobs += [(SHARED_SEGMENT_ID, t, v) for t, v in zip(sh, self.shared_views)]
+        threads = threads or (os.cpu_count() or 1)
+        with ThreadPoolExecutor(threads) as ex:
+            list(ex.map(lambda j: draw_tensor(cfg, j[0], j[1], j[2]), jobs))
+        self.segments = []
+        self.shared_map = []
+        for s in range(n):
+            tensors = list(self.seg_views[s])
+            if sh:
+                tensors = list(self.shared_views) + tensors
+                for i in range(len(sh)):
+                    self.shared_map.append((s, i, i))
+            self.segments.append((cfg.kind, tensors))
+
+    def _view(self, off: int, t: TensorSpec) -> np.ndarray:
+        dt = np.float32 if t.dtype == "f32" else np.uint16
+        return self.buffer[off:off + t.nbytes].view(dt).reshape(t.shape)

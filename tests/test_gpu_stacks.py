@@ -1,0 +1,268 @@
+"""Whole streamed stacks through ls_run against the fp64 oracle, with the executed
+schedule against the policy simulator and bit-identity across depth, residency
+and pool settings ("feat: pool VRAM for streamed layer", Verification: zero
+differing channels with and without the pool; "feat: prefetch streamed layers
+during compute", Verification: matching output hashes)."""
+import numpy as np
+import pytest
+import torch
+
+import synth
+from host_offloaded_weight_gb300 import lstream as L
+from oracle import policy
+from oracle import stack as ostack
+
+from gpu_util import BOUND, make_ctx, rel_err, to_f64, x_dev, logits_dev
+
+pytestmark = pytest.mark.gpu
+
+
+def _sim_events(cfg, hs, depth, resident, budget, pool, runs, load=None, **kw):
+    seg = [synth.segment_slot_bytes(cfg)] * len(hs.segments)
+    shared = [(i, v.nbytes) for i, v in enumerate(hs.shared_views)]
+    if load is None:  # a load moves the segment's exact private bytes
+        exact = sum(t.nbytes for t in synth.segment_tensors(cfg))
+        load = [[exact] * len(hs.segments) for _ in range(runs)]
+    sim, st = policy.simulate(seg, shared, depth, resident, budget, use_pool=pool, runs=runs,
+                              load_bytes=load, **kw)
+    return sim, st
+
+
+def _run(cfg, hs, runs=2, logits=None, **over):
+    ctx, st = make_ctx(cfg, hs, **over)
+    try:
+        x = x_dev(cfg)
+        y = torch.empty_like(x)
+        sts = [L.ls_run(ctx, x, y, cfg.tokens, logits=logits, top_k=cfg.top_k) for _ in range(runs)]
+        torch.cuda.synchronize()
+        return y.clone(), L.ls_get_schedule(ctx), L.ls_get_stats(ctx), st, sts
+    finally:
+        L.ls_ctx_destroy(ctx)
+
+
+def _bits(t):
+    return t.view(torch.int16 if t.dtype == torch.bfloat16 else torch.int32).cpu().numpy()
+
+
+# ------------------------------------------------------------------ tiny fp32 stack (full size)
+def test_tiny_fp32_stack_full():
+    cfg = synth.TINY
+    hs = synth.HostStack(cfg)
+    y, ev, stats, st, sts = _run(cfg, hs, runs=3)
+    ref = ostack.stack_forward(cfg)
+    assert rel_err(to_f64(y), ref) <= 1e-5
+    sim, sst = _sim_events(cfg, hs, 1, 0, cfg.max_vram_bytes, 1, 3)
+    assert ev == [tuple(e) for e in sim.events]
+    assert stats["pool_slots"] == 2 and [e[4] for e in ev if e[2] == L.LS_EV_ACTIVATE][:4] == [0, 1, 0, 1]
+    y0, ev0, *_ = _run(cfg, hs, runs=2, prefetch_depth=0)
+    assert np.array_equal(_bits(y0), _bits(y)), "depth 0 and depth 1 must give the same bits"
+
+
+# ------------------------------------------------------------------ small bf16 stacks (full oracle)
+SMALL = {
+    "ffn": synth.DIT.with_(n_segments=5, tokens=300, hidden=256, ffn=520),
+    "proj": synth.SHARED.with_(n_segments=6, tokens=200, hidden=256, ffn=1032),
+    "swiglu": synth.LARGE.with_(n_segments=6, tokens=130, hidden=264, ffn=512),
+}
+
+
+@pytest.mark.parametrize("name", sorted(SMALL))
+def test_small_stacks_all_settings(name):
+    cfg = SMALL[name]
+    hs = synth.HostStack(cfg)
+    S = synth.segment_slot_bytes(cfg)
+    shared_b = sum(synth.align256(v.nbytes) for v in hs.shared_views)
+    ref = ostack.stack_forward(cfg)
+    base = None
+    cases = [(d, r, b, p) for d in (0, 1, 2, 3) for (r, b) in ((0, shared_b + 2 * S), (-1, shared_b + 4 * S), (2, 0))
+             for p in (1, 0)]
+    for depth, resident, budget, pool in cases:
+        y, ev, stats, st, sts = _run(cfg, hs, runs=2, prefetch_depth=depth, resident_layers=resident,
+                                     max_vram_bytes=budget, use_pool=pool)
+        sim, sst = _sim_events(cfg, hs, depth, resident, budget, pool, 2)
+        assert ev == [tuple(e) for e in sim.events], (name, depth, resident, budget, pool)
+        assert sts == sst
+        if base is None:
+            base = _bits(y)
+            assert rel_err(to_f64(y), ref) <= BOUND, rel_err(to_f64(y), ref)
+        else:
+            assert np.array_equal(_bits(y), base), ("bits differ", name, depth, resident, budget, pool)
+
+
+@pytest.mark.parametrize("path", [L.LS_COPY_KERNEL, L.LS_COPY_ENGINE])
+def test_copy_paths_agree(path):
+    cfg = SMALL["ffn"]
+    hs = synth.HostStack(cfg)
+    y, ev, stats, *_ = _run(cfg, hs, copy_path=path,
+                            max_vram_bytes=2 * synth.segment_slot_bytes(cfg), prefetch_depth=1,
+                            resident_layers=0)
+    assert stats["copy_path"] == path
+    y2, *_ = _run(cfg, hs, copy_path=L.LS_COPY_KERNEL if path == L.LS_COPY_ENGINE else L.LS_COPY_ENGINE,
+                  max_vram_bytes=2 * synth.segment_slot_bytes(cfg), prefetch_depth=1, resident_layers=0)
+    assert np.array_equal(_bits(y), _bits(y2))
+
+
+# ------------------------------------------------------------------ full-size stacks, sampled rows
+def _rows(cfg, n=48):
+    return np.sort(np.random.default_rng(1).choice(cfg.tokens, n, replace=False))
+
+
+def test_dit_stack_full_size():
+    cfg = synth.DIT
+    hs = synth.HostStack(cfg)
+    y1, ev1, st1, *_ = _run(cfg, hs, runs=2)
+    rows = _rows(cfg)
+    ref = ostack.stack_forward(cfg, rows=rows)
+    assert rel_err(to_f64(y1)[rows], ref) <= BOUND
+    sim, _ = _sim_events(cfg, hs, 1, 0, cfg.max_vram_bytes, 1, 2)
+    assert ev1 == [tuple(e) for e in sim.events]
+    y0, *_ = _run(cfg, hs, runs=1, prefetch_depth=0)
+    assert np.array_equal(_bits(y0), _bits(y1))
+
+
+def test_shared_projection_stack_full_size():
+    cfg = synth.SHARED
+    hs = synth.HostStack(cfg)
+    rows = _rows(cfg, 32)
+    ref = ostack.stack_forward(cfg, rows=rows)
+    base = None
+    for depth in (0, 1, 2, 3):
+        for pool in (1, 0):
+            y, ev, stats, st, sts = _run(cfg, hs, runs=2, prefetch_depth=depth, use_pool=pool)
+            sim, _ = _sim_events(cfg, hs, depth, -1, cfg.max_vram_bytes, pool, 2)
+            assert ev == [tuple(e) for e in sim.events], (depth, pool)
+            assert stats["residents"] == 13 - depth and stats["pool_slots"] == 14
+            if base is None:
+                base = _bits(y)
+                assert rel_err(to_f64(y)[rows], ref) <= BOUND
+            else:
+                assert np.array_equal(_bits(y), base), (depth, pool)
+
+
+# ------------------------------------------------------------------ faults (host-made, bounded)
+def test_dropped_handoff_times_out_then_recovers():
+    """"layer split: overlap the stages' hand-off", Changes since #936: with the
+    drop hook the Nth publish leaves its flag down; the bounded wait sets the
+    error word, the run fails with a clear error, and the next run is clean."""
+    cfg = SMALL["ffn"].with_(max_vram_bytes=2 * synth.segment_slot_bytes(SMALL["ffn"]))
+    hs = synth.HostStack(cfg)
+    ctx, _ = make_ctx(cfg, hs, test_drop_publish=3, wait_limit_ms=200, copy_path=L.LS_COPY_KERNEL)
+    try:
+        x = x_dev(cfg)
+        y = torch.empty_like(x)
+        with pytest.raises(L.LsError) as e:
+            L.ls_run(ctx, x, y, cfg.tokens)
+        assert e.value.status == L.LS_ERR_HANDOFF_TIMEOUT
+        assert "slot" in L.ls_last_error(ctx)
+        L.ls_run(ctx, x, y, cfg.tokens)
+        torch.cuda.synchronize()
+        assert rel_err(to_f64(y), ostack.stack_forward(cfg)) <= BOUND
+    finally:
+        L.ls_ctx_destroy(ctx)
+
+
+def test_pool_degradation_under_allocator_cap():
+    cfg = SMALL["ffn"]
+    hs = synth.HostStack(cfg)
+    S = synth.segment_slot_bytes(cfg)
+    y_ref, *_ = _run(cfg, hs, max_vram_bytes=0, prefetch_depth=0)
+    y, ev, stats, st, sts = _run(cfg, hs, max_vram_bytes=6 * S, prefetch_depth=1, resident_layers=-1,
+                                 test_alloc_cap_bytes=3 * S)
+    assert stats["pool_slots"] == 3 and stats["pool_degradations"] >= 1 and stats["slot_bytes"] == S
+    sim, _ = _sim_events(cfg, hs, 1, -1, 6 * S, 1, 2, alloc_cap=3 * S)
+    assert ev == [tuple(e) for e in sim.events]
+    assert np.array_equal(_bits(y), _bits(y_ref))
+    with pytest.raises(L.LsError) as e:
+        _run(cfg, hs, max_vram_bytes=6 * S, prefetch_depth=1, test_alloc_cap_bytes=S // 2)
+    assert e.value.status == L.LS_ERR_OOM
+
+
+def test_async_failure_falls_back_synchronously():
+    cfg = SMALL["ffn"]
+    hs = synth.HostStack(cfg)
+    S = synth.segment_slot_bytes(cfg)
+    y_ref, *_ = _run(cfg, hs, max_vram_bytes=0, prefetch_depth=0)
+    y, ev, stats, st, sts = _run(cfg, hs, max_vram_bytes=2 * S, prefetch_depth=1, resident_layers=0,
+                                 test_fail_async=1)
+    assert sts[0] == L.LS_WARN_SYNC_FALLBACK and stats["sync_fallbacks"] == 1
+    assert all(e[2] != L.LS_EV_PREFETCH for e in ev)
+    assert np.array_equal(_bits(y), _bits(y_ref))
+
+
+def test_pool_off_eviction_under_pressure():
+    cfg = SMALL["ffn"].with_(n_segments=6)
+    hs = synth.HostStack(cfg)
+    S = synth.segment_slot_bytes(cfg)
+    y_ref, *_ = _run(cfg, hs, max_vram_bytes=0, prefetch_depth=0)
+    y, ev, stats, st, sts = _run(cfg, hs, runs=3, max_vram_bytes=10 * S, prefetch_depth=1, resident_layers=3,
+                                 use_pool=0, test_alloc_cap_bytes=4 * S)
+    sim, _ = _sim_events(cfg, hs, 1, 3, 10 * S, 0, 3, alloc_cap=4 * S)
+    assert ev == [tuple(e) for e in sim.events]
+    assert stats["evictions"] >= 1
+    assert np.array_equal(_bits(y), _bits(y_ref))
+
+
+def test_mandatory_slot_warning():
+    cfg = SMALL["ffn"]
+    hs = synth.HostStack(cfg)
+    ctx, st = make_ctx(cfg, hs, max_vram_bytes=synth.segment_slot_bytes(cfg) // 3, prefetch_depth=1)
+    try:
+        assert st == L.LS_WARN_MANDATORY_SLOT
+        s = L.ls_get_stats(ctx)
+        assert (s["pool_slots"], s["depth"], s["residents"]) == (1, 0, 0)
+    finally:
+        L.ls_ctx_destroy(ctx)
+
+
+def test_run_host_matches_run():
+    cfg = SMALL["proj"]
+    hs = synth.HostStack(cfg)
+    ctx, _ = make_ctx(cfg, hs, max_vram_bytes=0)
+    try:
+        x = x_dev(cfg)
+        y = torch.empty_like(x)
+        L.ls_run(ctx, x, y, cfg.tokens)
+        xh = x.cpu().pin_memory()
+        yh = torch.empty_like(xh).pin_memory()
+        L.ls_run_host(ctx, xh, yh, cfg.tokens)
+        assert torch.equal(yh.view(torch.int16), y.cpu().view(torch.int16))
+    finally:
+        L.ls_ctx_destroy(ctx)
+
+
+# ------------------------------------------------------------------ MoE
+def _moe_cfg(layers, tokens, experts=128, hidden=2048, ffn=768, k=8):
+    c = synth.MOE.with_(n_segments=layers, tokens=tokens, n_experts=experts, hidden=hidden, ffn=ffn, top_k=k)
+    return c.with_(max_vram_bytes=2 * synth.segment_slot_bytes(c))
+
+
+def test_moe_small_all_rows():
+    cfg = _moe_cfg(3, 200, experts=16, hidden=128, ffn=64, k=4)
+    hs = synth.HostStack(cfg)
+    lg_dev, lg = logits_dev(cfg)
+    y, ev, stats, st, sts = _run(cfg, hs, logits=lg_dev)
+    ref = ostack.stack_forward(cfg)
+    assert rel_err(to_f64(y), ref) <= BOUND
+    eb = synth.segment_slot_bytes(cfg) // cfg.n_experts
+    load = []
+    for _ in range(2):
+        from oracle import forward as F
+        row = []
+        for l in range(cfg.n_segments):
+            sel, _w = F.route_topk(lg[l], cfg.top_k)
+            row.append(len(np.unique(sel)) * eb)
+        load.append(row)
+    sim, _ = _sim_events(cfg, hs, 1, 0, cfg.max_vram_bytes, 1, 2, load=load)
+    assert ev == [tuple(e) for e in sim.events]
+    y0, *_ = _run(cfg, hs, logits=lg_dev, prefetch_depth=0, runs=1)
+    assert np.array_equal(_bits(y0), _bits(y))
+
+
+def test_moe_full_expert_shapes_sampled_rows():
+    cfg = _moe_cfg(4, 2048)
+    hs = synth.HostStack(cfg)
+    lg_dev, _ = logits_dev(cfg)
+    y, ev, stats, st, sts = _run(cfg, hs, logits=lg_dev, runs=1)
+    rows = _rows(cfg, 24)
+    ref = ostack.stack_forward(cfg, rows=rows)
+    assert rel_err(to_f64(y)[rows], ref) <= BOUND
