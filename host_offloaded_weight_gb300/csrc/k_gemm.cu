@@ -54,10 +54,12 @@ struct GemmParams {
     int num_m_tiles, num_n_tiles, num_k_blocks, num_tiles;
     int b2_row_off;
     const __nv_bfloat16* bias;
-    const __nv_bfloat16* resid;
+    const void* resid;       // bf16, or fp32 when resid_f32
+    int resid_f32;
     int64_t ldr;
     void* C;
     int64_t ldc;
+    float* C32;              // optional fp32 copy of the output (same ldc)
     const int* group_bounds;
     int n_groups;
     int b_group_stride_rows;
@@ -269,18 +271,45 @@ __device__ __forceinline__ void epilogue_chunk(const GemmParams& p, int row, int
         for (int j = 0; j < 32; ++j) o[j] = silu_f(o[j]) * u[j];
     }
     if (EPI == EPI_BIAS_RESID || EPI == EPI_RESID) {
-        const uint16_t* rr = reinterpret_cast<const uint16_t*>(p.resid) + (int64_t)row * p.ldr + n;
-        if (full) {
+        if (p.resid_f32) {
+            const float* rr = reinterpret_cast<const float*>(p.resid) + (int64_t)row * p.ldr + n;
+            if (full) {
 #pragma unroll
-            for (int j = 0; j < 32; j += 8) {
-                uint4 q = *reinterpret_cast<const uint4*>(rr + j);
-                const uint16_t* h = reinterpret_cast<const uint16_t*>(&q);
-#pragma unroll
-                for (int i = 0; i < 8; ++i) o[j + i] += bf2f(h[i]);
+                for (int j = 0; j < 32; j += 4) {
+                    const float4 q = *reinterpret_cast<const float4*>(rr + j);
+                    o[j] += q.x;
+                    o[j + 1] += q.y;
+                    o[j + 2] += q.z;
+                    o[j + 3] += q.w;
+                }
+            } else {
+                for (int j = 0; j < 32; ++j)
+                    if (n + j < p.N) o[j] += rr[j];
             }
         } else {
-            for (int j = 0; j < 32; ++j)
-                if (n + j < p.N) o[j] += bf2f(rr[j]);
+            const uint16_t* rr = reinterpret_cast<const uint16_t*>(p.resid) + (int64_t)row * p.ldr + n;
+            if (full) {
+#pragma unroll
+                for (int j = 0; j < 32; j += 8) {
+                    uint4 q = *reinterpret_cast<const uint4*>(rr + j);
+                    const uint16_t* h = reinterpret_cast<const uint16_t*>(&q);
+#pragma unroll
+                    for (int i = 0; i < 8; ++i) o[j + i] += bf2f(h[i]);
+                }
+            } else {
+                for (int j = 0; j < 32; ++j)
+                    if (n + j < p.N) o[j] += bf2f(rr[j]);
+            }
+        }
+        if (p.C32) {  // the fp32 residual stream carried to the next segment
+            float* c32 = p.C32 + (int64_t)out_row * p.ldc + n;
+            if (full) {
+#pragma unroll
+                for (int j = 0; j < 32; j += 4)
+                    *reinterpret_cast<float4*>(c32 + j) = make_float4(o[j], o[j + 1], o[j + 2], o[j + 3]);
+            } else {
+                for (int j = 0; j < 32 && n + j < p.N; ++j) c32[j] = o[j];
+            }
         }
     }
     __nv_bfloat16* c = reinterpret_cast<__nv_bfloat16*>(p.C) + (int64_t)out_row * p.ldc + n;
@@ -598,7 +627,9 @@ cudaError_t launch_gemm_bf16(const GemmDesc& d, int max_ctas, cudaStream_t s) {
     if (d.epi != EPI_SCALE_F32 && ((d.ldc % 8) || (reinterpret_cast<uintptr_t>(d.C) & 15)))
         return cudaErrorInvalidValue;
     if ((d.epi == EPI_BIAS_RESID || d.epi == EPI_RESID) &&
-        ((d.ldr % 8) || (reinterpret_cast<uintptr_t>(d.resid) & 15)))
+        ((d.ldr % 8) || (reinterpret_cast<uintptr_t>(d.resid) & 15) || !d.resid))
+        return cudaErrorInvalidValue;
+    if (d.C32 && ((d.epi != EPI_BIAS_RESID && d.epi != EPI_RESID) || (reinterpret_cast<uintptr_t>(d.C32) & 15)))
         return cudaErrorInvalidValue;
     if (grouped && (d.n_groups < 1 || d.n_groups > MAX_GROUPS)) return cudaErrorInvalidValue;
     if (d.M == 0) return cudaSuccess;
@@ -616,10 +647,12 @@ cudaError_t launch_gemm_bf16(const GemmDesc& d, int max_ctas, cudaStream_t s) {
     p.num_tiles = p.num_m_tiles * p.num_n_tiles;
     p.b2_row_off = d.b2_row_off;
     p.bias = reinterpret_cast<const __nv_bfloat16*>(d.bias);
-    p.resid = reinterpret_cast<const __nv_bfloat16*>(d.resid);
+    p.resid = d.resid;
+    p.resid_f32 = d.resid_f32 ? 1 : 0;
     p.ldr = d.ldr;
     p.C = d.C;
     p.ldc = d.ldc;
+    p.C32 = reinterpret_cast<float*>(d.C32);
     p.group_bounds = d.group_bounds;
     p.n_groups = d.n_groups;
     p.b_group_stride_rows = d.b_group_stride_rows;

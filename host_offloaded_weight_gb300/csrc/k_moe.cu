@@ -12,8 +12,9 @@
 //            table does not depend on thread timing.
 //   gather   x rows copied into expert order for the grouped GEMM.
 //   combine  out[t] = x[t] + sum_{j<k} Y[t*k + j] in fixed j order (fp32), one
-//            rounding to bf16. Y holds w[t,j] * expert output, written by the
-//            grouped down-projection's epilogue.
+//            rounding to bf16 (plus the fp32 value for the residual stream). Y
+//            holds w[t,j] * expert output, written by the grouped
+//            down-projection's epilogue.
 #include "common.cuh"
 #include "kernels.h"
 
@@ -147,8 +148,9 @@ __global__ void moe_gather_kernel(const uint4* __restrict__ x, const int* __rest
     for (int i = threadIdx.x; i < h16; i += blockDim.x) xs[(int64_t)r * h16 + i] = x[(int64_t)t * h16 + i];
 }
 
-__global__ void moe_combine_kernel(const __nv_bfloat16* __restrict__ x, const float* __restrict__ y,
-                                   int T, int k, int H, __nv_bfloat16* __restrict__ out) {
+__global__ void moe_combine_kernel(const void* __restrict__ x, int x_f32, const float* __restrict__ y,
+                                   int T, int k, int H, __nv_bfloat16* __restrict__ out,
+                                   float* __restrict__ out32) {
     const int64_t idx = ((int64_t)blockIdx.x * blockDim.x + threadIdx.x) * 4;
     if (idx >= (int64_t)T * H) return;
     const int t = (int)(idx / H), c = (int)(idx % H);
@@ -160,11 +162,19 @@ __global__ void moe_combine_kernel(const __nv_bfloat16* __restrict__ x, const fl
         acc.z += v.z;
         acc.w += v.w;
     }
-    const __nv_bfloat162* xr = reinterpret_cast<const __nv_bfloat162*>(x + idx);
-    const float2 a = __bfloat1622float2(xr[0]), b = __bfloat1622float2(xr[1]);
+    float4 xr;
+    if (x_f32) {
+        xr = *reinterpret_cast<const float4*>(reinterpret_cast<const float*>(x) + idx);
+    } else {
+        const __nv_bfloat162* xb = reinterpret_cast<const __nv_bfloat162*>(reinterpret_cast<const __nv_bfloat16*>(x) + idx);
+        const float2 a = __bfloat1622float2(xb[0]), b = __bfloat1622float2(xb[1]);
+        xr = make_float4(a.x, a.y, b.x, b.y);
+    }
+    const float4 o4 = make_float4(xr.x + acc.x, xr.y + acc.y, xr.z + acc.z, xr.w + acc.w);
     __nv_bfloat162* o = reinterpret_cast<__nv_bfloat162*>(out + idx);
-    o[0] = __floats2bfloat162_rn(a.x + acc.x, a.y + acc.y);
-    o[1] = __floats2bfloat162_rn(b.x + acc.z, b.y + acc.w);
+    o[0] = __floats2bfloat162_rn(o4.x, o4.y);
+    o[1] = __floats2bfloat162_rn(o4.z, o4.w);
+    if (out32) *reinterpret_cast<float4*>(out32 + idx) = o4;
 }
 
 cudaError_t launch_moe_route(const float* logits, int n_layers, int T, int E, int k, int* sel,
@@ -202,14 +212,14 @@ cudaError_t launch_moe_gather(const void* x, const int* row_table, int rows, int
     return cudaGetLastError();
 }
 
-cudaError_t launch_moe_combine(const void* x, const float* y, int T, int k, int H, void* out,
-                               cudaStream_t s) {
+cudaError_t launch_moe_combine(const void* x, bool x_f32, const float* y, int T, int k, int H, void* out,
+                               float* out32, cudaStream_t s) {
     if ((H % 4) != 0) return cudaErrorInvalidValue;
     const int64_t n4 = (int64_t)T * H / 4;
     if (n4 <= 0) return cudaSuccess;
     const int threads = 256;
     moe_combine_kernel<<<(int)((n4 + threads - 1) / threads), threads, 0, s>>>(
-        reinterpret_cast<const __nv_bfloat16*>(x), y, T, k, H, reinterpret_cast<__nv_bfloat16*>(out));
+        x, x_f32 ? 1 : 0, y, T, k, H, reinterpret_cast<__nv_bfloat16*>(out), out32);
     return cudaGetLastError();
 }
 

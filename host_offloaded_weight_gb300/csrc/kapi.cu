@@ -91,8 +91,8 @@ ls_status lsk_wait_ready(const uint32_t* ready_dev, uint32_t epoch, int32_t limi
 }
 
 ls_status lsk_gemm_bf16(int32_t epilogue, const void* A, const void* B, int64_t b_rows, int32_t b2_row_off,
-                        const void* bias, const void* resid, void* C, int32_t M, int32_t N, int32_t K,
-                        int32_t max_ctas, void* stream) {
+                        const void* bias, const void* resid, int32_t resid_f32, void* C, void* C32, int32_t M,
+                        int32_t N, int32_t K, int32_t max_ctas, void* stream) {
     if (epilogue < LSK_EPI_STORE || epilogue > LSK_EPI_RESID) return LS_ERR_INVALID_ARG;
     if ((epilogue == LSK_EPI_BIAS_GELU || epilogue == LSK_EPI_BIAS_RESID) && !bias) return LS_ERR_INVALID_ARG;
     if ((epilogue == LSK_EPI_BIAS_RESID || epilogue == LSK_EPI_RESID) && !resid) return LS_ERR_INVALID_ARG;
@@ -105,7 +105,9 @@ ls_status lsk_gemm_bf16(int32_t epilogue, const void* A, const void* B, int64_t 
     d.b2_row_off = b2_row_off;
     d.bias = bias;
     d.resid = resid; d.ldr = N;
+    d.resid_f32 = resid_f32 != 0;
     d.C = C; d.ldc = N;
+    d.C32 = C32;
     d.M = M; d.N = N; d.K = K;
     d.err_word = err_dev();
     return st(launch_gemm_bf16(d, max_ctas, (cudaStream_t)stream));
@@ -159,9 +161,10 @@ ls_status lsk_moe_gather(const void* x, const int32_t* row_table, int32_t rows, 
     return st(launch_moe_gather(x, row_table, rows, k, H, x_sorted, (cudaStream_t)stream));
 }
 
-ls_status lsk_moe_combine(const void* x, const float* y, int32_t T, int32_t k, int32_t H, void* out, void* stream) {
+ls_status lsk_moe_combine(const void* x, int32_t x_f32, const float* y, int32_t T, int32_t k, int32_t H, void* out,
+                          float* out32, void* stream) {
     if (!x || !y || !out || T < 0 || k < 1) return LS_ERR_INVALID_ARG;
-    return st(launch_moe_combine(x, y, T, k, H, out, (cudaStream_t)stream));
+    return st(launch_moe_combine(x, x_f32 != 0, y, T, k, H, out, out32, (cudaStream_t)stream));
 }
 
 }  // extern "C"

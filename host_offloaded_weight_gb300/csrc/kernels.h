@@ -49,10 +49,12 @@ struct GemmDesc {
     int M = 0, N = 0, K = 0;
     int b2_row_off = 0;          // dual: second B matrix starts this many rows after the first
     const void* bias = nullptr;  // [N] bf16
-    const void* resid = nullptr; // [M, ldr] bf16
+    const void* resid = nullptr; // [M, ldr] bf16 (fp32 with resid_f32)
+    bool resid_f32 = false;
     int64_t ldr = 0;
     void* C = nullptr;
     int64_t ldc = 0;
+    void* C32 = nullptr;         // residual epilogues: optional fp32 copy of C (ldc)
     // grouped (expert) mode: M is the total row count; groups split it
     const int* group_bounds = nullptr;  // [n_groups + 1], device
     int n_groups = 0;
@@ -80,7 +82,8 @@ cudaError_t launch_moe_group(const int* sel, int n_layers, int T, int E, int k, 
                              int* group_bounds, uint8_t* expert_used, cudaStream_t s);
 cudaError_t launch_moe_gather(const void* x, const int* row_table, int rows, int k, int H,
                               void* x_sorted, cudaStream_t s);
-cudaError_t launch_moe_combine(const void* x, const float* y, int T, int k, int H, void* out,
-                               cudaStream_t s);
+// out = x + sum_j y[t*k+j]; x bf16 (or fp32 with x_f32); out bf16, plus out32 fp32 if given
+cudaError_t launch_moe_combine(const void* x, bool x_f32, const float* y, int T, int k, int H, void* out,
+                               float* out32, cudaStream_t s);
 
 }  // namespace ls

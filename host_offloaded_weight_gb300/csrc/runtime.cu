@@ -104,7 +104,9 @@ struct ls_ctx {
     std::vector<int> seg_slot;
     // workspaces
     int64_t ws_tokens = 0;
-    void* act[2] = {nullptr, nullptr};
+    void* act[2] = {nullptr, nullptr};  // fp32 kind: ping-pong activations
+    void* xb = nullptr;                 // bf16 kinds: bf16 operand copy of the residual stream
+    float* xf = nullptr;                // bf16 kinds: fp32 residual stream (updated in place)
     void* hbuf = nullptr;
     void* ubuf = nullptr;
     // MoE workspaces
@@ -288,10 +290,19 @@ struct RunCtx {
     uint64_t wait_ns;
 };
 
+// Activations between segments: the fp32 kind ping-pongs two buffers; the bf16
+// kinds carry the residual stream in fp32 (xf, updated in place: every output
+// element reads and writes only its own residual element) plus its bf16
+// rounding (xb) as the next GEMM operand. Segment 0 reads the caller's bf16 x;
+// the last segment writes the caller's bf16 y.
 void compute_segment(ls_ctx* c, const RunCtx& rc, int seg, bool wait) {
     const int N = c->N;
-    const void* xin = seg == 0 ? rc.x : c->act[(seg - 1) & 1];
-    void* xout = seg == N - 1 ? rc.y : c->act[seg & 1];
+    const bool first = seg == 0, last = seg == N - 1;
+    const void* xin = first ? rc.x : (c->kind == LS_KIND_LINEAR_GELU_F32 ? c->act[(seg - 1) & 1] : c->xb);
+    void* xout = last ? rc.y : (c->kind == LS_KIND_LINEAR_GELU_F32 ? c->act[seg & 1] : c->xb);
+    const void* rin = first ? rc.x : (const void*)c->xf;   // residual input
+    const bool rin_f32 = !first;
+    float* xout32 = last ? nullptr : c->xf;                // fp32 residual output
     const int T = (int)rc.T, H = c->H, F = c->F;
     const int slot = c->seg_slot[seg];
     const uint32_t epoch = c->seg_epoch[seg];
@@ -348,9 +359,9 @@ void compute_segment(ls_ctx* c, const RunCtx& rc, int seg, bool wait) {
             g2.A = c->hbuf; g2.lda = F; g2.a_rows = T;
             g2.B = tptr(c, seg, o + 2); g2.ldb = F; g2.b_rows = H;
             g2.bias = tptr(c, seg, o + 3);
-            g2.resid = xin; g2.ldr = H;
+            g2.resid = rin; g2.resid_f32 = rin_f32; g2.ldr = H;
             g2.M = T; g2.N = H; g2.K = F;
-            g2.C = xout; g2.ldc = H;
+            g2.C = xout; g2.ldc = H; g2.C32 = xout32;
             KTime kt(c, "gemm_down", rc.s);
             track(c, launch_gemm_bf16(g2, ctas, rc.s));
             break;
@@ -371,9 +382,9 @@ void compute_segment(ls_ctx* c, const RunCtx& rc, int seg, bool wait) {
             g2.epi = EPI_RESID;
             g2.A = c->hbuf; g2.lda = F; g2.a_rows = T;
             g2.B = tptr(c, seg, 2); g2.ldb = F; g2.b_rows = H;
-            g2.resid = xin; g2.ldr = H;
+            g2.resid = rin; g2.resid_f32 = rin_f32; g2.ldr = H;
             g2.M = T; g2.N = H; g2.K = F;
-            g2.C = xout; g2.ldc = H;
+            g2.C = xout; g2.ldc = H; g2.C32 = xout32;
             KTime kt(c, "gemm_down", rc.s);
             track(c, launch_gemm_bf16(g2, ctas, rc.s));
             break;
@@ -419,7 +430,7 @@ void compute_segment(ls_ctx* c, const RunCtx& rc, int seg, bool wait) {
                 track(c, launch_gemm_bf16(g2, ctas, rc.s));
             }
             KTime kt(c, "moe_combine", rc.s);
-            track(c, launch_moe_combine(xin, c->moe_y, T, k, H, xout, rc.s));
+            track(c, launch_moe_combine(rin, rin_f32, c->moe_y, T, k, H, xout, xout32, rc.s));
             break;
         }
     }
@@ -738,15 +749,17 @@ ls_status autotune_copy(ls_ctx* c) {
 ls_status ensure_workspace(ls_ctx* c, int64_t T) {
     if (T <= c->ws_tokens) return LS_OK;
     cudaDeviceSynchronize();
-    for (void** p : {&c->act[0], &c->act[1], &c->hbuf, &c->ubuf, &c->moe_xs, &c->moe_hs})
+    for (void** p : {&c->act[0], &c->act[1], &c->xb, (void**)&c->xf, &c->hbuf, &c->ubuf, &c->moe_xs, &c->moe_hs})
         if (*p) { cudaFree(*p); *p = nullptr; }
     for (void* p : {(void*)c->moe_sel, (void*)c->moe_w, (void*)c->moe_table, (void*)c->moe_y})
         if (p) cudaFree(p);
     c->moe_sel = nullptr; c->moe_w = nullptr; c->moe_table = nullptr; c->moe_y = nullptr;
-    const size_t es = c->kind == LS_KIND_LINEAR_GELU_F32 ? 4 : 2;
-    if (c->N > 1) {
-        CK(cudaMalloc(&c->act[0], (size_t)T * c->H * es));
-        CK(cudaMalloc(&c->act[1], (size_t)T * c->H * es));
+    if (c->N > 1 && c->kind == LS_KIND_LINEAR_GELU_F32) {
+        CK(cudaMalloc(&c->act[0], (size_t)T * c->H * 4));
+        CK(cudaMalloc(&c->act[1], (size_t)T * c->H * 4));
+    } else if (c->N > 1) {
+        CK(cudaMalloc(&c->xb, (size_t)T * c->H * 2));
+        CK(cudaMalloc((void**)&c->xf, (size_t)T * c->H * 4));
     }
     if (c->kind == LS_KIND_FFN_GELU_BF16 || c->kind == LS_KIND_FFN_GELU_SHARED_BF16 || c->kind == LS_KIND_SWIGLU_BF16)
         CK(cudaMalloc(&c->hbuf, (size_t)T * c->F * 2));
@@ -1169,7 +1182,7 @@ void ls_ctx_destroy(ls_ctx* c) {
         if (c->copy_stream) cudaStreamSynchronize(c->copy_stream);
         for (auto& sr : c->segs)
             if (sr.ranges_dev) cudaFree(sr.ranges_dev);
-        for (void* p : {(void*)c->ready, (void*)c->tickets, c->act[0], c->act[1], c->hbuf, c->ubuf,
+        for (void* p : {(void*)c->ready, (void*)c->tickets, c->act[0], c->act[1], c->xb, (void*)c->xf, c->hbuf, c->ubuf,
                         (void*)c->moe_sel, (void*)c->moe_w, (void*)c->moe_table, (void*)c->moe_bounds,
                         (void*)c->moe_used, c->moe_xs, c->moe_hs, (void*)c->moe_y, c->stage_x, c->stage_y,
                         (void*)c->stage_logits})

@@ -110,14 +110,14 @@ _sig = {
     "lsk_device_error": (_U32, []),
     "lsk_copy_h2slot": (_I32, [_P, _P, _U64, _I32, _P, _P, _U32, _P]),
     "lsk_wait_ready": (_I32, [_P, _U32, _I32, _P, _I32, _P]),
-    "lsk_gemm_bf16": (_I32, [_I32, _P, _P, _I64, _I32, _P, _P, _P, _I32, _I32, _I32, _I32, _P]),
+    "lsk_gemm_bf16": (_I32, [_I32, _P, _P, _I64, _I32, _P, _P, _I32, _P, _P, _I32, _I32, _I32, _I32, _P]),
     "lsk_gemm_grouped_bf16": (_I32, [_I32, _P, _P, _I64, _I32, _I32, _I32, _P, _I32, _P, _P, _P,
                                      _I32, _I32, _I32, _I32, _P]),
     "lsk_linear_gelu_f32": (_I32, [_P, _P, _P, _P, _I32, _I32, _I32, _P]),
     "lsk_moe_route": (_I32, [_P, _I32, _I32, _I32, _I32, _P, _P, _P]),
     "lsk_moe_group": (_I32, [_P, _I32, _I32, _I32, _I32, _P, _P, _P, _P]),
     "lsk_moe_gather": (_I32, [_P, _P, _I32, _I32, _I32, _P, _P]),
-    "lsk_moe_combine": (_I32, [_P, _P, _I32, _I32, _I32, _P, _P]),
+    "lsk_moe_combine": (_I32, [_P, _I32, _P, _I32, _I32, _I32, _P, _P, _P]),
 }
 for _name, (_res, _args) in _sig.items():
     _f = getattr(_lib, _name)
@@ -351,10 +351,13 @@ def lsk_wait_ready(ready, epoch: int, limit_ms: int, err_host, slot: int = 0, st
 
 
 def lsk_gemm_bf16(epilogue: int, A, B, C_out, M: int, N: int, K: int, bias=None, resid=None,
-                  b_rows: int | None = None, b2_row_off: int = 0, max_ctas: int = 0, stream=None) -> int:
+                  b_rows: int | None = None, b2_row_off: int = 0, max_ctas: int = 0, stream=None,
+                  C32=None) -> int:
     rows = b_rows if b_rows is not None else B.shape[0]
+    rf32 = int(resid is not None and "float32" in str(getattr(resid, "dtype", "")))
     return _check(_lib.lsk_gemm_bf16(epilogue, _ptr(A), _ptr(B), rows, b2_row_off, _ptr(bias),
-                                     _ptr(resid), _ptr(C_out), M, N, K, max_ctas, _stream(stream)))
+                                     _ptr(resid), rf32, _ptr(C_out), _ptr(C32), M, N, K, max_ctas,
+                                     _stream(stream)))
 
 
 def lsk_gemm_grouped_bf16(epilogue: int, A, B, b_rows: int, b_base_row: int, b_group_stride_rows: int,
@@ -384,5 +387,6 @@ def lsk_moe_gather(x, row_table, rows, k, H, x_sorted, stream=None) -> int:
     return _check(_lib.lsk_moe_gather(_ptr(x), _ptr(row_table), rows, k, H, _ptr(x_sorted), _stream(stream)))
 
 
-def lsk_moe_combine(x, y, T, k, H, out, stream=None) -> int:
-    return _check(_lib.lsk_moe_combine(_ptr(x), _ptr(y), T, k, H, _ptr(out), _stream(stream)))
+def lsk_moe_combine(x, y, T, k, H, out, out32=None, stream=None) -> int:
+    xf32 = int("float32" in str(getattr(x, "dtype", "")))
+    return _check(_lib.lsk_moe_combine(_ptr(x), xf32, _ptr(y), T, k, H, _ptr(out), _ptr(out32), _stream(stream)))

@@ -54,12 +54,14 @@ ls_status lsk_wait_ready(const uint32_t* ready_dev, uint32_t epoch, int32_t limi
                          int32_t slot, void* stream);
 
 /* Dense tcgen05 GEMM with a fused epilogue. A_dev [M,K], B_dev [b_rows,K] (b_rows
- * >= N, or >= b2_row_off + N for SWIGLU), bias [N], R [M,N], C [M,N]; all bf16
- * row-major, dense. K and N multiples of 8, pointers 16-byte aligned.
- * max_ctas <= 0: one CTA per SM. */
+ * >= N, or >= b2_row_off + N for SWIGLU), bias [N], R [M,N], C [M,N]; bf16
+ * row-major, dense, except R, which is fp32 when resid_f32 != 0. The residual
+ * epilogues also write the fp32 result to C32_dev [M,N] when it is not NULL.
+ * K and N multiples of 8, pointers 16-byte aligned. max_ctas <= 0: one CTA per SM. */
 ls_status lsk_gemm_bf16(int32_t epilogue, const void* A_dev, const void* B_dev, int64_t b_rows,
-                        int32_t b2_row_off, const void* bias_dev, const void* resid_dev, void* C_dev,
-                        int32_t M, int32_t N, int32_t K, int32_t max_ctas, void* stream);
+                        int32_t b2_row_off, const void* bias_dev, const void* resid_dev, int32_t resid_f32,
+                        void* C_dev, void* C32_dev, int32_t M, int32_t N, int32_t K, int32_t max_ctas,
+                        void* stream);
 
 /* Grouped (expert) GEMM: rows of A_dev [M,K] are sorted by group;
  * group g = rows [group_bounds[g], group_bounds[g+1]) multiplies B rows
@@ -93,9 +95,10 @@ ls_status lsk_moe_group(const int32_t* sel_dev, int32_t n_layers, int32_t T, int
 ls_status lsk_moe_gather(const void* x_dev, const int32_t* row_table_dev, int32_t rows, int32_t k, int32_t H,
                          void* x_sorted_dev, void* stream);
 
-/* out[t] = x[t] + sum_{j<k} y[t*k + j] (fp32 sum in j order, one bf16 rounding). */
-ls_status lsk_moe_combine(const void* x_dev, const float* y_dev, int32_t T, int32_t k, int32_t H, void* out_dev,
-                          void* stream);
+/* out[t] = x[t] + sum_{j<k} y[t*k + j] (fp32 sum in j order, one bf16 rounding).
+ * x is bf16, or fp32 when x_f32 != 0; out32_dev (may be NULL) gets the fp32 sum. */
+ls_status lsk_moe_combine(const void* x_dev, int32_t x_f32, const float* y_dev, int32_t T, int32_t k, int32_t H,
+                          void* out_dev, float* out32_dev, void* stream);
 
 #ifdef __cplusplus
 }

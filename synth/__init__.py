@@ -9,7 +9,12 @@ Recipe (one stream per tensor):
   * generator: ``numpy.random.default_rng(SeedSequence([seed, segment, index]))``
     drawing ``standard_normal`` in float32, in row-major order;
   * weights and biases are multiplied (in float32) by ``1/sqrt(fan_in)`` of the
-    linear they belong to, so they are N(0, std = 1/sqrt(fan_in));
+    linear they belong to, so they are N(0, std = 1/sqrt(fan_in)); the down
+    projection D of the gate/up/down kinds (dense and per expert) also carries a
+    depth factor ``1/sqrt(n_segments)``: with plain 1/sqrt(fan_in) the residual
+    stream of a SwiGLU stack grows quadratically per layer and overflows float
+    range within a dozen layers (the product of two N(0, v) projections has
+    variance ~ v^2);
   * activations ``x`` are N(0, 1) from ``SeedSequence([seed, 2_000_000, 0])``;
   * MoE router logits for layer ``l`` are N(0, 1) float32 from
     ``SeedSequence([seed, 1_000_000 + l])``, shape ``[tokens, experts]``;
@@ -54,6 +59,7 @@ class TensorSpec:
     dtype: str          # "f32" or "bf16"
     fan_in: int
     index: int          # stream index inside the segment
+    gain: float = 1.0   # extra factor on top of 1/sqrt(fan_in)
 
     @property
     def numel(self) -> int:
@@ -97,15 +103,16 @@ def segment_tensors(cfg: StackConfig) -> list:
     if k in (KIND_FFN_GELU_BF16, KIND_FFN_GELU_SHARED_BF16):
         return [TensorSpec("W1", (f, h), "bf16", h, 0), TensorSpec("b1", (f,), "bf16", h, 1),
                 TensorSpec("W2", (h, f), "bf16", f, 2), TensorSpec("b2", (h,), "bf16", f, 3)]
+    depth_gain = 1.0 / math.sqrt(cfg.n_segments)
     if k == KIND_SWIGLU_BF16:
         return [TensorSpec("G", (f, h), "bf16", h, 0), TensorSpec("U", (f, h), "bf16", h, 1),
-                TensorSpec("D", (h, f), "bf16", f, 2)]
+                TensorSpec("D", (h, f), "bf16", f, 2, depth_gain)]
     if k == KIND_MOE_SWIGLU_BF16:
         out = []
         for e in range(cfg.n_experts):
             out += [TensorSpec(f"G{e}", (f, h), "bf16", h, 3 * e),
                     TensorSpec(f"U{e}", (f, h), "bf16", h, 3 * e + 1),
-                    TensorSpec(f"D{e}", (h, f), "bf16", f, 3 * e + 2)]
+                    TensorSpec(f"D{e}", (h, f), "bf16", f, 3 * e + 2, depth_gain)]
         return out
     raise ValueError(f"unknown kind {k}")
 
@@ -205,7 +212,7 @@ def tensor_seq(cfg: StackConfig, segment: int, spec: TensorSpec) -> list:
 
 def draw_tensor(cfg: StackConfig, segment: int, spec: TensorSpec, out: np.ndarray | None = None):
     """Draw one tensor. fp32 tensors come back as float32, bf16 as uint16 bit patterns."""
-    scale = 1.0 / math.sqrt(spec.fan_in)
+    scale = spec.gain / math.sqrt(spec.fan_in)
     if spec.dtype == "f32":
         if out is None:
             out = np.empty(spec.shape, np.float32)

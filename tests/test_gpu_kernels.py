@@ -97,6 +97,28 @@ def test_gemm_epilogues_vs_oracle(M, N, K, epi):
     assert np.all(np.abs(got - ref) <= tol), (epi, np.max(np.abs(got - ref) - tol))
 
 
+@pytest.mark.parametrize("M,N,K", [(300, 520, 200), (256, 264, 72)])
+@pytest.mark.parametrize("epi", [L.LSK_EPI_BIAS_RESID, L.LSK_EPI_RESID])
+def test_gemm_fp32_residual_stream(M, N, K, epi):
+    """Residual read in fp32, result written both as fp32 (the residual stream)
+    and as its bf16 rounding (the next GEMM's operand)."""
+    ab, a = rand_bf16((M, K), 31)
+    bb, b = rand_bf16((N, K), 32, 1.0 / np.sqrt(K))
+    biasb, bias = rand_bf16((N,), 33, 0.5)
+    r = np.random.default_rng(34).standard_normal((M, N)).astype(np.float32)
+    C = torch.empty((M, N), dtype=torch.bfloat16, device="cuda")
+    C32 = torch.empty((M, N), dtype=torch.float32, device="cuda")
+    L.lsk_gemm_bf16(epi, bf16_dev(ab), bf16_dev(bb), C, M, N, K, bias=bf16_dev(biasb),
+                    resid=torch.from_numpy(r).cuda(), C32=C32)
+    torch.cuda.synchronize()
+    _no_device_error()
+    ref = a @ b.T + r.astype(np.float64) + (bias if epi == L.LSK_EPI_BIAS_RESID else 0)
+    got32 = C32.cpu().numpy().astype(np.float64)
+    assert np.max(np.abs(got32 - ref)) <= 1e-5 * np.sqrt(K) * np.abs(ref).max()
+    # the bf16 output is exactly the rounding of the fp32 output
+    assert torch.equal(C.cpu(), C32.cpu().to(torch.bfloat16))
+
+
 @pytest.mark.parametrize("ctas", [1, 3, 37, 0])
 def test_gemm_bit_identical_across_grid_sizes(ctas):
     M, N, K = 700, 776, 320
@@ -230,3 +252,11 @@ def test_gather_and_combine():
     np.testing.assert_array_equal(to_f64(xs), x[table // k])
     ref = x + y.astype(np.float64).reshape(T, k, H).sum(1)
     assert np.all(np.abs(to_f64(out) - ref) <= 2.0 ** -8 * np.abs(ref) + 1e-6)
+    # fp32 residual in, fp32 residual out
+    xf = np.random.default_rng(5).standard_normal((T, H)).astype(np.float32)
+    out32 = torch.empty((T, H), dtype=torch.float32, device="cuda")
+    L.lsk_moe_combine(torch.from_numpy(xf).cuda(), torch.from_numpy(y).cuda(), T, k, H, out, out32=out32)
+    torch.cuda.synchronize()
+    ref32 = xf.astype(np.float64) + y.astype(np.float64).reshape(T, k, H).sum(1)
+    assert np.max(np.abs(out32.cpu().numpy() - ref32)) <= 1e-5
+    assert torch.equal(out.cpu(), out32.cpu().to(torch.bfloat16))

@@ -3,6 +3,8 @@ schedule against the policy simulator and bit-identity across depth, residency
 and pool settings ("feat: pool VRAM for streamed layer", Verification: zero
 differing channels with and without the pool; "feat: prefetch streamed layers
 during compute", Verification: matching output hashes)."""
+import os
+
 import numpy as np
 import pytest
 import torch
@@ -137,6 +139,52 @@ def test_shared_projection_stack_full_size():
                 assert rel_err(to_f64(y)[rows], ref) <= BOUND
             else:
                 assert np.array_equal(_bits(y), base), (depth, pool)
+
+
+def _oracle_from_host(cfg, hs, rows):
+    """fp64 oracle on sampled rows, widening the host stack's own tensors
+    (the same bytes the GPU streams) instead of drawing them again."""
+    from oracle import forward as F
+    x = F.as_f64(synth.draw_x(cfg)[rows], cfg.dtype)
+    specs = synth.segment_tensors(cfg)
+    for s in range(len(hs.segments)):
+        if cfg.kind == synth.KIND_MOE_SWIGLU_BF16:
+            views = hs.seg_views[s]
+            experts = lambda e, v=views: [F.as_f64(t, "bf16") for t in v[3 * e:3 * e + 3]]
+            x = F.moe_swiglu(x, synth.draw_logits(cfg, s)[rows], experts, cfg.top_k)
+        else:
+            t = [F.as_f64(v, sp.dtype) for v, sp in zip(hs.seg_views[s], specs)]
+            x = ostack.apply_segment(cfg, s, x, rows=rows, tensors=t)
+    return x
+
+
+def test_large_swiglu_stack_full_size():
+    """48 x 425 MB segments (20 GB in host memory), 4 GiB budget, resident cap
+    4, depth 2; then the one-slot budget that takes the mandatory-slot path."""
+    cfg = synth.LARGE
+    hs = synth.HostStack(cfg)
+    y, ev, stats, st, sts = _run(cfg, hs, runs=2)
+    assert (stats["residents"], stats["depth"], stats["pool_slots"]) == (4, 2, 7)
+    sim, _ = _sim_events(cfg, hs, 2, 4, cfg.max_vram_bytes, 1, 2)
+    assert ev == [tuple(e) for e in sim.events]
+    rows = _rows(cfg, 16)
+    ref = _oracle_from_host(cfg, hs, rows)
+    assert rel_err(to_f64(y)[rows], ref) <= BOUND
+    one = int(0.1 * 2**30)
+    y1, ev1, stats1, st1, _ = _run(cfg, hs, runs=1, max_vram_bytes=one)
+    assert st1 == L.LS_WARN_MANDATORY_SLOT and stats1["pool_slots"] == 1 and stats1["depth"] == 0
+    assert np.array_equal(_bits(y1), _bits(y))
+
+
+@pytest.mark.skipif(os.environ.get("LS_SLOW") != "1", reason="58 GB host stack: set LS_SLOW=1")
+def test_moe_stack_full_size():
+    cfg = synth.MOE
+    hs = synth.HostStack(cfg)
+    lg_dev, _ = logits_dev(cfg)
+    y, ev, stats, st, sts = _run(cfg, hs, logits=lg_dev, runs=1)
+    rows = _rows(cfg, 8)
+    ref = _oracle_from_host(cfg, hs, rows)
+    assert rel_err(to_f64(y)[rows], ref) <= BOUND
 
 
 # ------------------------------------------------------------------ faults (host-made, bounded)
