@@ -20,6 +20,7 @@
 #include <cstdio>
 #include <cstring>
 #include <map>
+#include <new>
 #include <string>
 #include <vector>
 
@@ -829,9 +830,25 @@ ls_status ls_ctx_create(const ls_params* params, ls_ctx** out) {
     return LS_OK;
 }
 
+static void release_resources(ls_ctx* c);
+
+static ls_status register_impl(ls_ctx* c, const ls_segment_desc* segs, int32_t n, const ls_shared_ref* shared_map,
+                               int32_t n_shared);
+
 ls_status ls_register_segments(ls_ctx* c, const ls_segment_desc* segs, int32_t n, const ls_shared_ref* shared_map,
                                int32_t n_shared) {
     if (!c) return LS_ERR_INVALID_ARG;
+    if (c->registered) {
+        set_err(c, "segments are already registered");
+        return LS_ERR_STATE;
+    }
+    ls_status st = register_impl(c, segs, n, shared_map, n_shared);
+    if (st < 0) release_resources(c);  // a failed registration leaves nothing behind
+    return st;
+}
+
+static ls_status register_impl(ls_ctx* c, const ls_segment_desc* segs, int32_t n, const ls_shared_ref* shared_map,
+                               int32_t n_shared) {
     if (c->registered) {
         set_err(c, "segments are already registered");
         return LS_ERR_STATE;
@@ -1170,8 +1187,7 @@ ls_status ls_get_kernel_times(ls_ctx* c, ls_kernel_time* out, int32_t cap, int32
     return LS_OK;
 }
 
-void ls_ctx_destroy(ls_ctx* c) {
-    if (!c) return;
+static void release_resources(ls_ctx* c) {
     if (c->N > 0) {
         cudaSetDevice(c->device);
         cudaDeviceSynchronize();
@@ -1202,6 +1218,18 @@ void ls_ctx_destroy(ls_ctx* c) {
         for (auto& r : c->host_registered) cudaHostUnregister(r.first);
         cudaGetLastError();
     }
+    // back to an empty, unregistered context
+    ls_params prm = c->prm;
+    std::string err = c->err;
+    c->~ls_ctx();
+    new (c) ls_ctx();
+    c->prm = prm;
+    c->err = err;
+}
+
+void ls_ctx_destroy(ls_ctx* c) {
+    if (!c) return;
+    release_resources(c);
     delete c;
 }
 

@@ -40,7 +40,11 @@ def make_ctx(cfg, hs, **over):
               max_vram_bytes=cfg.max_vram_bytes, use_pool=cfg.use_pool, wait_limit_ms=5000)
     kw.update(over)
     ctx = L.ls_ctx_create(L.ls_params_init(**kw))
-    st = L.ls_register_segments(ctx, hs.segments, hs.shared_map)
+    try:
+        st = L.ls_register_segments(ctx, hs.segments, hs.shared_map)
+    except Exception:
+        L.ls_ctx_destroy(ctx)
+        raise
     return ctx, st
 
 

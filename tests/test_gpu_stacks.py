@@ -223,6 +223,9 @@ def test_pool_degradation_under_allocator_cap():
     with pytest.raises(L.LsError) as e:
         _run(cfg, hs, max_vram_bytes=6 * S, prefetch_depth=1, test_alloc_cap_bytes=S // 2)
     assert e.value.status == L.LS_ERR_OOM
+    # the failed registration released its host registration: the same memory registers again
+    y2, *_ = _run(cfg, hs, max_vram_bytes=0, prefetch_depth=0)
+    assert np.array_equal(_bits(y2), _bits(y_ref))
 
 
 def test_async_failure_falls_back_synchronously():
