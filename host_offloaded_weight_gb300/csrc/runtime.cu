@@ -136,7 +136,10 @@ struct ls_ctx {
     std::vector<TimerClass> tclass;
     std::vector<std::pair<cudaEvent_t, cudaEvent_t>> tev;  // event pool
     std::vector<int> tev_class;                              // class of each used pair
+    std::vector<int> tev_stream, tev_seg;
     size_t tev_used = 0;
+    int cur_seg = -1;
+    std::vector<ls_trace_event> trace;
 };
 
 namespace {
@@ -202,9 +205,13 @@ struct KTime {
             if (cudaEventCreate(&a) != cudaSuccess || cudaEventCreate(&b) != cudaSuccess) return;
             c->tev.push_back({a, b});
             c->tev_class.push_back(cls);
+            c->tev_stream.push_back(0);
+            c->tev_seg.push_back(-1);
         }
         idx = c->tev_used++;
         c->tev_class[idx] = cls;
+        c->tev_stream[idx] = s == c->copy_stream ? 1 : 0;
+        c->tev_seg[idx] = c->cur_seg;
         track(c, cudaEventRecord(c->tev[idx].first, s));
     }
     ~KTime() {
@@ -214,6 +221,7 @@ struct KTime {
 
 // After the run's final synchronisation: fold the recorded pairs into the classes.
 void collect_times(ls_ctx* c) {
+    if (c->prm.kernel_timing >= 2) c->trace.clear();
     for (size_t i = 0; i < c->tev_used; ++i) {
         float ms = 0;
         if (cudaEventElapsedTime(&ms, c->tev[i].first, c->tev[i].second) == cudaSuccess) {
@@ -221,6 +229,19 @@ void collect_times(ls_ctx* c) {
             c->tclass[c->tev_class[i]].total_ms += ms;
         } else {
             cudaGetLastError();
+        }
+        if (c->prm.kernel_timing >= 2) {
+            ls_trace_event t{};
+            snprintf(t.name, sizeof(t.name), "%s", c->tclass[c->tev_class[i]].name.c_str());
+            t.stream = c->tev_stream[i];
+            t.segment = c->tev_seg[i];
+            float a = 0, b = 0;
+            if (cudaEventElapsedTime(&a, c->tev[0].first, c->tev[i].first) != cudaSuccess ||
+                cudaEventElapsedTime(&b, c->tev[0].first, c->tev[i].second) != cudaSuccess)
+                cudaGetLastError();
+            t.start_ms = a;
+            t.end_ms = b;
+            c->trace.push_back(t);
         }
     }
     c->tev_used = 0;
@@ -468,6 +489,7 @@ struct GpuExec : Executor {
                                          cudaMemcpyHostToDevice, rc.s));
     }
     void load(int seg, int slot, int kind, int64_t) override {
+        c->cur_seg = seg;
         void* dst = c->prm.use_pool ? (uint8_t*)c->pool + (int64_t)slot * c->sched.plan().S : c->seg_buf[seg];
         const uint32_t epoch = ++c->slot_epoch[slot];
         c->seg_epoch[seg] = epoch;
@@ -488,6 +510,7 @@ struct GpuExec : Executor {
         }
     }
     void activate(int seg, int slot, bool via_queue) override {
+        c->cur_seg = seg;
         compute_segment(c, rc, seg, via_queue);
         track(c, cudaEventRecord(c->slot_free[slot], rc.s));
     }
@@ -536,7 +559,8 @@ ls_status check_params(const ls_params* p, ls_params* out, std::string* why) {
         return LS_ERR_INVALID_ARG;
     }
     if (d.copy_path < LS_COPY_AUTO || d.copy_path > LS_COPY_ENGINE) { *why = "bad copy_path"; return LS_ERR_INVALID_ARG; }
-    if (d.copy_ctas < 0 || d.test_alloc_cap_bytes < 0 || d.test_drop_publish < 0) {
+    if (d.copy_ctas < 0 || d.test_alloc_cap_bytes < 0 || d.test_drop_publish < 0 || d.kernel_timing < 0 ||
+        d.kernel_timing > 2) {
         *why = "negative count";
         return LS_ERR_INVALID_ARG;
     }
@@ -1167,6 +1191,14 @@ ls_status ls_get_stats(ls_ctx* c, ls_stats* out) {
     const uint32_t n = std::min<uint32_t>(out->struct_size, sizeof(s));
     memcpy(out, &s, n);
     out->struct_size = n;
+    return LS_OK;
+}
+
+ls_status ls_get_trace(ls_ctx* c, ls_trace_event* out, int64_t cap, int64_t* n_out) {
+    if (!c || !n_out || cap < 0 || (cap > 0 && !out)) return LS_ERR_INVALID_ARG;
+    *n_out = (int64_t)c->trace.size();
+    const int64_t n = std::min<int64_t>(cap, (int64_t)c->trace.size());
+    if (n > 0) memcpy(out, c->trace.data(), sizeof(ls_trace_event) * n);
     return LS_OK;
 }
 

@@ -68,6 +68,11 @@ class ls_kernel_time(C.Structure):
     _fields_ = [("name", C.c_char * 32), ("launches", C.c_int64), ("total_ms", C.c_double)]
 
 
+class ls_trace_event(C.Structure):
+    _fields_ = [("name", C.c_char * 32), ("stream", C.c_int32), ("segment", C.c_int32),
+                ("start_ms", C.c_double), ("end_ms", C.c_double)]
+
+
 class ls_sched_event(C.Structure):
     _fields_ = [("run", C.c_int32), ("step", C.c_int32), ("kind", C.c_int32),
                 ("segment", C.c_int32), ("slot", C.c_int32), ("reserved", C.c_int32),
@@ -100,6 +105,7 @@ _sig = {
     "ls_get_schedule": (_I32, [_P, C.POINTER(ls_sched_event), _I64, C.POINTER(_I64)]),
     "ls_get_stats": (_I32, [_P, C.POINTER(ls_stats)]),
     "ls_get_kernel_times": (_I32, [_P, C.POINTER(ls_kernel_time), _I32, C.POINTER(_I32), _I32]),
+    "ls_get_trace": (_I32, [_P, C.POINTER(ls_trace_event), _I64, C.POINTER(_I64)]),
     "ls_ctx_destroy": (None, [_P]),
     "ls_status_string": (C.c_char_p, [_I32]),
     "ls_last_error": (C.c_char_p, [_P]),
@@ -296,6 +302,15 @@ def ls_get_kernel_times(ctx: Ctx, reset: bool = False) -> dict:
     buf = (ls_kernel_time * max(1, n.value))()
     _check(_lib.ls_get_kernel_times(ctx.handle, buf, n.value, C.byref(n), int(reset)), ctx)
     return {buf[i].name.decode(): (buf[i].launches, buf[i].total_ms) for i in range(n.value)}
+
+
+def ls_get_trace(ctx: Ctx) -> list:
+    """[(name, stream, segment, start_ms, end_ms)] of the passes the last ls_sync completed."""
+    n = _I64()
+    _check(_lib.ls_get_trace(ctx.handle, None, 0, C.byref(n)), ctx)
+    buf = (ls_trace_event * max(1, n.value))()
+    _check(_lib.ls_get_trace(ctx.handle, buf, n.value, C.byref(n)), ctx)
+    return [(b.name.decode(), b.stream, b.segment, b.start_ms, b.end_ms) for b in buf[:n.value]]
 
 
 def ls_ctx_destroy(ctx: Ctx) -> None:

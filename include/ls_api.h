@@ -114,7 +114,8 @@ typedef struct ls_params {
     int64_t test_alloc_cap_bytes; /* parameter allocations beyond this many live bytes fail */
     int32_t test_fail_async;      /* the first prefetch finds asynchronous transfer unavailable */
     int32_t test_drop_publish;    /* the Nth publish (1-based, over the context's life) leaves its ready word down */
-    int32_t kernel_timing;        /* 1 = bracket every launch with CUDA events (see ls_get_kernel_times) */
+    int32_t kernel_timing;        /* 1 = bracket every launch with CUDA events (see ls_get_kernel_times);
+                                     2 = also keep a per-launch trace (see ls_get_trace) */
 } ls_params;
 
 /* One tensor of a segment: host memory owned by the caller, kept alive and
@@ -195,6 +196,16 @@ typedef struct ls_kernel_time {
     double total_ms;
 } ls_kernel_time;
 
+/* One launch of the per-launch trace (kernel_timing = 2): times in ms from the
+ * first launch recorded since the previous ls_sync. */
+typedef struct ls_trace_event {
+    char name[32];
+    int32_t stream;            /* 0 = the caller's (compute) stream, 1 = the context's copy stream */
+    int32_t segment;           /* segment the launch belongs to, -1 if none */
+    double start_ms;
+    double end_ms;
+} ls_trace_event;
+
 typedef struct ls_ctx ls_ctx;
 
 /* Fill *p with defaults (struct_size = sizeof(ls_params), version = 1). */
@@ -251,6 +262,9 @@ ls_status ls_get_stats(ls_ctx* ctx, ls_stats* out);
 /* Copy up to cap kernel-time records into out; *n_out = number of classes.
  * reset != 0 clears the accumulators afterwards. */
 ls_status ls_get_kernel_times(ls_ctx* ctx, ls_kernel_time* out, int32_t cap, int32_t* n_out, int32_t reset);
+
+/* Copy up to cap trace records of the passes completed by the last ls_sync. */
+ls_status ls_get_trace(ls_ctx* ctx, ls_trace_event* out, int64_t cap, int64_t* n_out);
 
 /* Release everything the context owns (pool, buffers, streams, registrations). NULL is a no-op. */
 void ls_ctx_destroy(ls_ctx* ctx);
