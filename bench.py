@@ -314,6 +314,7 @@ def run_ours(args, cfg, world, rank, local):
         "roofline_gemm": roof(gemm_name) if gemm_name else None,
         "kernels": kt,
         "gpu_launches": launches,
+        "step_ms": {"min": min(step_ms), "median": statistics.median(step_ms), "max": max(step_ms)},
         "clocks": {k: clocks[k] for k in ("sm_mhz", "sm_max_mhz", "reasons")},
         "e2e": {"value": e2e_tokens / e2e_max, "unit": UNIT, "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h},
         "copy_paths_gbs": {"kernel": stats["copy_kernel_gbs"], "engine": stats["copy_engine_gbs"]},

@@ -767,7 +767,12 @@ ls_status autotune_copy(ls_ctx* c) {
     const double bytes = (double)c->segs[seg].load_bytes;
     c->gbs_kernel = bytes / (best[0] * 1e-3) / 1e9;
     c->gbs_engine = bytes / (best[1] * 1e-3) / 1e9;
-    c->copy_path = forced != LS_COPY_AUTO ? forced : (best[0] <= best[1] ? LS_COPY_KERNEL : LS_COPY_ENGINE);
+    // The copy kernel occupies SM issue slots and registers next to the segment's GEMMs
+    // while the copy engine uses none, so AUTO keeps the kernel only when it is
+    // clearly faster on its own (by more than KERNEL_MARGIN).
+    constexpr double KERNEL_MARGIN = 1.15;
+    c->copy_path = forced != LS_COPY_AUTO ? forced
+                                          : (best[0] * KERNEL_MARGIN < best[1] ? LS_COPY_KERNEL : LS_COPY_ENGINE);
     return LS_OK;
 }
 
