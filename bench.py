@@ -137,35 +137,42 @@ def aggregate(step_seconds: float, units: float, world: int, device=None) -> tup
 
 
 # ---------------------------------------------------------------- oracle (CPU) timing
-def oracle_time(cfg, tokens: int, reps: int = 1) -> tuple:
-    """fp64 oracle forward of `tokens` rows through every segment; weights are
-    drawn and widened beforehand (generation excluded). Returns (seconds per
-    pass, cores used)."""
-    from oracle import stack as ostack
-    from oracle import forward as F
-    cores = len(os.sched_getaffinity(0))
-    rows = np.arange(tokens)
-    x0 = F.as_f64(synth.draw_x(cfg, tokens), cfg.dtype)
-    shared = ostack.shared_f64(cfg)[0] if cfg.kind == synth.KIND_FFN_GELU_SHARED_BF16 else None
-    segs = [ostack.segment_f64(cfg, s) for s in range(cfg.n_segments)] \
-        if cfg.kind != synth.KIND_MOE_SWIGLU_BF16 else [None] * cfg.n_segments
-    times = []
-    for _ in range(reps):
+class OracleRun:
+    """The fp64 oracle forward of `tokens` rows through every segment, with the
+    weights drawn and widened once beforehand (generation is not timed)."""
+
+    def __init__(self, cfg, tokens: int):
+        from oracle import forward as F
+        from oracle import stack as ostack
+        self.cfg, self.ostack = cfg, ostack
+        self.rows = np.arange(tokens)
+        self.x0 = F.as_f64(synth.draw_x(cfg, tokens), cfg.dtype)
+        self.shared = ostack.shared_f64(cfg)[0] if cfg.kind == synth.KIND_FFN_GELU_SHARED_BF16 else None
+        self.segs = [ostack.segment_f64(cfg, s) for s in range(cfg.n_segments)] \
+            if cfg.kind != synth.KIND_MOE_SWIGLU_BF16 else [None] * cfg.n_segments
+
+    def time_pass(self) -> float:
         t0 = time.perf_counter()
-        x = x0
-        for s in range(cfg.n_segments):
-            x = ostack.apply_segment(cfg, s, x, rows=rows, tensors=segs[s], shared=shared)
-        times.append(time.perf_counter() - t0)
-    return min(times), cores
+        x = self.x0
+        for s in range(self.cfg.n_segments):
+            x = self.ostack.apply_segment(self.cfg, s, x, rows=self.rows, tensors=self.segs[s],
+                                          shared=self.shared)
+        return time.perf_counter() - t0
+
+
+def oracle_time(cfg, tokens: int) -> tuple:
+    """(seconds of one oracle pass over `tokens` rows, cores used)."""
+    return OracleRun(cfg, tokens).time_pass(), len(os.sched_getaffinity(0))
 
 
 def run_reference(args, cfg, world, rank):
     if rank != 0:
         return 0
     tokens = args.ref_tokens
+    run = OracleRun(cfg, tokens)
     for _ in range(args.warmup):
-        oracle_time(cfg, tokens)
-    secs = [oracle_time(cfg, tokens)[0] for _ in range(args.steps)]
+        run.time_pass()
+    secs = [run.time_pass() for _ in range(args.steps)]
     cores = len(os.sched_getaffinity(0))
     mean = statistics.mean(secs)
     value = tokens / mean
@@ -279,7 +286,8 @@ def run_ours(args, cfg, world, rank, local):
     launches = sum(v["launches"] for k, v in kt.items() if k != "copy_engine")
     if "copy_engine" in kt:
         launches += kt["copy_engine"]["launches"]  # one publish kernel per copy-engine load
-    dominant = max(kt, key=lambda k: kt[k]["total_ms"]) if kt else None
+    kernels_only = [k for k in kt if k != "copy_engine"]  # the copy engine is not a kernel
+    dominant = max(kernels_only, key=lambda k: kt[k]["total_ms"]) if kernels_only else None
     kf = kernel_flops(cfg, T)
     per_load = link_bytes / max(1, sum(1 for e in sched if e[2] in (L.LS_EV_PREFETCH, L.LS_EV_LOAD_SYNC)) / args.steps)
     def roof(name):

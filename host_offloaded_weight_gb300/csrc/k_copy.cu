@@ -23,11 +23,13 @@
 namespace ls {
 
 // One chunk = CHUNK_UNITS 16-byte units of one range.
-static constexpr int COPY_THREADS = 512;
+// 256 threads x 8 loads of 16 B in flight: small enough (about 16K registers per
+// CTA) to sit on an SM next to a GEMM CTA.
+static constexpr int COPY_THREADS = 256;
 static constexpr int COPY_UNROLL = 8;
 static constexpr int64_t CHUNK_UNITS = (int64_t)COPY_THREADS * COPY_UNROLL;
 
-__global__ void __launch_bounds__(COPY_THREADS)
+__global__ void __launch_bounds__(COPY_THREADS, 4)
 copy_h2slot_kernel(const CopyRange* __restrict__ ranges, int n_ranges, int64_t n_chunks,
                    uint8_t* __restrict__ dst_base, const uint8_t* __restrict__ group_mask, int ranges_per_group,
                    uint32_t* ready, uint32_t* ticket, uint32_t epoch, int publish) {

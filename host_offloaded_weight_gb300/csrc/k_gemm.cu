@@ -2,7 +2,7 @@
 // accumulation in tensor memory, with the segment's elementwise work fused into
 // the epilogue (bias, GELU, residual add, SiLU-gated product, routing weight).
 //
-// Structure (one persistent CTA per SM, 192 threads):
+// Structure (one persistent CTA per SM, 320 threads):
 //   warp 0     TMA producer: 128x64 A tile and 256x64 B tile (or two 128x64 B
 //              tiles for the gate/up pair) per stage, 128-byte swizzle, into a
 //              4-stage shared-memory ring guarded by full/empty mbarriers.
@@ -10,9 +10,12 @@
 //              issues tcgen05.mma (M=128, K=16 per instruction) from one thread;
 //              tcgen05.commit releases smem stages and hands finished
 //              accumulators to the epilogue.
-//   warps 2-5  epilogue: tcgen05.ld of their 32 TMEM lanes (one output row per
-//              thread), fused elementwise work, 16-byte stores. The second
-//              accumulator lets the next tile's mainloop run meanwhile.
+//   warps 2-9  epilogue: two warps per TMEM lane quarter, each taking half of
+//              the tile's columns: tcgen05.ld of its 32 lanes (one output row
+//              per thread), fused elementwise work, 16-byte stores. Two warps
+//              per sub-partition hide the latency of the GELU and of the
+//              residual loads; the second accumulator lets the next tile's
+//              mainloop run meanwhile.
 // Tiles are visited in a fixed order and each output element is produced by
 // one thread from one fixed-order accumulation, so results do not depend on
 // the grid size or on where the weights live.
@@ -23,7 +26,8 @@
 //
 // Every mbarrier wait is bounded in time; on expiry the CTA records an error
 // word, stops issuing work, waits (bounded) for its own copies and MMAs, frees
-// its TMEM and exits.
+// its TMEM and exits. The GEMM never waits on another kernel: a persistent
+// grid that spins on a flag would hold the SMs its producer needs.
 #include <cuda.h>
 
 #include "common.cuh"
@@ -42,9 +46,10 @@ constexpr int STAGES = 4;
 constexpr int A_BYTES = BM * BK * 2;
 constexpr int B_BYTES = ACC_COLS * BK * 2;
 constexpr int STAGE_BYTES = A_BYTES + B_BYTES;
-constexpr int NUM_THREADS = 192;
+constexpr int EPI_WARPS = 8;
+constexpr int NUM_THREADS = 64 + 32 * EPI_WARPS;
 constexpr int SMEM_BYTES = STAGES * STAGE_BYTES + 1024 + 256;
-constexpr uint64_t MBAR_LIMIT_NS = 2000000000ull;  // 2 s beyond any ready-word wait: far above a legitimate stall
+constexpr uint64_t MBAR_LIMIT_NS = 2000000000ull;  // 2 s: far above any legitimate stall
 constexpr int MAX_GROUPS = 256;
 
 struct GemmParams {
@@ -66,11 +71,7 @@ struct GemmParams {
     int b_base_row;
     const int* row_table;
     const float* row_weight;
-    const uint32_t* ready;
-    uint32_t epoch;
-    uint64_t wait_ns;
     uint32_t* err;
-    uint32_t wait_code;
     uint64_t mbar_limit_ns;  // bound of every internal mbarrier wait
 };
 
@@ -355,7 +356,7 @@ __global__ void __launch_bounds__(NUM_THREADS, 1) gemm_bf16_tc(const __grid_cons
         }
         for (int b = 0; b < 2; ++b) {
             mbar_init(tfull_bar(b), 1);
-            mbar_init(tempty_bar(b), 128);
+            mbar_init(tempty_bar(b), 32 * EPI_WARPS);
         }
         mbar_init(done_bar, 1);
         asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
@@ -389,17 +390,6 @@ __global__ void __launch_bounds__(NUM_THREADS, 1) gemm_bf16_tc(const __grid_cons
             tma_prefetch_desc(&p.tmA);
             tma_prefetch_desc(&p.tmB);
             bool ok = true;
-            if (p.ready) {  // the weights this GEMM reads arrive through a ready word
-                const uint64_t t0 = globaltimer_ns();
-                while (ld_acquire_gpu(p.ready) != p.epoch) {
-                    if (*(volatile uint32_t*)p.err || globaltimer_ns() - t0 > p.wait_ns) {
-                        raise_error(p.err, p.wait_code);
-                        break;
-                    }
-                    __nanosleep(64);
-                }
-                asm volatile("fence.proxy.async.global;" ::: "memory");
-            }
             int it = 0;
             uint32_t issued_mask = 0;
             for (int t = blockIdx.x; t < num_tiles && ok; t += gridDim.x) {
@@ -480,8 +470,9 @@ __global__ void __launch_bounds__(NUM_THREADS, 1) gemm_bf16_tc(const __grid_cons
             mbar_wait(done_bar, 0, p.err, 6, p.mbar_limit_ns);
         }
     } else {
-        // ------------------------------------------------------------ epilogue (warps 2..5)
+        // ------------------------------------------------------------ epilogue (warps 2..9)
         const int q = warp & 3;                 // TMEM lane quarter this warp may read
+        const int half = (warp - 2) >> 2;       // which half of the tile's columns
         const int row_in_tile = q * 32 + lane;
         int tcount = 0;
         for (int t = blockIdx.x; t < num_tiles; t += gridDim.x, ++tcount) {
@@ -497,8 +488,9 @@ __global__ void __launch_bounds__(NUM_THREADS, 1) gemm_bf16_tc(const __grid_cons
             const bool valid = row < tl.row_end && row < p.M;
             const uint32_t tbase = tmem_base + ((uint32_t)(q * 32) << 16) + (uint32_t)(buf * ACC_COLS);
             constexpr int CHUNKS = DUAL ? ACC_COLS / 64 : ACC_COLS / 32;
+            constexpr int PER_WARP = CHUNKS / (EPI_WARPS / 4);
 #pragma unroll 1
-            for (int c = 0; c < CHUNKS; ++c) {
+            for (int c = half * PER_WARP; c < (half + 1) * PER_WARP; ++c) {
                 uint32_t r[32], r2[32];
                 tmem_ld32(tbase + c * 32, r);
                 if (DUAL) tmem_ld32(tbase + ACC_COLS / 2 + c * 32, r2);
@@ -659,12 +651,8 @@ cudaError_t launch_gemm_bf16(const GemmDesc& d, int max_ctas, cudaStream_t s) {
     p.b_base_row = d.b_base_row;
     p.row_table = d.row_table;
     p.row_weight = d.row_weight;
-    p.ready = d.ready;
-    p.epoch = d.epoch;
-    p.wait_ns = d.wait_ns;
     p.err = d.err_word;
-    p.wait_code = d.wait_code;
-    p.mbar_limit_ns = MBAR_LIMIT_NS + (d.ready ? d.wait_ns : 0);
+    p.mbar_limit_ns = MBAR_LIMIT_NS;
     int tiles = p.num_tiles;
     if (grouped) {
         // sum over groups of ceil(rows/BM) <= M/BM + n_groups

@@ -63,12 +63,7 @@ struct GemmDesc {
     const int* row_table = nullptr;     // EPI_SCALE_F32: destination row of sorted row i
     const float* row_weight = nullptr;  // EPI_SCALE_F32: weight by destination row
     int max_tiles_hint = 0;             // grouped: upper bound of tiles (grid sizing)
-    // fused ready-word wait before the first weight load (optional)
-    const uint32_t* ready = nullptr;
-    uint32_t epoch = 0;
-    uint64_t wait_ns = 0;
-    uint32_t* err_word = nullptr;       // mapped host word for timeouts
-    uint32_t wait_code = 0;
+    uint32_t* err_word = nullptr;       // mapped host word for internal timeouts
 };
 
 // max_ctas <= 0: one CTA per SM.

@@ -329,21 +329,19 @@ void compute_segment(ls_ctx* c, const RunCtx& rc, int seg, bool wait) {
     const int slot = c->seg_slot[seg];
     const uint32_t epoch = c->seg_epoch[seg];
     const uint32_t code = DERR_HANDOFF_TIMEOUT | ((uint32_t)slot << 8);
-    GemmDesc w0;  // fused wait for the first kernel reading streamed weights
-    if (wait) {
-        w0.ready = c->ready + slot;
-        w0.epoch = epoch;
-        w0.wait_ns = rc.wait_ns;
-        w0.err_word = c->err_word_dev;
-        w0.wait_code = code;
-    }
+    // A prefetched segment's kernels start behind a one-CTA wait on the slot's
+    // ready word. The wait is its own launch: a spinning waiter must hold almost
+    // nothing, so the copy it waits for can always find SMs to run on.
+    auto wait_slot = [&]() {
+        KTime kt(c, "wait_ready", rc.s);
+        track(c, launch_wait_ready(c->ready + slot, epoch, rc.wait_ns, c->err_word_dev, code, rc.s));
+    };
+    GemmDesc w0;
+    w0.err_word = c->err_word_dev;
     const int ctas = gemm_ctas(c);
     switch (c->kind) {
         case LS_KIND_LINEAR_GELU_F32: {
-            if (wait) {
-                KTime kt(c, "wait_ready", rc.s);
-                track(c, launch_wait_ready(c->ready + slot, epoch, rc.wait_ns, c->err_word_dev, code, rc.s));
-            }
+            if (wait) wait_slot();
             KTime kt(c, "linear_gelu_f32", rc.s);
             track(c, launch_linear_gelu_f32((const float*)xin, (const float*)tptr(c, seg, 0),
                                             (const float*)tptr(c, seg, 1), (float*)xout, T, H, F, rc.s));
@@ -354,17 +352,20 @@ void compute_segment(ls_ctx* c, const RunCtx& rc, int seg, bool wait) {
             const bool proj = c->kind == LS_KIND_FFN_GELU_SHARED_BF16;
             const int o = proj ? 1 : 0;
             const void* a1 = xin;
-            if (proj) {
+            if (proj) {  // reads only the resident shared projection: runs before the wait
+
                 GemmDesc g;
                 g.epi = EPI_STORE;
                 g.A = xin; g.lda = H; g.a_rows = T;
                 g.B = tptr(c, seg, 0); g.ldb = H; g.b_rows = H;
                 g.M = T; g.N = H; g.K = H;
                 g.C = c->ubuf; g.ldc = H;
+                g.err_word = c->err_word_dev;
                 KTime kt(c, "gemm_proj", rc.s);
                 track(c, launch_gemm_bf16(g, ctas, rc.s));
                 a1 = c->ubuf;
             }
+            if (wait) wait_slot();
             GemmDesc g1 = w0;
             g1.epi = EPI_BIAS_GELU;
             g1.A = a1; g1.lda = H; g1.a_rows = T;
@@ -376,7 +377,7 @@ void compute_segment(ls_ctx* c, const RunCtx& rc, int seg, bool wait) {
                 KTime kt(c, "gemm_up", rc.s);
                 track(c, launch_gemm_bf16(g1, ctas, rc.s));
             }
-            GemmDesc g2;
+            GemmDesc g2 = w0;
             g2.epi = EPI_BIAS_RESID;
             g2.A = c->hbuf; g2.lda = F; g2.a_rows = T;
             g2.B = tptr(c, seg, o + 2); g2.ldb = F; g2.b_rows = H;
@@ -389,6 +390,7 @@ void compute_segment(ls_ctx* c, const RunCtx& rc, int seg, bool wait) {
             break;
         }
         case LS_KIND_SWIGLU_BF16: {
+            if (wait) wait_slot();
             GemmDesc g1 = w0;
             g1.epi = EPI_SWIGLU;
             g1.A = xin; g1.lda = H; g1.a_rows = T;
@@ -400,7 +402,7 @@ void compute_segment(ls_ctx* c, const RunCtx& rc, int seg, bool wait) {
                 KTime kt(c, "gemm_up", rc.s);
                 track(c, launch_gemm_bf16(g1, ctas, rc.s));
             }
-            GemmDesc g2;
+            GemmDesc g2 = w0;
             g2.epi = EPI_RESID;
             g2.A = c->hbuf; g2.lda = F; g2.a_rows = T;
             g2.B = tptr(c, seg, 2); g2.ldb = F; g2.b_rows = H;
@@ -422,6 +424,7 @@ void compute_segment(ls_ctx* c, const RunCtx& rc, int seg, bool wait) {
             }
             const int64_t eb = c->segs[seg].slot_bytes / E;  // bytes per expert (G, U, D packed)
             const void* base = c->seg_ptr[seg];
+            if (wait) wait_slot();
             GemmDesc g1 = w0;
             g1.epi = EPI_SWIGLU;
             g1.A = c->moe_xs; g1.lda = H; g1.a_rows = rows;
@@ -436,7 +439,7 @@ void compute_segment(ls_ctx* c, const RunCtx& rc, int seg, bool wait) {
                 KTime kt(c, "gemm_up", rc.s);
                 track(c, launch_gemm_bf16(g1, ctas, rc.s));
             }
-            GemmDesc g2;
+            GemmDesc g2 = w0;
             g2.epi = EPI_SCALE_F32;
             g2.A = c->moe_hs; g2.lda = F; g2.a_rows = rows;
             g2.B = base; g2.ldb = F; g2.b_rows = c->segs[seg].slot_bytes / (2 * (int64_t)F);
