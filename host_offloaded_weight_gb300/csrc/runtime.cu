@@ -200,13 +200,22 @@ struct KTime {
             c->tclass.push_back({name, 0, 0});
             cls = (int)c->tclass.size() - 1;
         }
-        if (c->tev_used == c->tev.size()) {
-            cudaEvent_t a, b;
-            if (cudaEventCreate(&a) != cudaSuccess || cudaEventCreate(&b) != cudaSuccess) return;
-            c->tev.push_back({a, b});
-            c->tev_class.push_back(cls);
-            c->tev_stream.push_back(0);
-            c->tev_seg.push_back(-1);
+        if (c->tev_used == c->tev.size()) {  // grow the pool in batches, not per launch
+            const size_t grow = c->tev.empty() ? 4096 : c->tev.size();
+            for (size_t g = 0; g < grow; ++g) {
+                cudaEvent_t a, b;
+                if (cudaEventCreate(&a) != cudaSuccess) break;
+                if (cudaEventCreate(&b) != cudaSuccess) {
+                    cudaEventDestroy(a);
+                    break;
+                }
+                c->tev.push_back({a, b});
+                c->tev_class.push_back(-1);
+                c->tev_stream.push_back(0);
+                c->tev_seg.push_back(-1);
+            }
+            cudaGetLastError();
+            if (c->tev_used == c->tev.size()) return;
         }
         idx = c->tev_used++;
         c->tev_class[idx] = cls;
@@ -572,18 +581,19 @@ ls_status check_params(const ls_params* p, ls_params* out, std::string* why) {
     return LS_OK;
 }
 
-// Pin and map every host range that is not pinned yet (merged by page).
+// Pin and map every host range that is not pinned yet. Exactly the tensors'
+// bytes are registered (ranges that overlap or touch are merged), never whole
+// pages: a page-rounded range would also register the neighbouring bytes of
+// other allocations, and a copy of the caller's that straddles the end of a
+// registered range is refused by the driver.
 ls_status pin_host(ls_ctx* c, std::vector<std::pair<const void*, uint64_t>>& ranges) {
-    const uintptr_t PG = 4096;
     std::vector<std::pair<uintptr_t, uintptr_t>> todo;
     for (auto& r : ranges) {
         if (!r.first || !r.second) continue;
         cudaPointerAttributes a;
         if (cudaPointerGetAttributes(&a, r.first) == cudaSuccess && a.type == cudaMemoryTypeHost) continue;
         cudaGetLastError();
-        uintptr_t b = (uintptr_t)r.first & ~(PG - 1);
-        uintptr_t e = ((uintptr_t)r.first + r.second + PG - 1) & ~(PG - 1);
-        todo.push_back({b, e});
+        todo.push_back({(uintptr_t)r.first, (uintptr_t)r.first + r.second});
     }
     std::sort(todo.begin(), todo.end());
     std::vector<std::pair<uintptr_t, uintptr_t>> merged;

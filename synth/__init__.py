@@ -31,6 +31,7 @@ Weights are row-major ``[out, in]`` (PyTorch's linear layout); activations are
 from __future__ import annotations
 
 import math
+import mmap
 import os
 from concurrent.futures import ThreadPoolExecutor
 from dataclasses import dataclass, field, replace
@@ -288,11 +289,9 @@ class HostStack:
         seg_bytes = segment_slot_bytes(cfg)
         sh_bytes = sum(align256(t.nbytes) for t in sh)
         total = n * seg_bytes + sh_bytes
-        page = 4096
-        raw = np.empty(total + page, np.uint8)
-        off0 = (-raw.ctypes.data) % page
-        self.buffer = raw[off0:off0 + total]
-        self._raw = raw
+        # anonymous pages of its own: nothing else lives in the buffer's pages
+        self._map = mmap.mmap(-1, max(total, 1))
+        self.buffer = np.frombuffer(self._map, dtype=np.uint8, count=total)
         self.shared_views = []
         o = n * seg_bytes
         for t in sh:

@@ -21,3 +21,18 @@ def pytest_collection_modifyitems(config, items):
     for it in items:
         if "gpu" in it.keywords:
             it.add_marker(skip)
+
+
+@pytest.fixture(autouse=True)
+def _cuda_state_is_clean(request):
+    """Every GPU test starts and ends with a usable CUDA state (a pending error
+    left by one test must not be charged to the next)."""
+    if "gpu" not in request.keywords:
+        yield
+        return
+    import torch
+    torch.ones(1, device="cuda").add_(1)
+    torch.cuda.synchronize()
+    yield
+    torch.ones(1, device="cuda").add_(1)
+    torch.cuda.synchronize()
