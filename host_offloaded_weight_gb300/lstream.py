@@ -116,6 +116,8 @@ _sig = {
     "lsk_device_error": (_U32, []),
     "lsk_copy_h2slot": (_I32, [_P, _P, _U64, _I32, _P, _P, _U32, _P]),
     "lsk_wait_ready": (_I32, [_P, _U32, _I32, _P, _I32, _P]),
+    "lsk_copy_h2slot_static": (_I32, [_P, C.POINTER(_P), C.POINTER(_U64), C.POINTER(_U64), _I32, _I32, _P,
+                                      _U32, _P]),
     "lsk_gemm_bf16": (_I32, [_I32, _P, _P, _I64, _I32, _P, _P, _I32, _P, _P, _I32, _I32, _I32, _I32, _P]),
     "lsk_gemm_grouped_bf16": (_I32, [_I32, _P, _P, _I64, _I32, _I32, _I32, _P, _I32, _P, _P, _P,
                                      _I32, _I32, _I32, _I32, _P]),
@@ -359,6 +361,20 @@ def lsk_device_error() -> int:
 def lsk_copy_h2slot(dst, src_host, nbytes: int, ctas: int, ready, ticket, epoch: int, stream=None) -> int:
     return _check(_lib.lsk_copy_h2slot(_ptr(dst), _ptr(src_host), int(nbytes), ctas, _ptr(ready),
                                        _ptr(ticket), epoch, _stream(stream)))
+
+
+LSK_STATIC_MAX_RANGES = 64
+
+
+def lsk_copy_h2slot_static(dst, srcs, sizes, dst_offsets, ctas: int, ready, epoch: int, stream=None) -> int:
+    """The copy and publish of lsk_copy_h2slot for up to 64 pinned host ranges,
+    without allocating device memory (its scratch is a fixed array in the library)."""
+    n = len(srcs)
+    src_arr = (_P * max(1, n))(*[_ptr(s) for s in srcs])
+    sz = (_U64 * max(1, n))(*[int(b) for b in sizes])
+    off = (_U64 * max(1, n))(*[int(o) for o in dst_offsets])
+    return _check(_lib.lsk_copy_h2slot_static(_ptr(dst), src_arr, sz, off, n, ctas, _ptr(ready), epoch,
+                                              _stream(stream)))
 
 
 def lsk_wait_ready(ready, epoch: int, limit_ms: int, err_host, slot: int = 0, stream=None) -> int:

@@ -48,6 +48,36 @@ uint32_t lsk_device_error(void);
 ls_status lsk_copy_h2slot(void* dst_dev, const void* src_host, uint64_t bytes, int32_t ctas,
                           uint32_t* ready_dev, uint32_t* ticket_dev, uint32_t epoch, void* stream);
 
+/* lsk_copy_h2slot for callers that cannot allocate device memory: callers
+ * whose device memory is all owned by another allocator (a framework's caching
+ * pool holding the card), and latency-critical loops that must not call
+ * cudaMalloc/cudaFree because those can synchronise the device. The pages have
+ * no counterpart of this call; it is an interface convenience of this library.
+ *
+ * It copies n_ranges host ranges (src_hosts[i], bytes[i]) to dst_dev +
+ * dst_offsets[i] with the same copy kernel, then raises ready_dev[0] = epoch
+ * after a system fence (last CTA). It allocates nothing: the range table and the
+ * CTAs' ticket word live in a fixed device array of LSK_STATIC_SCRATCH_BYTES
+ * bytes, defined in the library, that every device which loads the library
+ * holds until the process exits.
+ *   - n_ranges must be 1..LSK_STATIC_MAX_RANGES; more returns LS_ERR_INVALID_ARG
+ *     before any work is queued.
+ *   - Sources must be pinned and mapped, sources, dst_dev and the offsets
+ *     16-byte aligned (LS_ERR_INVALID_ARG otherwise).
+ *   - The first call on a device looks up the array's device address with that
+ *     device current (cudaGetSymbolAddress); make that first call before any
+ *     stream capture.
+ *   - Every call shares the one array per device and each call overwrites it
+ *     (the ticket is cleared by the call itself). Calls whose work overlaps on
+ *     the GPU (different streams, no ordering between them) race on the array.
+ *   - The range table is copied from a host array on `stream` as pageable
+ *     memory; the call returns once that copy has been staged. */
+#define LSK_STATIC_MAX_RANGES 64
+#define LSK_STATIC_SCRATCH_BYTES (256 + 64 * 40)
+ls_status lsk_copy_h2slot_static(void* dst_dev, const void* const* src_hosts, const uint64_t* bytes,
+                                 const uint64_t* dst_offsets, int32_t n_ranges, int32_t ctas, uint32_t* ready_dev,
+                                 uint32_t epoch, void* stream);
+
 /* One thread waits until ready_dev[0] == epoch, at most limit_ms; on expiry it
  * writes err_host[0] (pinned, mapped host memory) = 1 | (slot << 8) and returns. */
 ls_status lsk_wait_ready(const uint32_t* ready_dev, uint32_t epoch, int32_t limit_ms, uint32_t* err_host,
