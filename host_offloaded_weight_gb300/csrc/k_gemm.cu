@@ -12,10 +12,10 @@
 //              accumulators to the epilogue.
 //   warps 2-9  epilogue: two warps per TMEM lane quarter, each taking half of
 //              the tile's columns: tcgen05.ld of its 32 lanes (one output row
-//              per thread), fused elementwise work, 16-byte stores. Two warps
-//              per sub-partition hide the latency of the GELU and of the
-//              residual loads; the second accumulator lets the next tile's
-//              mainloop run meanwhile.
+//              per thread), fused elementwise work in registers, then a 32x32
+//              transpose through a swizzled shared buffer so that residual
+//              loads and output stores are coalesced row segments. The second
+//              accumulator lets the next tile's mainloop run meanwhile.
 // Tiles are visited in a fixed order and each output element is produced by
 // one thread from one fixed-order accumulation, so results do not depend on
 // the grid size or on where the weights live.
@@ -48,7 +48,8 @@ constexpr int B_BYTES = ACC_COLS * BK * 2;
 constexpr int STAGE_BYTES = A_BYTES + B_BYTES;
 constexpr int EPI_WARPS = 8;
 constexpr int NUM_THREADS = 64 + 32 * EPI_WARPS;
-constexpr int SMEM_BYTES = STAGES * STAGE_BYTES + 1024 + 256;
+constexpr int EPI_BUF_BYTES = 32 * 32 * 4;  // one 32x32 fp32 transpose buffer per epilogue warp
+constexpr int SMEM_BYTES = STAGES * STAGE_BYTES + EPI_WARPS * EPI_BUF_BYTES + 1024 + 256;
 constexpr uint64_t MBAR_LIMIT_NS = 2000000000ull;  // 2 s: far above any legitimate stall
 constexpr int MAX_GROUPS = 256;
 
@@ -227,105 +228,101 @@ __device__ __forceinline__ float bf2f(uint16_t h) { return __uint_as_float((uint
 __device__ __forceinline__ float gelu_f(float v) { return 0.5f * v * (1.0f + erff(v * 0.70710678118654752f)); }
 __device__ __forceinline__ float silu_f(float v) { return v / (1.0f + __expf(-v)); }
 
-// Epilogue of one 32-column chunk of one row.
+// 32x32 fp32 staging of one warp, held as 32 rows x 8 float4 and XOR-swizzled
+// at float4 granularity: float4 (r, c4) sits at r*8 + (c4 ^ (r & 7)). Row-wise
+// writes (lane r writes its row) and row-segment reads (8 lanes read one row)
+// are both free of bank conflicts within each quarter-warp phase.
+__device__ __forceinline__ int sw4(int r, int c4) { return r * 8 + (c4 ^ (r & 7)); }
+
+// Epilogue of one 32x32 chunk: lane l holds row row0 + l of the chunk in v[]
+// (and u[] for the gate/up pair), columns n .. n+31. Elementwise work runs
+// row-wise in registers; everything that touches global memory goes through
+// the warp's staging buffer, so each instruction reads or writes four whole
+// 32-column row segments with 16-byte (fp32) or 8-byte (bf16) accesses per lane.
 template <int EPI>
-__device__ __forceinline__ void epilogue_chunk(const GemmParams& p, int row, int n, const float* v,
-                                               const float* u, int out_row) {
-    if (EPI == EPI_SCALE_F32) {
-        const int dst = p.row_table[out_row];
-        const float w = p.row_weight[dst];
-        float* c = reinterpret_cast<float*>(p.C) + (int64_t)dst * p.ldc + n;
-        if (n + 32 <= p.N) {
-#pragma unroll
-            for (int j = 0; j < 32; j += 4)
-                *reinterpret_cast<float4*>(c + j) = make_float4(w * v[j], w * v[j + 1], w * v[j + 2], w * v[j + 3]);
-        } else {
-            for (int j = 0; j < 32 && n + j < p.N; ++j) c[j] = w * v[j];
-        }
-        return;
-    }
-    float o[32];
-    const bool full = n + 32 <= p.N;
+__device__ __forceinline__ void epilogue_chunk(const GemmParams& p, int row0, int row_end, int n, float* v,
+                                               const float* u, float* buf) {
+    const int lane = threadIdx.x & 31;
+    float4* b4 = reinterpret_cast<float4*>(buf);
+    const int c4 = lane & 7;              // this lane's float4 column in the transposed phase
+    const int col = n + 4 * c4;           // N % 8 == 0, so a group of 4 never straddles N
+    const bool col_ok = col < p.N;
     if (EPI == EPI_BIAS_GELU || EPI == EPI_BIAS_RESID) {
         const uint16_t* bb = reinterpret_cast<const uint16_t*>(p.bias) + n;
-        if (full) {
+        if (n + 32 <= p.N) {
 #pragma unroll
             for (int j = 0; j < 32; j += 8) {
                 uint4 q = *reinterpret_cast<const uint4*>(bb + j);
                 const uint16_t* h = reinterpret_cast<const uint16_t*>(&q);
 #pragma unroll
-                for (int i = 0; i < 8; ++i) o[j + i] = v[j + i] + bf2f(h[i]);
+                for (int i = 0; i < 8; ++i) v[j + i] += bf2f(h[i]);
             }
         } else {
-            for (int j = 0; j < 32; ++j) o[j] = v[j] + (n + j < p.N ? bf2f(bb[j]) : 0.f);
+            for (int j = 0; j < 32; ++j) v[j] += (n + j < p.N ? bf2f(bb[j]) : 0.f);
         }
-    } else {
-#pragma unroll
-        for (int j = 0; j < 32; ++j) o[j] = v[j];
     }
     if (EPI == EPI_BIAS_GELU) {
 #pragma unroll
-        for (int j = 0; j < 32; ++j) o[j] = gelu_f(o[j]);
+        for (int j = 0; j < 32; ++j) v[j] = gelu_f(v[j]);
     }
     if (EPI == EPI_SWIGLU) {
 #pragma unroll
-        for (int j = 0; j < 32; ++j) o[j] = silu_f(o[j]) * u[j];
+        for (int j = 0; j < 32; ++j) v[j] = silu_f(v[j]) * u[j];
     }
     if (EPI == EPI_BIAS_RESID || EPI == EPI_RESID) {
-        if (p.resid_f32) {
-            const float* rr = reinterpret_cast<const float*>(p.resid) + (int64_t)row * p.ldr + n;
-            if (full) {
+        float4 rv[8];
 #pragma unroll
-                for (int j = 0; j < 32; j += 4) {
-                    const float4 q = *reinterpret_cast<const float4*>(rr + j);
-                    o[j] += q.x;
-                    o[j + 1] += q.y;
-                    o[j + 2] += q.z;
-                    o[j + 3] += q.w;
+        for (int it = 0; it < 8; ++it) {  // all eight loads in flight before any use
+            const int row = row0 + it * 4 + (lane >> 3);
+            rv[it] = make_float4(0.f, 0.f, 0.f, 0.f);
+            if (row < row_end && col_ok) {
+                if (p.resid_f32) {
+                    rv[it] = *reinterpret_cast<const float4*>(reinterpret_cast<const float*>(p.resid) +
+                                                              (int64_t)row * p.ldr + col);
+                } else {
+                    const uint2 h = *reinterpret_cast<const uint2*>(reinterpret_cast<const uint16_t*>(p.resid) +
+                                                                    (int64_t)row * p.ldr + col);
+                    rv[it] = make_float4(bf2f(h.x & 0xffff), bf2f(h.x >> 16), bf2f(h.y & 0xffff), bf2f(h.y >> 16));
                 }
-            } else {
-                for (int j = 0; j < 32; ++j)
-                    if (n + j < p.N) o[j] += rr[j];
             }
+        }
+#pragma unroll
+        for (int it = 0; it < 8; ++it) b4[sw4(it * 4 + (lane >> 3), c4)] = rv[it];
+        __syncwarp();
+#pragma unroll
+        for (int j = 0; j < 8; ++j) {
+            const float4 t = b4[sw4(lane, j)];
+            v[4 * j] += t.x;
+            v[4 * j + 1] += t.y;
+            v[4 * j + 2] += t.z;
+            v[4 * j + 3] += t.w;
+        }
+        __syncwarp();
+    }
+#pragma unroll
+    for (int j = 0; j < 8; ++j) b4[sw4(lane, j)] = make_float4(v[4 * j], v[4 * j + 1], v[4 * j + 2], v[4 * j + 3]);
+    __syncwarp();
+#pragma unroll
+    for (int it = 0; it < 8; ++it) {
+        const int row = row0 + it * 4 + (lane >> 3);
+        if (row >= row_end || !col_ok) continue;
+        const float4 o = b4[sw4(it * 4 + (lane >> 3), c4)];
+        if (EPI == EPI_SCALE_F32) {
+            const int dst = p.row_table[row];
+            const float w = p.row_weight[dst];
+            *reinterpret_cast<float4*>(reinterpret_cast<float*>(p.C) + (int64_t)dst * p.ldc + col) =
+                make_float4(w * o.x, w * o.y, w * o.z, w * o.w);
         } else {
-            const uint16_t* rr = reinterpret_cast<const uint16_t*>(p.resid) + (int64_t)row * p.ldr + n;
-            if (full) {
-#pragma unroll
-                for (int j = 0; j < 32; j += 8) {
-                    uint4 q = *reinterpret_cast<const uint4*>(rr + j);
-                    const uint16_t* h = reinterpret_cast<const uint16_t*>(&q);
-#pragma unroll
-                    for (int i = 0; i < 8; ++i) o[j + i] += bf2f(h[i]);
-                }
-            } else {
-                for (int j = 0; j < 32; ++j)
-                    if (n + j < p.N) o[j] += bf2f(rr[j]);
-            }
-        }
-        if (p.C32) {  // the fp32 residual stream carried to the next segment
-            float* c32 = p.C32 + (int64_t)out_row * p.ldc + n;
-            if (full) {
-#pragma unroll
-                for (int j = 0; j < 32; j += 4)
-                    *reinterpret_cast<float4*>(c32 + j) = make_float4(o[j], o[j + 1], o[j + 2], o[j + 3]);
-            } else {
-                for (int j = 0; j < 32 && n + j < p.N; ++j) c32[j] = o[j];
-            }
+            if ((EPI == EPI_BIAS_RESID || EPI == EPI_RESID) && p.C32)
+                *reinterpret_cast<float4*>(p.C32 + (int64_t)row * p.ldc + col) = o;
+            __nv_bfloat162 lo = __floats2bfloat162_rn(o.x, o.y), hi = __floats2bfloat162_rn(o.z, o.w);
+            uint2 pk;
+            pk.x = *reinterpret_cast<uint32_t*>(&lo);
+            pk.y = *reinterpret_cast<uint32_t*>(&hi);
+            *reinterpret_cast<uint2*>(reinterpret_cast<__nv_bfloat16*>(p.C) + (int64_t)row * p.ldc + col) = pk;
         }
     }
-    __nv_bfloat16* c = reinterpret_cast<__nv_bfloat16*>(p.C) + (int64_t)out_row * p.ldc + n;
-    if (full) {
-#pragma unroll
-        for (int j = 0; j < 32; j += 8) {
-            uint4 q;
-            __nv_bfloat162* h2 = reinterpret_cast<__nv_bfloat162*>(&q);
-#pragma unroll
-            for (int i = 0; i < 4; ++i) h2[i] = __floats2bfloat162_rn(o[j + 2 * i], o[j + 2 * i + 1]);
-            *reinterpret_cast<uint4*>(c + j) = q;
-        }
-    } else {
-        for (int j = 0; j < 32 && n + j < p.N; ++j) c[j] = __float2bfloat16_rn(o[j]);
-    }
+    __syncwarp();
 }
 
 template <int EPI, bool DUAL, bool GROUPED>
@@ -334,14 +331,15 @@ __global__ void __launch_bounds__(NUM_THREADS, 1) gemm_bf16_tc(const __grid_cons
     const uint32_t raw = smem_u32(smem_raw);
     const uint32_t base = (raw + 1023u) & ~1023u;
     uint8_t* gbase = smem_raw + (base - raw);
-    const uint32_t bar0 = base + STAGES * STAGE_BYTES;
+    const uint32_t bar0 = base + STAGES * STAGE_BYTES + EPI_WARPS * EPI_BUF_BYTES;
     // barrier layout: full[S], empty[S], tfull[2], tempty[2], done; then tmem base word
     auto full_bar = [&](int s) { return bar0 + 8u * s; };
     auto empty_bar = [&](int s) { return bar0 + 8u * (STAGES + s); };
     auto tfull_bar = [&](int b) { return bar0 + 8u * (2 * STAGES + b); };
     auto tempty_bar = [&](int b) { return bar0 + 8u * (2 * STAGES + 2 + b); };
     const uint32_t done_bar = bar0 + 8u * (2 * STAGES + 4);
-    uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(gbase + STAGES * STAGE_BYTES + 8 * (2 * STAGES + 5));
+    uint32_t* tmem_slot =
+        reinterpret_cast<uint32_t*>(gbase + STAGES * STAGE_BYTES + EPI_WARPS * EPI_BUF_BYTES + 8 * (2 * STAGES + 5));
     __shared__ int s_mt_prefix[MAX_GROUPS + 1];
     __shared__ volatile int s_abort;
 
@@ -473,7 +471,7 @@ __global__ void __launch_bounds__(NUM_THREADS, 1) gemm_bf16_tc(const __grid_cons
         // ------------------------------------------------------------ epilogue (warps 2..9)
         const int q = warp & 3;                 // TMEM lane quarter this warp may read
         const int half = (warp - 2) >> 2;       // which half of the tile's columns
-        const int row_in_tile = q * 32 + lane;
+        float* ebuf = reinterpret_cast<float*>(gbase + STAGES * STAGE_BYTES + (warp - 2) * EPI_BUF_BYTES);
         int tcount = 0;
         for (int t = blockIdx.x; t < num_tiles; t += gridDim.x, ++tcount) {
             const int buf = tcount & 1;
@@ -484,8 +482,8 @@ __global__ void __launch_bounds__(NUM_THREADS, 1) gemm_bf16_tc(const __grid_cons
             }
             tc_fence_after();
             const Tile tl = tile_of<GROUPED, DUAL>(p, t, s_mt_prefix);
-            const int row = tl.a_row + row_in_tile;
-            const bool valid = row < tl.row_end && row < p.M;
+            const int row0 = tl.a_row + q * 32;            // first row of this warp's 32
+            const int row_end = tl.row_end < p.M ? tl.row_end : p.M;
             const uint32_t tbase = tmem_base + ((uint32_t)(q * 32) << 16) + (uint32_t)(buf * ACC_COLS);
             constexpr int CHUNKS = DUAL ? ACC_COLS / 64 : ACC_COLS / 32;
             constexpr int PER_WARP = CHUNKS / (EPI_WARPS / 4);
@@ -496,14 +494,14 @@ __global__ void __launch_bounds__(NUM_THREADS, 1) gemm_bf16_tc(const __grid_cons
                 if (DUAL) tmem_ld32(tbase + ACC_COLS / 2 + c * 32, r2);
                 tmem_ld_wait();
                 const int n = tl.n0 + c * 32;
-                if (valid && n < p.N) {
+                if (n < p.N && row0 < row_end) {      // uniform across the warp
                     float v[32], u[32];
 #pragma unroll
                     for (int j = 0; j < 32; ++j) {
                         v[j] = __uint_as_float(r[j]);
                         u[j] = DUAL ? __uint_as_float(r2[j]) : 0.f;
                     }
-                    epilogue_chunk<EPI>(p, row, n, v, u, row);
+                    epilogue_chunk<EPI>(p, row0, row_end, n, v, u, ebuf);
                 }
             }
             tc_fence_before();
