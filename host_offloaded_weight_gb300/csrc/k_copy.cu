@@ -17,6 +17,10 @@
 // ("layer split: overlap the stages' hand-off", Changes since #936: bounded
 // wait, error word, the host fails the window). A wait that finds the error
 // word already set returns at once, so one lost hand-off costs one limit.
+#include <cuda.h>
+
+#include <mutex>
+
 #include "common.cuh"
 #include "kernels.h"
 
@@ -116,8 +120,37 @@ cudaError_t launch_copy_h2slot(const CopyRange* ranges_dev, int n_ranges, int64_
     return cudaGetLastError();
 }
 
+// After a copy-engine load the ready word is raised by a stream memory
+// operation: it runs in stream order after the copy, behind a memory barrier,
+// and needs no SM, so it is not held up by GEMM CTAs that fill every SM (a
+// publish kernel was, and the next copy queued behind it). If the driver does
+// not offer stream memory operations, a one-thread kernel publishes instead.
+typedef CUresult (*WriteValueFn)(CUstream, CUdeviceptr, cuuint32_t, unsigned int);
+
+static WriteValueFn write_value_fn() {
+    static WriteValueFn fn = nullptr;
+    static std::once_flag once;
+    std::call_once(once, [] {
+        void* p = nullptr;
+        cudaDriverEntryPointQueryResult q;
+        if (cudaGetDriverEntryPointByVersion("cuStreamWriteValue32", &p, 12000, cudaEnableDefault, &q) == cudaSuccess &&
+            q == cudaDriverEntryPointSuccess)
+            fn = reinterpret_cast<WriteValueFn>(p);
+        cudaGetLastError();
+    });
+    return fn;
+}
+
 cudaError_t launch_publish(uint32_t* ready, uint32_t epoch, bool publish, cudaStream_t s) {
-    publish_kernel<<<1, 1, 0, s>>>(ready, epoch, publish ? 1 : 0);
+    if (!publish) return cudaSuccess;  // the drop hook: the word stays down
+    static bool use_mem_op = true;
+    if (use_mem_op) {
+        WriteValueFn fn = write_value_fn();
+        if (fn && fn((CUstream)s, (CUdeviceptr)ready, epoch, CU_STREAM_WRITE_VALUE_DEFAULT) == CUDA_SUCCESS)
+            return cudaSuccess;
+        use_mem_op = false;
+    }
+    publish_kernel<<<1, 1, 0, s>>>(ready, epoch, 1);
     return cudaGetLastError();
 }
 

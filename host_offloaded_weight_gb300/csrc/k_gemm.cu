@@ -20,6 +20,10 @@
 // one thread from one fixed-order accumulation, so results do not depend on
 // the grid size or on where the weights live.
 //
+// Dense GEMMs with more than 128 rows use the pair-CTA form below (256x256 tiles
+// over a 2-CTA cluster); single-CTA 128x256 tiles serve the grouped mode and
+// short problems.
+//
 // Grouped mode (expert GEMM of the MoE stack): rows of A are already sorted by
 // expert; group g owns rows [group_bounds[g], group_bounds[g+1]) and reads its
 // own B matrix at row b_base_row + g * b_group_stride_rows of the B view.
@@ -101,10 +105,18 @@ __device__ __forceinline__ bool mbar_try_wait(uint32_t bar, uint32_t parity) {
         : "memory");
     return ok != 0;
 }
-// Bounded wait; false (with the error word set) if the phase did not complete in time.
-__device__ __noinline__ bool mbar_wait(uint32_t bar, uint32_t parity, uint32_t* err, uint32_t role,
-                                       uint64_t limit_ns) {
+// Bounded wait; false (with the error word set) if the phase did not complete in
+// time. The common case (phase already complete) stays inline: an out-of-line
+// call per k-block cost the MMA issuer about a third of its rate.
+__device__ __noinline__ bool mbar_wait_slow(uint32_t bar, uint32_t parity, uint32_t* err, uint32_t role,
+                                            uint64_t limit_ns);
+__device__ __forceinline__ bool mbar_wait(uint32_t bar, uint32_t parity, uint32_t* err, uint32_t role,
+                                          uint64_t limit_ns) {
     if (mbar_try_wait(bar, parity)) return true;
+    return mbar_wait_slow(bar, parity, err, role, limit_ns);
+}
+__device__ __noinline__ bool mbar_wait_slow(uint32_t bar, uint32_t parity, uint32_t* err, uint32_t role,
+                                            uint64_t limit_ns) {
     const uint64_t t0 = globaltimer_ns();
     while (!mbar_try_wait(bar, parity)) {
         if (globaltimer_ns() - t0 > limit_ns) {
@@ -395,7 +407,7 @@ __global__ void __launch_bounds__(NUM_THREADS, 1) gemm_bf16_tc(const __grid_cons
                 for (int kb = 0; kb < kb_n; ++kb, ++it) {
                     const int s = it % STAGES;
                     const uint32_t ph = (uint32_t)(it / STAGES) & 1u;
-                    if (!mbar_wait(empty_bar(s), ph ^ 1u, p.err, 1, p.mbar_limit_ns) || s_abort) {
+                    if (!mbar_wait(empty_bar(s), ph ^ 1u, p.err, 1, p.mbar_limit_ns)) {
                         ok = false;
                         s_abort = 1;
                         break;
@@ -440,7 +452,7 @@ __global__ void __launch_bounds__(NUM_THREADS, 1) gemm_bf16_tc(const __grid_cons
                 for (int kb = 0; kb < kb_n; ++kb, ++it) {
                     const int s = it % STAGES;
                     const uint32_t ph = (uint32_t)(it / STAGES) & 1u;
-                    if (!mbar_wait(full_bar(s), ph, p.err, 3, p.mbar_limit_ns) || s_abort) {
+                    if (!mbar_wait(full_bar(s), ph, p.err, 3, p.mbar_limit_ns)) {
                         ok = false;
                         s_abort = 1;
                         break;
@@ -516,6 +528,239 @@ __global__ void __launch_bounds__(NUM_THREADS, 1) gemm_bf16_tc(const __grid_cons
     }
 }
 
+// ------------------------------------------------------------------ pair-CTA (cta_group::2) kernel
+// A 2-CTA cluster computes a 256x256 tile: CTA r loads its 128 rows of A and
+// its 128 rows of B (for the gate/up pair: the leader the G half, the peer the
+// U half), so each SM takes in half of B; the even CTA issues
+// tcgen05.mma.cta_group::2 (M = 256) reading both CTAs' shared memory and
+// writing each CTA's 128 rows into that CTA's TMEM. Both CTAs' TMA loads
+// complete on the leader's full barrier; the leader's commits arrive on both
+// CTAs' barriers; both epilogues release the accumulator on the leader's
+// barrier. All waits are bounded, and both CTAs always reach the closing
+// cluster barrier before TMEM is freed.
+constexpr int S2_STAGES = 6;
+constexpr int S2_A = 128 * 64 * 2;             // this CTA's 128 rows of A
+constexpr int S2_B = 128 * 64 * 2;             // this CTA's half (128 rows) of B
+constexpr int S2_STAGE = S2_A + S2_B;
+constexpr int S2_SMEM = S2_STAGES * S2_STAGE + EPI_WARPS * EPI_BUF_BYTES + 1024 + 256;
+
+__device__ __forceinline__ uint32_t cluster_rank() {
+    uint32_t r;
+    asm volatile("mov.u32 %0, %%cluster_ctarank;" : "=r"(r));
+    return r;
+}
+__device__ __forceinline__ uint32_t mapa(uint32_t addr, uint32_t rank) {
+    uint32_t out;
+    asm volatile("mapa.shared::cluster.u32 %0, %1, %2;" : "=r"(out) : "r"(addr), "r"(rank));
+    return out;
+}
+__device__ __forceinline__ void cluster_sync() {
+    asm volatile("barrier.cluster.arrive.release.aligned;\n\tbarrier.cluster.wait.acquire.aligned;" ::: "memory");
+}
+__device__ __forceinline__ void remote_arrive(uint32_t cluster_addr) {
+    asm volatile("mbarrier.arrive.release.cluster.shared::cluster.b64 _, [%0];" ::"r"(cluster_addr) : "memory");
+}
+__device__ __forceinline__ void tma_load_2d_2sm(uint32_t dst, const CUtensorMap* map, uint32_t bar_cluster, int c0,
+                                                int c1) {
+    asm volatile(
+        "cp.async.bulk.tensor.2d.cta_group::2.shared::cluster.global.mbarrier::complete_tx::bytes"
+        " [%0], [%1, {%2, %3}], [%4];" ::"r"(dst),
+        "l"(reinterpret_cast<uint64_t>(map)), "r"(c0), "r"(c1), "r"(bar_cluster)
+        : "memory");
+}
+__device__ __forceinline__ void tmem_alloc2(uint32_t dst_smem, uint32_t ncols) {
+    asm volatile("tcgen05.alloc.cta_group::2.sync.aligned.shared::cta.b32 [%0], %1;" ::"r"(dst_smem), "r"(ncols)
+                 : "memory");
+}
+__device__ __forceinline__ void tmem_relinquish2() {
+    asm volatile("tcgen05.relinquish_alloc_permit.cta_group::2.sync.aligned;" ::: "memory");
+}
+__device__ __forceinline__ void tmem_dealloc2(uint32_t taddr, uint32_t ncols) {
+    asm volatile("tcgen05.dealloc.cta_group::2.sync.aligned.b32 %0, %1;" ::"r"(taddr), "r"(ncols) : "memory");
+}
+__device__ __forceinline__ void umma2_bf16(uint32_t d_tmem, uint64_t a_desc, uint64_t b_desc, uint32_t idesc,
+                                           uint32_t accumulate) {
+    asm volatile(
+        "{\n\t.reg .pred p;\n\t"
+        "setp.ne.b32 p, %4, 0;\n\t"
+        "tcgen05.mma.cta_group::2.kind::f16 [%0], %1, %2, %3, p;\n\t}" ::"r"(d_tmem),
+        "l"(a_desc), "l"(b_desc), "r"(idesc), "r"(accumulate)
+        : "memory");
+}
+__device__ __forceinline__ void umma2_commit_both(uint32_t bar) {
+    const uint16_t mask = 0x3;
+    asm volatile(
+        "tcgen05.commit.cta_group::2.mbarrier::arrive::one.shared::cluster.multicast::cluster.b64 [%0], %1;" ::"r"(bar),
+        "h"(mask)
+        : "memory");
+}
+
+template <int EPI, bool DUAL>
+__global__ void __launch_bounds__(NUM_THREADS, 1) gemm_bf16_tc2(const __grid_constant__ GemmParams p) {
+    extern __shared__ uint8_t smem_raw[];
+    const uint32_t raw = smem_u32(smem_raw);
+    const uint32_t base = (raw + 1023u) & ~1023u;
+    uint8_t* gbase = smem_raw + (base - raw);
+    const uint32_t bar0 = base + S2_STAGES * S2_STAGE + EPI_WARPS * EPI_BUF_BYTES;
+    auto full_bar = [&](int s) { return bar0 + 8u * s; };
+    auto empty_bar = [&](int s) { return bar0 + 8u * (S2_STAGES + s); };
+    auto tfull_bar = [&](int b) { return bar0 + 8u * (2 * S2_STAGES + b); };
+    auto tempty_bar = [&](int b) { return bar0 + 8u * (2 * S2_STAGES + 2 + b); };
+    const uint32_t done_bar = bar0 + 8u * (2 * S2_STAGES + 4);
+    uint32_t* tmem_slot =
+        reinterpret_cast<uint32_t*>(gbase + S2_STAGES * S2_STAGE + EPI_WARPS * EPI_BUF_BYTES + 8 * (2 * S2_STAGES + 5));
+    __shared__ volatile int s_abort;
+    const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+    const uint32_t rank = cluster_rank();
+    const bool leader = rank == 0;
+    const int cluster_id = blockIdx.x >> 1, n_clusters = gridDim.x >> 1;
+
+    if (threadIdx.x == 0) {
+        s_abort = 0;
+        for (int s = 0; s < S2_STAGES; ++s) {
+            mbar_init(full_bar(s), 1);
+            mbar_init(empty_bar(s), 1);
+        }
+        for (int b = 0; b < 2; ++b) {
+            mbar_init(tfull_bar(b), 1);
+            mbar_init(tempty_bar(b), 2 * 32 * EPI_WARPS);
+        }
+        mbar_init(done_bar, 1);
+        asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
+    }
+    if (warp == 1) {
+        tmem_alloc2(smem_u32(tmem_slot), 512);
+        tmem_relinquish2();
+    }
+    tc_fence_before();
+    cluster_sync();  // barriers of both CTAs initialised, TMEM allocated in both
+    tc_fence_after();
+    const uint32_t tmem_base = *tmem_slot;
+    const int num_m2 = (p.M + 255) / 256;
+    const int num_tiles = num_m2 * p.num_n_tiles;  // num_n_tiles counts 256 (dual: 128) columns
+    const int kb_n = p.num_k_blocks;
+
+    if (warp == 0) {
+        if (lane == 0) {
+            tma_prefetch_desc(&p.tmA);
+            tma_prefetch_desc(&p.tmB);
+            int it = 0;
+            uint32_t issued_mask = 0;
+            bool ok = true;
+            for (int t = cluster_id; t < num_tiles && ok; t += n_clusters) {
+                const int m2 = t % num_m2, n = t / num_m2;
+                const int a_row = m2 * 256 + (int)rank * 128;
+                // dense: the pair covers 256 columns; gate/up pair: 128 columns of G (leader) and of U (peer)
+                const int b_row = DUAL ? n * 128 + (rank ? p.b2_row_off : 0) : n * 256 + (int)rank * 128;
+                for (int kb = 0; kb < kb_n; ++kb, ++it) {
+                    const int s = it % S2_STAGES;
+                    const uint32_t ph = (uint32_t)(it / S2_STAGES) & 1u;
+                    if (!mbar_wait(empty_bar(s), ph ^ 1u, p.err, 1, p.mbar_limit_ns)) {
+                        ok = false;
+                        s_abort = 1;
+                        break;
+                    }
+                    const uint32_t sa = base + s * S2_STAGE;
+                    const uint32_t sb = sa + S2_A;
+                    const uint32_t leader_full = mapa(full_bar(s), 0);
+                    if (leader) mbar_expect_tx(full_bar(s), 2 * S2_STAGE);
+                    tma_load_2d_2sm(sa, &p.tmA, leader_full, kb * BK, a_row);
+                    tma_load_2d_2sm(sb, &p.tmB, leader_full, kb * BK, b_row);
+                    issued_mask |= 1u << s;
+                }
+            }
+            // the leader's full barrier tracks both CTAs' loads: drain there (leader only)
+            if (leader)
+                for (int s = 0; s < S2_STAGES; ++s) {
+                    if (!(issued_mask & (1u << s))) continue;
+                    int last = it - 1 - ((it - 1 - s) % S2_STAGES + S2_STAGES) % S2_STAGES;
+                    mbar_wait(full_bar(s), (uint32_t)(last / S2_STAGES) & 1u, p.err, 5, p.mbar_limit_ns);
+                }
+        }
+    } else if (warp == 1) {
+        if (lane == 0 && leader) {
+            constexpr uint32_t IDESC = make_idesc(256, 256);
+            int it = 0, tcount = 0;
+            bool ok = true;
+            for (int t = cluster_id; t < num_tiles && ok; t += n_clusters, ++tcount) {
+                const int buf = tcount & 1;
+                const uint32_t tph = (uint32_t)(tcount >> 1) & 1u;
+                if (!mbar_wait(tempty_bar(buf), tph ^ 1u, p.err, 2, p.mbar_limit_ns) || s_abort) {
+                    s_abort = 1;
+                    break;
+                }
+                tc_fence_after();
+                const uint32_t d = tmem_base + (uint32_t)(buf * ACC_COLS);
+                for (int kb = 0; kb < kb_n; ++kb, ++it) {
+                    const int s = it % S2_STAGES;
+                    const uint32_t ph = (uint32_t)(it / S2_STAGES) & 1u;
+                    if (!mbar_wait(full_bar(s), ph, p.err, 3, p.mbar_limit_ns)) {
+                        ok = false;
+                        s_abort = 1;
+                        break;
+                    }
+                    tc_fence_after();
+                    const uint32_t sa = base + s * S2_STAGE;
+                    const uint32_t sb = sa + S2_A;
+#pragma unroll
+                    for (int kk = 0; kk < BK / 16; ++kk)
+                        umma2_bf16(d, make_sdesc(sa + kk * 32), make_sdesc(sb + kk * 32), IDESC, (kb > 0 || kk > 0) ? 1u : 0u);
+                    umma2_commit_both(empty_bar(s));
+                }
+                if (ok) umma2_commit_both(tfull_bar(buf));
+            }
+            umma2_commit_both(done_bar);
+            mbar_wait(done_bar, 0, p.err, 6, p.mbar_limit_ns);
+        }
+    } else {
+        const int q = warp & 3;
+        const int half = (warp - 2) >> 2;
+        float* ebuf = reinterpret_cast<float*>(gbase + S2_STAGES * S2_STAGE + (warp - 2) * EPI_BUF_BYTES);
+        const uint32_t leader_tempty0 = mapa(tempty_bar(0), 0), leader_tempty1 = mapa(tempty_bar(1), 0);
+        int tcount = 0;
+        for (int t = cluster_id; t < num_tiles; t += n_clusters, ++tcount) {
+            const int buf = tcount & 1;
+            const uint32_t tph = (uint32_t)(tcount >> 1) & 1u;
+            if (!mbar_wait(tfull_bar(buf), tph, p.err, 4, p.mbar_limit_ns) || s_abort) {
+                s_abort = 1;
+                break;
+            }
+            tc_fence_after();
+            const int m2 = t % num_m2, n = t / num_m2;
+            const int row0 = m2 * 256 + (int)rank * 128 + q * 32;
+            const int row_end = p.M;
+            const uint32_t tbase = tmem_base + ((uint32_t)(q * 32) << 16) + (uint32_t)(buf * ACC_COLS);
+            constexpr int CHUNKS = DUAL ? ACC_COLS / 64 : ACC_COLS / 32;
+            constexpr int PER_WARP = CHUNKS / (EPI_WARPS / 4);
+#pragma unroll 1
+            for (int c = half * PER_WARP; c < (half + 1) * PER_WARP; ++c) {
+                uint32_t r[32], r2[32];
+                tmem_ld32(tbase + c * 32, r);
+                if (DUAL) tmem_ld32(tbase + ACC_COLS / 2 + c * 32, r2);
+                tmem_ld_wait();
+                const int n0 = (DUAL ? n * 128 : n * 256) + c * 32;
+                if (n0 < p.N && row0 < row_end) {
+                    float v[32], u[32];
+#pragma unroll
+                    for (int j = 0; j < 32; ++j) {
+                        v[j] = __uint_as_float(r[j]);
+                        u[j] = DUAL ? __uint_as_float(r2[j]) : 0.f;
+                    }
+                    epilogue_chunk<EPI>(p, row0, row_end, n0, v, u, ebuf);
+                }
+            }
+            tc_fence_before();
+            remote_arrive(buf ? leader_tempty1 : leader_tempty0);
+        }
+    }
+    tc_fence_before();
+    __syncthreads();
+    cluster_sync();  // the pair's MMAs and epilogues are done before either CTA frees TMEM
+    if (warp == 1) {
+        tc_fence_after();
+        tmem_dealloc2(tmem_base, 512);
+    }
+}
 // ------------------------------------------------------------------ host side
 typedef CUresult (*EncodeTiledFn)(CUtensorMap*, CUtensorMapDataType, cuuint32_t, void*, const cuuint64_t*,
                                   const cuuint64_t*, const cuuint32_t*, const cuuint32_t*,
@@ -595,6 +840,30 @@ cudaError_t launch_t(const GemmParams& p, int grid, cudaStream_t s) {
     return cudaGetLastError();
 }
 
+template <int EPI, bool DUAL>
+cudaError_t launch_t2(const GemmParams& p, int clusters, cudaStream_t s) {
+    auto kern = gemm_bf16_tc2<EPI, DUAL>;
+    static bool attr_set = false;
+    if (!attr_set) {
+        cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, S2_SMEM);
+        if (e != cudaSuccess) return e;
+        attr_set = true;
+    }
+    cudaLaunchConfig_t cfg = {};
+    cfg.gridDim = dim3(2 * clusters);
+    cfg.blockDim = dim3(NUM_THREADS);
+    cfg.dynamicSmemBytes = S2_SMEM;
+    cfg.stream = s;
+    cudaLaunchAttribute at[1];
+    at[0].id = cudaLaunchAttributeClusterDimension;
+    at[0].val.clusterDim.x = 2;
+    at[0].val.clusterDim.y = 1;
+    at[0].val.clusterDim.z = 1;
+    cfg.attrs = at;
+    cfg.numAttrs = 1;
+    return cudaLaunchKernelEx(&cfg, kern, p);
+}
+
 }  // namespace
 
 int gemm_num_sms() {
@@ -659,6 +928,25 @@ cudaError_t launch_gemm_bf16(const GemmDesc& d, int max_ctas, cudaStream_t s) {
     }
     int sms = gemm_num_sms();
     int grid = max_ctas > 0 ? (max_ctas < sms ? max_ctas : sms) : sms;
+    if (!grouped && d.M > BM) {
+        // pair-CTA tiles of 256 rows; the choice depends only on the shape, so the
+        // bits do not depend on the grid size
+        if (!cached_tmap(&p.tmA, d.A, d.a_rows > 0 ? d.a_rows : d.M, d.K, d.lda, 128) ||
+            !cached_tmap(&p.tmB, d.B, d.b_rows > 0 ? d.b_rows : d.N, d.K, d.ldb, 128))
+            return cudaErrorInvalidValue;
+        const int pair_tiles = ((d.M + 255) / 256) * p.num_n_tiles;
+        int clusters = grid / 2;
+        if (clusters > pair_tiles) clusters = pair_tiles;
+        if (clusters < 1) clusters = 1;
+        switch (d.epi) {
+            case EPI_STORE: return launch_t2<EPI_STORE, false>(p, clusters, s);
+            case EPI_BIAS_GELU: return launch_t2<EPI_BIAS_GELU, false>(p, clusters, s);
+            case EPI_BIAS_RESID: return launch_t2<EPI_BIAS_RESID, false>(p, clusters, s);
+            case EPI_RESID: return launch_t2<EPI_RESID, false>(p, clusters, s);
+            case EPI_SWIGLU: return launch_t2<EPI_SWIGLU, true>(p, clusters, s);
+        }
+        return cudaErrorInvalidValue;
+    }
     if (grid > tiles) grid = tiles;
     if (grid < 1) grid = 1;
     switch (d.epi) {
