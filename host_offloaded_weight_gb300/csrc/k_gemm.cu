@@ -237,7 +237,22 @@ __device__ __forceinline__ Tile tile_of(const GemmParams& p, int t, const int* s
 }
 
 __device__ __forceinline__ float bf2f(uint16_t h) { return __uint_as_float((uint32_t)h << 16); }
-__device__ __forceinline__ float gelu_f(float v) { return 0.5f * v * (1.0f + erff(v * 0.70710678118654752f)); }
+// erf by Abramowitz & Stegun, Handbook of Mathematical Functions, formula 7.1.26:
+// erf(x) = 1 - (a1 t + a2 t^2 + a3 t^3 + a4 t^4 + a5 t^5) exp(-x^2), t = 1/(1 + p x),
+// x >= 0, |error| <= 1.5e-7 (odd extension for x < 0). About a dozen
+// instructions with the fast reciprocal and exponential, well below the bf16
+// rounding of the output; it keeps the GELU epilogue from outlasting the mainloop.
+__device__ __forceinline__ float erf_as7126(float x) {
+    const float ax = fabsf(x);
+    const float t = __fdividef(1.0f, fmaf(0.3275911f, ax, 1.0f));
+    float poly = fmaf(1.061405429f, t, -1.453152027f);
+    poly = fmaf(poly, t, 1.421413741f);
+    poly = fmaf(poly, t, -0.284496736f);
+    poly = fmaf(poly, t, 0.254829592f);
+    const float y = fmaf(-poly * t, __expf(-ax * ax), 1.0f);
+    return copysignf(y, x);
+}
+__device__ __forceinline__ float gelu_f(float v) { return 0.5f * v * (1.0f + erf_as7126(v * 0.70710678118654752f)); }
 __device__ __forceinline__ float silu_f(float v) { return v / (1.0f + __expf(-v)); }
 
 // 32x32 fp32 staging of one warp, held as 32 rows x 8 float4 and XOR-swizzled
