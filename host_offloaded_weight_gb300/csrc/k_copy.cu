@@ -86,6 +86,9 @@ __global__ void publish_kernel(uint32_t* ready, uint32_t epoch, int publish) {
 
 __global__ void wait_ready_kernel(const uint32_t* ready, uint32_t epoch, uint64_t limit_ns,
                                   uint32_t* err_word, uint32_t code) {
+    // the GEMM behind this wait may be placed now: it reads the weights only after
+    // this kernel has completed (its grid-dependency wait), never before
+    asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
     if (threadIdx.x != 0) return;
     if (*(volatile uint32_t*)err_word) return;
     if (ld_acquire_gpu(ready) == epoch) return;

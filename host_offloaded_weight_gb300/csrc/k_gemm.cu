@@ -60,6 +60,8 @@ constexpr int MAX_GROUPS = 256;
 struct GemmParams {
     CUtensorMap tmA;
     CUtensorMap tmB;
+    CUtensorMap tmC;    // pair kernel: bf16 output, 32x32 box, 64-byte swizzle
+    CUtensorMap tmC32;  // pair kernel: fp32 output copy, 32x32 box, 128-byte swizzle
     int M, N, K;
     int num_m_tiles, num_n_tiles, num_k_blocks, num_tiles;
     int b2_row_off;
@@ -137,6 +139,14 @@ __device__ __forceinline__ void tma_load_2d(uint32_t dst, const CUtensorMap* map
 __device__ __forceinline__ void tma_prefetch_desc(const CUtensorMap* map) {
     asm volatile("prefetch.tensormap [%0];" ::"l"(reinterpret_cast<uint64_t>(map)) : "memory");
 }
+// Programmatic dependent launch: a GEMM is launched while the kernel before it in
+// the stream is still running, so its prologue (barriers, TMEM, descriptors)
+// overlaps that kernel's tail. grid_dep_wait() blocks until the previous kernel
+// has completed and its writes are visible, and comes before this kernel's first
+// global-memory access; grid_dep_launch() lets the next kernel start early.
+// Both are no-ops for a launch without the attribute.
+__device__ __forceinline__ void grid_dep_wait() { asm volatile("griddepcontrol.wait;" ::: "memory"); }
+__device__ __forceinline__ void grid_dep_launch() { asm volatile("griddepcontrol.launch_dependents;" ::: "memory"); }
 __device__ __forceinline__ void tc_fence_before() {
     asm volatile("tcgen05.fence::before_thread_sync;" ::: "memory");
 }
@@ -237,22 +247,47 @@ __device__ __forceinline__ Tile tile_of(const GemmParams& p, int t, const int* s
 }
 
 __device__ __forceinline__ float bf2f(uint16_t h) { return __uint_as_float((uint32_t)h << 16); }
-// erf by Abramowitz & Stegun, Handbook of Mathematical Functions, formula 7.1.26:
-// erf(x) = 1 - (a1 t + a2 t^2 + a3 t^3 + a4 t^4 + a5 t^5) exp(-x^2), t = 1/(1 + p x),
-// x >= 0, |error| <= 1.5e-7 (odd extension for x < 0). About a dozen
-// instructions with the fast reciprocal and exponential, well below the bf16
-// rounding of the output; it keeps the GELU epilogue from outlasting the mainloop.
-__device__ __forceinline__ float erf_as7126(float x) {
-    const float ax = fabsf(x);
-    const float t = __fdividef(1.0f, fmaf(0.3275911f, ax, 1.0f));
-    float poly = fmaf(1.061405429f, t, -1.453152027f);
-    poly = fmaf(poly, t, 1.421413741f);
-    poly = fmaf(poly, t, -0.284496736f);
-    poly = fmaf(poly, t, 0.254829592f);
-    const float y = fmaf(-poly * t, __expf(-ax * ax), 1.0f);
-    return copysignf(y, x);
+// GELU(v) = v/2 (1 + erf(v/sqrt 2)) with erf by Abramowitz & Stegun, Handbook of
+// Mathematical Functions, formula 7.1.28: for z >= 0,
+//   erf(z) = 1 - (1 + a1 z + a2 z^2 + a3 z^3 + a4 z^4 + a5 z^5 + a6 z^6)^-16,
+// |error| <= 3e-7 (odd extension for z < 0); evaluated in fp32 the sixteenth
+// power amplifies rounding to at most 2e-6 in erf. With z = |v|/sqrt 2 and
+// q = 1 - erf(z), both signs reduce to GELU(v) = max(v, 0) - (|v|/2) q.
+// One approximate reciprocal per element (the only special-function op; +inf
+// gives 0); the rest runs two elements per instruction on the packed fp32
+// pipe. All of it sits far below the bf16 rounding of the output.
+__device__ __forceinline__ float rcp_approx(float x) {
+    float r;
+    asm("rcp.approx.ftz.f32 %0, %1;" : "=f"(r) : "f"(x));
+    return r;
 }
-__device__ __forceinline__ float gelu_f(float v) { return 0.5f * v * (1.0f + erf_as7126(v * 0.70710678118654752f)); }
+__device__ __forceinline__ float2 f2(float a) { return make_float2(a, a); }
+__device__ __forceinline__ float2 gelu2(float2 v) {
+    const float2 z = __fmul2_rn(make_float2(fabsf(v.x), fabsf(v.y)), f2(0.70710678118654752f));
+    float2 p = __ffma2_rn(f2(4.30638e-5f), z, f2(2.765672e-4f));
+    p = __ffma2_rn(p, z, f2(1.520143e-4f));
+    p = __ffma2_rn(p, z, f2(9.2705272e-3f));
+    p = __ffma2_rn(p, z, f2(4.22820123e-2f));
+    p = __ffma2_rn(p, z, f2(7.05230784e-2f));
+    p = __ffma2_rn(p, z, f2(1.0f));
+    p = __fmul2_rn(p, p);
+    p = __fmul2_rn(p, p);
+    p = __fmul2_rn(p, p);
+    p = __fmul2_rn(p, p);
+    const float2 q = make_float2(rcp_approx(p.x), rcp_approx(p.y));
+    const float2 w = __fmul2_rn(z, f2(-0.70710678118654752f));  // -|v|/2
+    return __ffma2_rn(w, q, make_float2(fmaxf(v.x, 0.f), fmaxf(v.y, 0.f)));
+}
+// in place over an even-length register array
+template <int N>
+__device__ __forceinline__ void gelu_inplace(float* v) {
+#pragma unroll
+    for (int j = 0; j < N; j += 2) {
+        const float2 g = gelu2(make_float2(v[j], v[j + 1]));
+        v[j] = g.x;
+        v[j + 1] = g.y;
+    }
+}
 __device__ __forceinline__ float silu_f(float v) { return v / (1.0f + __expf(-v)); }
 
 // 32x32 fp32 staging of one warp, held as 32 rows x 8 float4 and XOR-swizzled
@@ -288,10 +323,7 @@ __device__ __forceinline__ void epilogue_chunk(const GemmParams& p, int row0, in
             for (int j = 0; j < 32; ++j) v[j] += (n + j < p.N ? bf2f(bb[j]) : 0.f);
         }
     }
-    if (EPI == EPI_BIAS_GELU) {
-#pragma unroll
-        for (int j = 0; j < 32; ++j) v[j] = gelu_f(v[j]);
-    }
+    if (EPI == EPI_BIAS_GELU) gelu_inplace<32>(v);
     if (EPI == EPI_SWIGLU) {
 #pragma unroll
         for (int j = 0; j < 32; ++j) v[j] = silu_f(v[j]) * u[j];
@@ -381,12 +413,17 @@ __global__ void __launch_bounds__(NUM_THREADS, 1) gemm_bf16_tc(const __grid_cons
         }
         for (int b = 0; b < 2; ++b) {
             mbar_init(tfull_bar(b), 1);
-            mbar_init(tempty_bar(b), 32 * EPI_WARPS);
+            mbar_init(tempty_bar(b), EPI_WARPS);
         }
         mbar_init(done_bar, 1);
         asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
         asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
     }
+    if (warp == 1) {
+        tmem_alloc(smem_u32(tmem_slot), 512);
+        tmem_relinquish();
+    }
+    grid_dep_wait();
     if (GROUPED && threadIdx.x == 32) {
         int acc = 0;
         for (int g = 0; g < p.n_groups; ++g) {
@@ -395,10 +432,6 @@ __global__ void __launch_bounds__(NUM_THREADS, 1) gemm_bf16_tc(const __grid_cons
             acc += (rows + BM - 1) / BM;
         }
         s_mt_prefix[p.n_groups] = acc;
-    }
-    if (warp == 1) {
-        tmem_alloc(smem_u32(tmem_slot), 512);
-        tmem_relinquish();
     }
     tc_fence_before();
     __syncthreads();
@@ -441,6 +474,7 @@ __global__ void __launch_bounds__(NUM_THREADS, 1) gemm_bf16_tc(const __grid_cons
                     issued_mask |= 1u << s;
                 }
             }
+            grid_dep_launch();  // every load is issued: the next kernel may start placing CTAs
             // drain: every stage's last armed phase must have landed before exit
             for (int s = 0; s < STAGES; ++s) {
                 if (!(issued_mask & (1u << s))) continue;
@@ -503,7 +537,8 @@ __global__ void __launch_bounds__(NUM_THREADS, 1) gemm_bf16_tc(const __grid_cons
         for (int t = blockIdx.x; t < num_tiles; t += gridDim.x, ++tcount) {
             const int buf = tcount & 1;
             const uint32_t tph = (uint32_t)(tcount >> 1) & 1u;
-            if (!mbar_wait(tfull_bar(buf), tph, p.err, 4, p.mbar_limit_ns) || s_abort) {
+            // warp-uniform outcome: the warp's TMEM loads and its single arrive below need every lane
+            if (!__all_sync(0xffffffffu, mbar_wait(tfull_bar(buf), tph, p.err, 4, p.mbar_limit_ns) && !s_abort)) {
                 s_abort = 1;
                 break;
             }
@@ -532,7 +567,8 @@ __global__ void __launch_bounds__(NUM_THREADS, 1) gemm_bf16_tc(const __grid_cons
                 }
             }
             tc_fence_before();
-            mbar_arrive(tempty_bar(buf));
+            __syncwarp();
+            if (lane == 0) mbar_arrive(tempty_bar(buf));  // one arrive per warp
         }
     }
     tc_fence_before();
@@ -553,11 +589,23 @@ __global__ void __launch_bounds__(NUM_THREADS, 1) gemm_bf16_tc(const __grid_cons
 // CTAs' barriers; both epilogues release the accumulator on the leader's
 // barrier. All waits are bounded, and both CTAs always reach the closing
 // cluster barrier before TMEM is freed.
-constexpr int S2_STAGES = 6;
 constexpr int S2_A = 128 * 64 * 2;             // this CTA's 128 rows of A
 constexpr int S2_B = 128 * 64 * 2;             // this CTA's half (128 rows) of B
 constexpr int S2_STAGE = S2_A + S2_B;
-constexpr int S2_SMEM = S2_STAGES * S2_STAGE + EPI_WARPS * EPI_BUF_BYTES + 1024 + 256;
+constexpr int S2_STG_BF = 32 * 32 * 2;         // 32x32 bf16 output staging tile (64-byte rows)
+constexpr int S2_STG_F32 = 32 * 32 * 4;        // 32x32 fp32 output staging tile (128-byte rows)
+// Residual epilogues also write the fp32 copy: they give up one mainloop stage
+// and single-buffer their staging tiles; the others double-buffer theirs.
+__host__ __device__ constexpr bool s2_out_f32(int epi) { return epi == EPI_BIAS_RESID || epi == EPI_RESID; }
+__host__ __device__ constexpr int s2_stages(int epi) { return s2_out_f32(epi) ? 5 : 6; }
+__host__ __device__ constexpr int s2_nbuf(int epi) { return s2_out_f32(epi) ? 1 : 2; }
+__host__ __device__ constexpr int s2_warp_bytes(int epi) {
+    return s2_nbuf(epi) * (S2_STG_BF + (s2_out_f32(epi) ? S2_STG_F32 : 0));
+}
+__host__ __device__ constexpr int s2_smem_bytes(int epi) {
+    return s2_stages(epi) * S2_STAGE + EPI_WARPS * s2_warp_bytes(epi) + 1024 + 256;
+}
+static_assert(s2_smem_bytes(EPI_BIAS_RESID) <= 232448 && s2_smem_bytes(EPI_STORE) <= 232448, "shared memory");
 
 __device__ __forceinline__ uint32_t cluster_rank() {
     uint32_t r;
@@ -610,20 +658,81 @@ __device__ __forceinline__ void umma2_commit_both(uint32_t bar) {
         : "memory");
 }
 
+// Bulk tensor store from shared memory (issued by one thread; completion tracked
+// per thread in bulk groups).
+__device__ __forceinline__ void tma_store_2d(const CUtensorMap* map, uint32_t src, int c0, int c1) {
+    asm volatile("cp.async.bulk.tensor.2d.global.shared::cta.bulk_group [%0, {%2, %3}], [%1];" ::"l"(
+                     reinterpret_cast<uint64_t>(map)),
+                 "r"(src), "r"(c0), "r"(c1)
+                 : "memory");
+}
+__device__ __forceinline__ void bulk_commit() { asm volatile("cp.async.bulk.commit_group;" ::: "memory"); }
+template <int N>
+__device__ __forceinline__ void bulk_wait_read() { asm volatile("cp.async.bulk.wait_group.read %0;" ::"n"(N) : "memory"); }
+__device__ __forceinline__ void bulk_wait_all() { asm volatile("cp.async.bulk.wait_group 0;" ::: "memory"); }
+__device__ __forceinline__ void fence_async_smem() { asm volatile("fence.proxy.async.shared::cta;" ::: "memory"); }
+__device__ __forceinline__ void st_shared_v4(uint32_t addr, uint32_t a, uint32_t b, uint32_t c, uint32_t d) {
+    asm volatile("st.shared.v4.b32 [%0], {%1, %2, %3, %4};" ::"r"(addr), "r"(a), "r"(b), "r"(c), "r"(d) : "memory");
+}
+__device__ __forceinline__ uint32_t pack_bf16(float lo, float hi) {
+    __nv_bfloat162 t = __floats2bfloat162_rn(lo, hi);
+    return *reinterpret_cast<uint32_t*>(&t);
+}
+// v[j] += bias[n0 + j] for the columns below N.
+__device__ __forceinline__ void add_bias_row(const GemmParams& p, int n0, float (&v)[32]) {
+    const uint16_t* bb = reinterpret_cast<const uint16_t*>(p.bias) + n0;
+#pragma unroll
+    for (int g = 0; g < 4; ++g) {
+        if (n0 + 8 * g >= p.N) break;
+        const uint4 qv = *reinterpret_cast<const uint4*>(bb + 8 * g);
+        const uint32_t w[4] = {qv.x, qv.y, qv.z, qv.w};
+#pragma unroll
+        for (int i = 0; i < 4; ++i) {
+            v[8 * g + 2 * i] += bf2f((uint16_t)(w[i] & 0xffff));
+            v[8 * g + 2 * i + 1] += bf2f((uint16_t)(w[i] >> 16));
+        }
+    }
+}
+// Four residual values at (row, col .. col+3), zeros past M or N (N % 8 == 0, so a
+// group of four never straddles N).
+__device__ __forceinline__ float4 load_resid4(const GemmParams& p, int row, int col) {
+    if (row >= p.M || col >= p.N) return make_float4(0.f, 0.f, 0.f, 0.f);
+    if (p.resid_f32)
+        return *reinterpret_cast<const float4*>(reinterpret_cast<const float*>(p.resid) + (int64_t)row * p.ldr + col);
+    const uint2 h = *reinterpret_cast<const uint2*>(reinterpret_cast<const uint16_t*>(p.resid) + (int64_t)row * p.ldr + col);
+    return make_float4(bf2f((uint16_t)(h.x & 0xffff)), bf2f((uint16_t)(h.x >> 16)), bf2f((uint16_t)(h.y & 0xffff)),
+                       bf2f((uint16_t)(h.y >> 16)));
+}
+__device__ __forceinline__ void st_shared_f4(uint32_t addr, float4 v) {
+    asm volatile("st.shared.v4.f32 [%0], {%1, %2, %3, %4};" ::"r"(addr), "f"(v.x), "f"(v.y), "f"(v.z), "f"(v.w)
+                 : "memory");
+}
+__device__ __forceinline__ float4 ld_shared_f4(uint32_t addr) {
+    float4 v;
+    asm volatile("ld.shared.v4.f32 {%0, %1, %2, %3}, [%4];" : "=f"(v.x), "=f"(v.y), "=f"(v.z), "=f"(v.w) : "r"(addr)
+                 : "memory");
+    return v;
+}
+
 template <int EPI, bool DUAL>
 __global__ void __launch_bounds__(NUM_THREADS, 1) gemm_bf16_tc2(const __grid_constant__ GemmParams p) {
     extern __shared__ uint8_t smem_raw[];
     const uint32_t raw = smem_u32(smem_raw);
     const uint32_t base = (raw + 1023u) & ~1023u;
     uint8_t* gbase = smem_raw + (base - raw);
-    const uint32_t bar0 = base + S2_STAGES * S2_STAGE + EPI_WARPS * EPI_BUF_BYTES;
+    constexpr int S2_STAGES = s2_stages(EPI);
+    constexpr int WSB = s2_warp_bytes(EPI);
+    constexpr bool OUT32 = s2_out_f32(EPI);
+    constexpr int NBUF = s2_nbuf(EPI);
+    const uint32_t stg0 = base + S2_STAGES * S2_STAGE;  // epilogue staging tiles, WSB bytes per warp
+    const uint32_t bar0 = stg0 + EPI_WARPS * WSB;
     auto full_bar = [&](int s) { return bar0 + 8u * s; };
     auto empty_bar = [&](int s) { return bar0 + 8u * (S2_STAGES + s); };
     auto tfull_bar = [&](int b) { return bar0 + 8u * (2 * S2_STAGES + b); };
     auto tempty_bar = [&](int b) { return bar0 + 8u * (2 * S2_STAGES + 2 + b); };
     const uint32_t done_bar = bar0 + 8u * (2 * S2_STAGES + 4);
     uint32_t* tmem_slot =
-        reinterpret_cast<uint32_t*>(gbase + S2_STAGES * S2_STAGE + EPI_WARPS * EPI_BUF_BYTES + 8 * (2 * S2_STAGES + 5));
+        reinterpret_cast<uint32_t*>(gbase + (bar0 - base) + 8 * (2 * S2_STAGES + 5));
     __shared__ volatile int s_abort;
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
     const uint32_t rank = cluster_rank();
@@ -638,7 +747,7 @@ __global__ void __launch_bounds__(NUM_THREADS, 1) gemm_bf16_tc2(const __grid_con
         }
         for (int b = 0; b < 2; ++b) {
             mbar_init(tfull_bar(b), 1);
-            mbar_init(tempty_bar(b), 2 * 32 * EPI_WARPS);
+            mbar_init(tempty_bar(b), 2 * EPI_WARPS);
         }
         mbar_init(done_bar, 1);
         asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
@@ -650,6 +759,7 @@ __global__ void __launch_bounds__(NUM_THREADS, 1) gemm_bf16_tc2(const __grid_con
     tc_fence_before();
     cluster_sync();  // barriers of both CTAs initialised, TMEM allocated in both
     tc_fence_after();
+    grid_dep_wait();
     const uint32_t tmem_base = *tmem_slot;
     const int num_m2 = (p.M + 255) / 256;
     const int num_tiles = num_m2 * p.num_n_tiles;  // num_n_tiles counts 256 (dual: 128) columns
@@ -684,6 +794,7 @@ __global__ void __launch_bounds__(NUM_THREADS, 1) gemm_bf16_tc2(const __grid_con
                     issued_mask |= 1u << s;
                 }
             }
+            grid_dep_launch();  // every load is issued: the next kernel may start placing CTAs
             // the leader's full barrier tracks both CTAs' loads: drain there (leader only)
             if (leader)
                 for (int s = 0; s < S2_STAGES; ++s) {
@@ -719,7 +830,8 @@ __global__ void __launch_bounds__(NUM_THREADS, 1) gemm_bf16_tc2(const __grid_con
                     const uint32_t sb = sa + S2_A;
 #pragma unroll
                     for (int kk = 0; kk < BK / 16; ++kk)
-                        umma2_bf16(d, make_sdesc(sa + kk * 32), make_sdesc(sb + kk * 32), IDESC, (kb > 0 || kk > 0) ? 1u : 0u);
+                        umma2_bf16(d, make_sdesc(sa + kk * 32), make_sdesc(sb + kk * 32), IDESC,
+                                   (kb > 0 || kk > 0) ? 1u : 0u);
                     umma2_commit_both(empty_bar(s));
                 }
                 if (ok) umma2_commit_both(tfull_bar(buf));
@@ -728,45 +840,129 @@ __global__ void __launch_bounds__(NUM_THREADS, 1) gemm_bf16_tc2(const __grid_con
             mbar_wait(done_bar, 0, p.err, 6, p.mbar_limit_ns);
         }
     } else {
+        // Epilogue: warp (q, half) owns TMEM lanes q*32.. (its 32 output rows, one per
+        // thread) and half of the tile's 32-column chunks. A chunk is finished in
+        // registers, written into a swizzled staging tile and sent out by one bulk
+        // tensor store that runs while the warp moves on; the tensor map clips
+        // rows >= M and columns >= N.
         const int q = warp & 3;
         const int half = (warp - 2) >> 2;
-        float* ebuf = reinterpret_cast<float*>(gbase + S2_STAGES * S2_STAGE + (warp - 2) * EPI_BUF_BYTES);
+        const uint32_t stg = stg0 + (uint32_t)(warp - 2) * WSB;
         const uint32_t leader_tempty0 = mapa(tempty_bar(0), 0), leader_tempty1 = mapa(tempty_bar(1), 0);
-        int tcount = 0;
+        const bool want32 = OUT32 && p.C32 != nullptr;
+        if (lane == 0) {
+            tma_prefetch_desc(&p.tmC);
+            if (want32) tma_prefetch_desc(&p.tmC32);
+        }
+        constexpr int CHUNKS = DUAL ? ACC_COLS / 64 : ACC_COLS / 32;
+        constexpr int PER_WARP = CHUNKS / (EPI_WARPS / 4);
+        const int c_begin = half * PER_WARP;
+        // Residual epilogues read the residual while the accumulator is still being
+        // computed: coalesced loads (8 lanes cover one row's 32 columns, 4 rows per
+        // instruction) for the tile's first two chunks go out before the wait, each
+        // later chunk's as soon as a register set frees up. The fp32 staging tile
+        // turns each chunk into one row per lane (its layout is the 128-byte swizzle
+        // the output store reads).
+        const int c4 = lane & 7, rsub = lane >> 3;
+        auto issue = [&](int rbase, int n0, float4 (&g)[8]) {
+#pragma unroll
+            for (int it = 0; it < 8; ++it) g[it] = load_resid4(p, rbase + it * 4 + rsub, n0 + 4 * c4);
+        };
+        auto release = [&](int b) {
+            tc_fence_before();
+            __syncwarp();
+            if (lane == 0) remote_arrive(b ? leader_tempty1 : leader_tempty0);  // one arrive per warp
+        };
+        int tcount = 0, sb = 0;
         for (int t = cluster_id; t < num_tiles; t += n_clusters, ++tcount) {
             const int buf = tcount & 1;
             const uint32_t tph = (uint32_t)(tcount >> 1) & 1u;
-            if (!mbar_wait(tfull_bar(buf), tph, p.err, 4, p.mbar_limit_ns) || s_abort) {
+            const int m2 = t % num_m2, n = t / num_m2;
+            const int row0 = m2 * 256 + (int)rank * 128 + q * 32;
+            const int nbase = DUAL ? n * 128 : n * 256;
+            float4 g[2][8];
+            if (OUT32) {
+                issue(row0, nbase + c_begin * 32, g[0]);
+                issue(row0, nbase + (c_begin + 1) * 32, g[1]);
+            }
+            // warp-uniform outcome: TMEM loads and the single arrive below need every lane
+            if (!__all_sync(0xffffffffu, mbar_wait(tfull_bar(buf), tph, p.err, 4, p.mbar_limit_ns) && !s_abort)) {
                 s_abort = 1;
                 break;
             }
             tc_fence_after();
-            const int m2 = t % num_m2, n = t / num_m2;
-            const int row0 = m2 * 256 + (int)rank * 128 + q * 32;
-            const int row_end = p.M;
             const uint32_t tbase = tmem_base + ((uint32_t)(q * 32) << 16) + (uint32_t)(buf * ACC_COLS);
-            constexpr int CHUNKS = DUAL ? ACC_COLS / 64 : ACC_COLS / 32;
-            constexpr int PER_WARP = CHUNKS / (EPI_WARPS / 4);
-#pragma unroll 1
-            for (int c = half * PER_WARP; c < (half + 1) * PER_WARP; ++c) {
+            // unrolled only where the residual registers rotate (static indexing)
+#pragma unroll (OUT32 ? PER_WARP : 1)
+            for (int i = 0; i < PER_WARP; ++i) {
+                const int c = c_begin + i;
+                const int n0 = nbase + c * 32;
                 uint32_t r[32], r2[32];
                 tmem_ld32(tbase + c * 32, r);
                 if (DUAL) tmem_ld32(tbase + ACC_COLS / 2 + c * 32, r2);
                 tmem_ld_wait();
-                const int n0 = (DUAL ? n * 128 : n * 256) + c * 32;
-                if (n0 < p.N && row0 < row_end) {
-                    float v[32], u[32];
+                if (n0 < p.N && row0 < p.M) {  // uniform across the warp
+                    float v[32];
 #pragma unroll
-                    for (int j = 0; j < 32; ++j) {
-                        v[j] = __uint_as_float(r[j]);
-                        u[j] = DUAL ? __uint_as_float(r2[j]) : 0.f;
+                    for (int j = 0; j < 32; ++j) v[j] = __uint_as_float(r[j]);
+                    if (EPI == EPI_BIAS_GELU) {
+                        add_bias_row(p, n0, v);
+                        gelu_inplace<32>(v);
                     }
-                    epilogue_chunk<EPI>(p, row0, row_end, n0, v, u, ebuf);
+                    const uint32_t s32 = stg + NBUF * S2_STG_BF + (uint32_t)sb * S2_STG_F32;
+                    if (OUT32) {
+                        if (EPI == EPI_BIAS_RESID) add_bias_row(p, n0, v);
+                        if (lane == 0) bulk_wait_read<0>();  // the previous chunk's stores have left the staging tiles
+                        __syncwarp();
+#pragma unroll
+                        for (int it = 0; it < 8; ++it) st_shared_f4(s32 + 16u * sw4(it * 4 + rsub, c4), g[i & 1][it]);
+                        __syncwarp();
+                        // each lane reads (and below overwrites) only its own row
+#pragma unroll
+                        for (int j = 0; j < 8; ++j) {
+                            const float4 t4 = ld_shared_f4(s32 + 16u * sw4(lane, j));
+                            v[4 * j] += t4.x; v[4 * j + 1] += t4.y; v[4 * j + 2] += t4.z; v[4 * j + 3] += t4.w;
+                        }
+                    }
+                    if (EPI == EPI_SWIGLU) {
+#pragma unroll
+                        for (int j = 0; j < 32; ++j) v[j] = silu_f(v[j]) * __uint_as_float(r2[j]);
+                    }
+                    if (!OUT32) {
+                        // the staging tile about to be written was last read by the store NBUF chunks ago
+                        if (lane == 0) bulk_wait_read<NBUF - 1>();
+                        __syncwarp();
+                    }
+                    const uint32_t sbf = stg + (uint32_t)sb * S2_STG_BF;
+                    // 64-byte swizzle: 16-byte unit j of row r sits at unit j ^ ((r >> 1) & 3)
+#pragma unroll
+                    for (int j = 0; j < 4; ++j)
+                        st_shared_v4(sbf + lane * 64 + ((j ^ ((lane >> 1) & 3)) << 4), pack_bf16(v[8 * j], v[8 * j + 1]),
+                                     pack_bf16(v[8 * j + 2], v[8 * j + 3]), pack_bf16(v[8 * j + 4], v[8 * j + 5]),
+                                     pack_bf16(v[8 * j + 6], v[8 * j + 7]));
+                    if (want32) {
+                        // 128-byte swizzle: 16-byte unit j of row r sits at unit j ^ (r & 7)
+#pragma unroll
+                        for (int j = 0; j < 8; ++j)
+                            st_shared_v4(s32 + lane * 128 + ((j ^ (lane & 7)) << 4), __float_as_uint(v[4 * j]),
+                                         __float_as_uint(v[4 * j + 1]), __float_as_uint(v[4 * j + 2]),
+                                         __float_as_uint(v[4 * j + 3]));
+                    }
+                    fence_async_smem();
+                    __syncwarp();
+                    if (lane == 0) {
+                        tma_store_2d(&p.tmC, sbf, n0, row0);
+                        if (want32) tma_store_2d(&p.tmC32, s32, n0, row0);
+                        bulk_commit();
+                    }
+                    if (NBUF == 2) sb ^= 1;
                 }
+                if (OUT32 && i + 2 < PER_WARP) issue(row0, n0 + 64, g[i & 1]);
             }
-            tc_fence_before();
-            remote_arrive(buf ? leader_tempty1 : leader_tempty0);
+            release(buf);
         }
+        if (lane == 0) bulk_wait_all();  // stores complete before the CTA exits
+        __syncwarp();
     }
     tc_fence_before();
     __syncthreads();
@@ -796,50 +992,60 @@ EncodeTiledFn encode_fn() {
     return fn;
 }
 
-// 2-D bf16 view [rows, cols] with row stride ld (elements); box = 64 x box_rows, 128-byte swizzle.
-bool make_tmap(CUtensorMap* m, const void* ptr, int64_t rows, int64_t cols, int64_t ld, int box_rows) {
+// 2-D view [rows, cols] of 2- or 4-byte elements with row stride ld (elements);
+// box = box_cols x box_rows.
+struct MapSpec {
+    const void* p;
+    int64_t rows, cols, ld;
+    int box_cols, box_rows;
+    int esize;    // 2: bf16, 4: fp32
+    int swizzle;  // bytes: 64 or 128
+    bool operator==(const MapSpec& o) const {
+        return p == o.p && rows == o.rows && cols == o.cols && ld == o.ld && box_cols == o.box_cols &&
+               box_rows == o.box_rows && esize == o.esize && swizzle == o.swizzle;
+    }
+};
+struct MapSpecHash {
+    size_t operator()(const MapSpec& k) const {
+        size_t h = std::hash<const void*>()(k.p);
+        h ^= std::hash<int64_t>()(k.rows * 1000003 + k.cols * 31 + k.ld) + 0x9e3779b9 + (h << 6) + (h >> 2);
+        h ^= std::hash<int64_t>()(((int64_t)k.box_cols << 24) ^ ((int64_t)k.box_rows << 8) ^ (k.esize << 4) ^
+                                  k.swizzle) + 0x9e3779b9 + (h << 6) + (h >> 2);
+        return h;
+    }
+};
+
+bool make_tmap(CUtensorMap* m, const MapSpec& k) {
     EncodeTiledFn fn = encode_fn();
     if (!fn) return false;
-    cuuint64_t dims[2] = {(cuuint64_t)cols, (cuuint64_t)rows};
-    cuuint64_t strides[1] = {(cuuint64_t)(ld * 2)};
-    cuuint32_t box[2] = {(cuuint32_t)BK, (cuuint32_t)box_rows};
+    cuuint64_t dims[2] = {(cuuint64_t)k.cols, (cuuint64_t)k.rows};
+    cuuint64_t strides[1] = {(cuuint64_t)(k.ld * k.esize)};
+    cuuint32_t box[2] = {(cuuint32_t)k.box_cols, (cuuint32_t)k.box_rows};
     cuuint32_t estr[2] = {1, 1};
-    CUresult r = fn(m, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, const_cast<void*>(ptr), dims, strides, box,
-                    estr, CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
+    CUresult r = fn(m, k.esize == 4 ? CU_TENSOR_MAP_DATA_TYPE_FLOAT32 : CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2,
+                    const_cast<void*>(k.p), dims, strides, box, estr, CU_TENSOR_MAP_INTERLEAVE_NONE,
+                    k.swizzle == 64 ? CU_TENSOR_MAP_SWIZZLE_64B : CU_TENSOR_MAP_SWIZZLE_128B,
                     CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
     return r == CUDA_SUCCESS;
 }
 
-struct MapKey {
-    const void* p;
-    int64_t rows, cols, ld;
-    int box;
-    bool operator==(const MapKey& o) const {
-        return p == o.p && rows == o.rows && cols == o.cols && ld == o.ld && box == o.box;
-    }
-};
-struct MapKeyHash {
-    size_t operator()(const MapKey& k) const {
-        size_t h = std::hash<const void*>()(k.p);
-        h ^= std::hash<int64_t>()(k.rows * 1000003 + k.cols * 31 + k.ld) + 0x9e3779b9 + (h << 6) + (h >> 2);
-        return h ^ (size_t)k.box;
-    }
-};
-
-bool cached_tmap(CUtensorMap* out, const void* ptr, int64_t rows, int64_t cols, int64_t ld, int box) {
+bool cached_tmap(CUtensorMap* out, const MapSpec& k) {
     static std::mutex mu;
-    static std::unordered_map<MapKey, CUtensorMap, MapKeyHash> cache;
-    MapKey k{ptr, rows, cols, ld, box};
+    static std::unordered_map<MapSpec, CUtensorMap, MapSpecHash> cache;
     std::lock_guard<std::mutex> g(mu);
     auto it = cache.find(k);
     if (it != cache.end()) {
         *out = it->second;
         return true;
     }
-    if (!make_tmap(out, ptr, rows, cols, ld, box)) return false;
+    if (!make_tmap(out, k)) return false;
     if (cache.size() > 4096) cache.clear();
     cache.emplace(k, *out);
     return true;
+}
+// bf16 operand view: 64-element (128-byte) K box, 128-byte swizzle
+bool cached_tmap(CUtensorMap* out, const void* ptr, int64_t rows, int64_t cols, int64_t ld, int box) {
+    return cached_tmap(out, MapSpec{ptr, rows, cols, ld, BK, box, 2, 128});
 }
 
 template <int EPI, bool DUAL, bool GROUPED>
@@ -851,8 +1057,17 @@ cudaError_t launch_t(const GemmParams& p, int grid, cudaStream_t s) {
         if (e != cudaSuccess) return e;
         attr_set = true;
     }
-    kern<<<grid, NUM_THREADS, SMEM_BYTES, s>>>(p);
-    return cudaGetLastError();
+    cudaLaunchConfig_t cfg = {};
+    cfg.gridDim = dim3(grid);
+    cfg.blockDim = dim3(NUM_THREADS);
+    cfg.dynamicSmemBytes = SMEM_BYTES;
+    cfg.stream = s;
+    cudaLaunchAttribute at[1];
+    at[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+    at[0].val.programmaticStreamSerializationAllowed = 1;
+    cfg.attrs = at;
+    cfg.numAttrs = 1;
+    return cudaLaunchKernelEx(&cfg, kern, p);
 }
 
 template <int EPI, bool DUAL>
@@ -860,22 +1075,24 @@ cudaError_t launch_t2(const GemmParams& p, int clusters, cudaStream_t s) {
     auto kern = gemm_bf16_tc2<EPI, DUAL>;
     static bool attr_set = false;
     if (!attr_set) {
-        cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, S2_SMEM);
+        cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, s2_smem_bytes(EPI));
         if (e != cudaSuccess) return e;
         attr_set = true;
     }
     cudaLaunchConfig_t cfg = {};
     cfg.gridDim = dim3(2 * clusters);
     cfg.blockDim = dim3(NUM_THREADS);
-    cfg.dynamicSmemBytes = S2_SMEM;
+    cfg.dynamicSmemBytes = s2_smem_bytes(EPI);
     cfg.stream = s;
-    cudaLaunchAttribute at[1];
+    cudaLaunchAttribute at[2];
     at[0].id = cudaLaunchAttributeClusterDimension;
     at[0].val.clusterDim.x = 2;
     at[0].val.clusterDim.y = 1;
     at[0].val.clusterDim.z = 1;
+    at[1].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+    at[1].val.programmaticStreamSerializationAllowed = 1;
     cfg.attrs = at;
-    cfg.numAttrs = 1;
+    cfg.numAttrs = 2;
     return cudaLaunchKernelEx(&cfg, kern, p);
 }
 
@@ -948,6 +1165,10 @@ cudaError_t launch_gemm_bf16(const GemmDesc& d, int max_ctas, cudaStream_t s) {
         // bits do not depend on the grid size
         if (!cached_tmap(&p.tmA, d.A, d.a_rows > 0 ? d.a_rows : d.M, d.K, d.lda, 128) ||
             !cached_tmap(&p.tmB, d.B, d.b_rows > 0 ? d.b_rows : d.N, d.K, d.ldb, 128))
+            return cudaErrorInvalidValue;
+        // output views for the bulk tensor stores (32x32 boxes; clipped at M and N)
+        if (!cached_tmap(&p.tmC, MapSpec{d.C, d.M, d.N, d.ldc, 32, 32, 2, 64})) return cudaErrorInvalidValue;
+        if (d.C32 && !cached_tmap(&p.tmC32, MapSpec{d.C32, d.M, d.N, d.ldc, 32, 32, 4, 128}))
             return cudaErrorInvalidValue;
         const int pair_tiles = ((d.M + 255) / 256) * p.num_n_tiles;
         int clusters = grid / 2;

@@ -1220,6 +1220,16 @@ ls_status ls_get_trace(ls_ctx* c, ls_trace_event* out, int64_t cap, int64_t* n_o
     return LS_OK;
 }
 
+ls_status ls_set_kernel_timing(ls_ctx* c, int32_t mode) {
+    if (!c || mode < 0 || mode > 2) return LS_ERR_INVALID_ARG;
+    if (!c->pending.empty()) {
+        set_err(c, "ls_set_kernel_timing: passes are queued; call ls_sync first");
+        return LS_ERR_STATE;
+    }
+    c->prm.kernel_timing = mode;
+    return LS_OK;
+}
+
 ls_status ls_get_kernel_times(ls_ctx* c, ls_kernel_time* out, int32_t cap, int32_t* n_out, int32_t reset) {
     if (!c || !n_out || cap < 0 || (cap > 0 && !out)) return LS_ERR_INVALID_ARG;
     *n_out = (int32_t)c->tclass.size();

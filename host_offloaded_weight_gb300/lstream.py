@@ -104,6 +104,7 @@ _sig = {
     "ls_sync": (_I32, [_P]),
     "ls_get_schedule": (_I32, [_P, C.POINTER(ls_sched_event), _I64, C.POINTER(_I64)]),
     "ls_get_stats": (_I32, [_P, C.POINTER(ls_stats)]),
+    "ls_set_kernel_timing": (_I32, [_P, _I32]),
     "ls_get_kernel_times": (_I32, [_P, C.POINTER(ls_kernel_time), _I32, C.POINTER(_I32), _I32]),
     "ls_get_trace": (_I32, [_P, C.POINTER(ls_trace_event), _I64, C.POINTER(_I64)]),
     "ls_ctx_destroy": (None, [_P]),
@@ -295,6 +296,10 @@ def ls_get_stats(ctx: Ctx) -> dict:
     s.struct_size = C.sizeof(ls_stats)
     _check(_lib.ls_get_stats(ctx.handle, C.byref(s)), ctx)
     return _stats_dict(s)
+
+
+def ls_set_kernel_timing(ctx: Ctx, mode: int) -> int:
+    return _check(_lib.ls_set_kernel_timing(ctx.handle, mode), ctx)
 
 
 def ls_get_kernel_times(ctx: Ctx, reset: bool = False) -> dict:

@@ -259,6 +259,15 @@ ls_status ls_get_schedule(ls_ctx* ctx, ls_sched_event* out, int64_t cap, int64_t
 /* Counters and the current plan. out->struct_size must be set by the caller. */
 ls_status ls_get_stats(ls_ctx* ctx, ls_stats* out);
 
+/* Switch per-launch timing (the kernel_timing field of ls_params: 0, 1 or 2)
+ * for the passes issued from now on. Event records between launches cost the
+ * stream a little time and keep consecutive GEMMs from overlapping their
+ * start-up, so a throughput measurement runs with timing off and a separate
+ * set of passes collects the per-kernel times. LS_ERR_STATE while passes issued
+ * by ls_run_async have not been collected by ls_sync; LS_ERR_INVALID_ARG for a
+ * mode outside 0..2. The pages define no such call: it is instrumentation. */
+ls_status ls_set_kernel_timing(ls_ctx* ctx, int32_t mode);
+
 /* Copy up to cap kernel-time records into out; *n_out = number of classes.
  * reset != 0 clears the accumulators afterwards. */
 ls_status ls_get_kernel_times(ls_ctx* ctx, ls_kernel_time* out, int32_t cap, int32_t* n_out, int32_t reset);

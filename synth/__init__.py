@@ -289,8 +289,15 @@ class HostStack:
         seg_bytes = segment_slot_bytes(cfg)
         sh_bytes = sum(align256(t.nbytes) for t in sh)
         total = n * seg_bytes + sh_bytes
-        # anonymous pages of its own: nothing else lives in the buffer's pages
+        # anonymous pages of its own: nothing else lives in the buffer's pages. Large
+        # pages where the kernel offers them on request: fewer translations for the
+        # device's reads of pinned host memory (a hint; ignored where unsupported)
         self._map = mmap.mmap(-1, max(total, 1))
+        if hasattr(mmap, "MADV_HUGEPAGE") and total >= (64 << 20):
+            try:
+                self._map.madvise(mmap.MADV_HUGEPAGE)
+            except OSError:
+                pass
         self.buffer = np.frombuffer(self._map, dtype=np.uint8, count=total)
         self.shared_views = []
         o = n * seg_bytes

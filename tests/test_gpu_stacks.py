@@ -281,6 +281,34 @@ def test_run_host_matches_run():
         L.ls_ctx_destroy(ctx)
 
 
+def test_kernel_timing_switch():
+    """Per-launch timing switched on between passes: refused while a pass is
+    queued, and the results do not depend on it (timed and untimed passes
+    produce the same bits)."""
+    cfg = SMALL["ffn"]
+    hs = synth.HostStack(cfg)
+    ctx, _ = make_ctx(cfg, hs, kernel_timing=0)
+    try:
+        x = x_dev(cfg)
+        y0, y1 = torch.empty_like(x), torch.empty_like(x)
+        L.ls_run_async(ctx, x, y0, cfg.tokens)
+        with pytest.raises(L.LsError) as e:
+            L.ls_set_kernel_timing(ctx, 1)
+        assert e.value.status == L.LS_ERR_STATE
+        L.ls_sync(ctx)
+        assert L.ls_get_kernel_times(ctx) == {}
+        L.ls_set_kernel_timing(ctx, 1)
+        L.ls_run(ctx, x, y1, cfg.tokens)
+        kt = L.ls_get_kernel_times(ctx, reset=True)
+        assert kt["gemm_up"][0] == cfg.n_segments and kt["gemm_down"][0] == cfg.n_segments
+        assert all(ms > 0 for _, ms in kt.values())
+        assert torch.equal(y0.view(torch.int16), y1.view(torch.int16))
+        with pytest.raises(L.LsError):
+            L.ls_set_kernel_timing(ctx, 3)
+    finally:
+        L.ls_ctx_destroy(ctx)
+
+
 # ------------------------------------------------------------------ MoE
 def _moe_cfg(layers, tokens, experts=128, hidden=2048, ffn=768, k=8):
     c = synth.MOE.with_(n_segments=layers, tokens=tokens, n_experts=experts, hidden=hidden, ffn=ffn, top_k=k)
