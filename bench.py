@@ -355,6 +355,9 @@ def run_ours(args, cfg, world, rank, local):
                    "ffn": cfg.ffn, "prefetch_depth": cfg.prefetch_depth, "resident_layers": cfg.resident_layers,
                    "max_vram_bytes": cfg.max_vram_bytes, "pool": cfg.use_pool,
                    "copy_path": ["auto", "kernel", "engine"][stats["copy_path"]],
+                   "plan": {"residents": stats["residents"], "depth": stats["depth"],
+                            "pool_slots": stats["pool_slots"], "slot_bytes": stats["slot_bytes"],
+                            "warnings": stats["warnings"]},
                    "parallelism": f"replicas{world}" if world > 1 else "single",
                    "l2": "flushed between timed passes (256 MB write)"},
         "overlap_eff": max(link_bytes / (link_peak * 1e9), flops / (tc_peak * 1e12)) / mean_s,
@@ -388,8 +391,12 @@ def run_ours(args, cfg, world, rank, local):
     return 0
 
 
-# DRAM bytes per launch from ncu captures of the current kernels (None = not captured).
-TRAFFIC: dict = {}
+# DRAM bytes (read + write) per launch from ncu captures of the current kernels
+# (profiles/gemm_pair_dit_ffn_12x1024x4096.md); absent = not captured.
+TRAFFIC: dict = {
+    ("dit_ffn_12x1024x4096", "gemm_up"): 16_812_800 + 364_032,
+    ("dit_ffn_12x1024x4096", "gemm_down"): 50_394_624 + 1_917_696,
+}
 
 
 def main() -> int:
@@ -405,11 +412,19 @@ def main() -> int:
     ap.add_argument("--cpu-tokens", type=int, default=1024)
     ap.add_argument("--ref-tokens", type=int, default=256)
     ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--prefetch-depth", type=int, default=None,
+                    help="override the workload's prefetch depth (the planner re-derives residents)")
+    ap.add_argument("--max-vram-bytes", type=int, default=None,
+                    help="override the workload's parameter budget (e.g. a one-slot run)")
     args = ap.parse_args()
     if args.warmup < 3:
         ap.error("--warmup must be at least 3")
     world, rank, local = dist_env()
     cfg = synth.STACKS[args.workload]
+    if args.prefetch_depth is not None:
+        cfg = cfg.with_(prefetch_depth=args.prefetch_depth)
+    if args.max_vram_bytes is not None:
+        cfg = cfg.with_(max_vram_bytes=args.max_vram_bytes)
     if args.impl == "reference":
         return run_reference(args, cfg, world, rank)
     return run_ours(args, cfg, world, rank, local)
