@@ -37,45 +37,62 @@ def brute_plan(N: int, S: int, shared_total: int, depth: int, resident: int, max
     return best[0], best[1], False
 
 
-def replay(events: list, n_segments: int, n_slots: int) -> int:
-    """Check slot ownership along the schedule; return the peak occupied slots."""
+def replay(events: list, n_segments: int, n_slots) -> int:
+    """Check slot ownership along the schedule; return the peak occupied slots.
+
+    ``n_slots`` is the pool size, or {run: pool size} when the plan changes between
+    runs. A streamed load may be activated in a later run (cross-run window); such a
+    load, and any resident, may be released at a plan change (EVICT at step -1)."""
     owner: dict = {}
     residents: set = set()
+    pending: set = set()          # loaded, not yet activated (may cross a run boundary)
     peak = 0
     by_run: dict = {}
     for ev in events:
         by_run.setdefault(ev[0], []).append(ev)
     for run in sorted(by_run):
+        slots = n_slots[run] if isinstance(n_slots, dict) else n_slots
         activated = []
-        loaded_this_run = set()
+        run_peak = 0
         for (_, step, kind, seg, slot, _nb) in by_run[run]:
             if kind == SHARED_LOAD:
                 assert slot == -1
                 continue
-            assert 0 <= slot < n_slots, f"slot {slot} outside the pool of {n_slots}"
+            # a release at a plan change names a slot of the pool before the change
+            if not (kind == EVICT and step == -1):
+                assert 0 <= slot < slots, f"slot {slot} outside the pool of {slots}"
             if kind == LOAD_RESIDENT:
                 assert slot not in owner, f"resident {seg} lands on occupied slot {slot}"
+                assert step == -1, "residents load before the run's first step"
                 owner[slot] = seg
                 residents.add(seg)
-                loaded_this_run.add(seg)
             elif kind in (PREFETCH, LOAD_SYNC):
                 assert seg not in residents, f"resident {seg} loaded again"
+                assert seg not in pending, f"{seg} loaded twice before its activation"
                 assert slot not in owner, \
                     f"run {run} step {step}: load of {seg} overwrites slot {slot} held by {owner[slot]}"
                 owner[slot] = seg
-                loaded_this_run.add(seg)
+                pending.add(seg)
             elif kind == EVICT:
-                assert seg in residents and owner.get(slot) == seg
-                # the segment active at step k is k: only ones computed earlier may go
-                assert seg < step, "evicted the active segment or one not yet computed"
+                assert owner.get(slot) == seg, f"evict {seg} finds slot {slot} holding {owner.get(slot)}"
+                if seg in residents:
+                    # the segment active at step k is k: only ones computed earlier may go
+                    assert step == -1 or seg < step, "evicted the active segment or one not yet computed"
+                    residents.discard(seg)
+                else:
+                    assert seg in pending and step == -1, "only a stale prefetch is released, between runs"
+                    pending.discard(seg)
                 del owner[slot]
-                residents.discard(seg)
             elif kind == ACTIVATE:
                 assert owner.get(slot) == seg, f"activate {seg} finds slot {slot} holding {owner.get(slot)}"
-                assert seg in residents or seg in loaded_this_run
+                assert seg in residents or seg in pending
                 activated.append(seg)
-            peak = max(peak, len(owner))
+            if not (kind == EVICT and step == -1):   # occupancy once the plan change is done
+                run_peak = max(run_peak, len(owner))
             if kind == ACTIVATE and seg not in residents:
+                pending.discard(seg)
                 del owner[slot]          # a streamed slot is free once its segment computed
+        assert run_peak <= slots
+        peak = max(peak, run_peak)
         assert activated == list(range(len(activated))), "segments activate in order"
     return peak

@@ -37,6 +37,31 @@ design notes of the repository):
   * shared parameters are resident (deduplicated) and loaded once in run 0,
     followed by the resident prefix, both synchronously;
   * load j of a run goes to ring slot R + (j mod Q) with Q = min(d + 1, N - R).
+
+Plan changes between runs and the cross-run window (the pages' "releases stale
+residents and prefetches when the graph plan changes", "evicts residents from
+the end of the resident prefix", "reuses a sufficiently large pool ... and
+remembers reduced runtime caps", sd.cpp #1905 and #1906, Summary):
+  * ``replan`` takes new controls (depth, resident cap, budget) between runs. It
+    plans with the same rules, under the remembered reduced slot cap, and keeps
+    a remembered synchronous fallback;
+  * prefetches issued for a run that has not started are stale: each one is
+    released (EVICT of that segment and slot) first;
+  * residents that the new plan no longer holds are released from the end of
+    the prefix (EVICT, descending), before the next run's first step;
+  * pool on: the pool is kept while the slot count stays the same. Otherwise it
+    is given back and a pool of the new count is allocated (smaller counts tried
+    on failure, as at registration). That empties every slot, so every old
+    resident is released and the whole new prefix is loaded again. Pool off: the
+    kept residents' buffers stay;
+  * a run loads, synchronously before its first step, the residents that hold no
+    data yet (LOAD_RESIDENT), so a grown prefix is filled at the next run;
+  * cross-run window (opt-in; off matches the maintainer's removal of cross-forward
+    state): the window of the last steps reaches into the next run's first
+    streamed segments, so their prefetches are issued before the run ends. Load
+    numbers then continue across runs (slot R + (J mod Q), J counted from the
+    last plan change). The window crosses the boundary only when the ring is a
+    full d + 1 slots (N - R > d).
 """
 from __future__ import annotations
 
@@ -138,7 +163,13 @@ class Sim:
     use_pool: int
     alloc_cap: int | None = None        # parameter allocator refuses beyond this many live bytes
     fail_async: bool = False            # the first prefetch finds async transfer unavailable
+    cross_run: bool = False             # the prefetch window crosses the run boundary
     plan: Plan | None = None
+    slot_cap: int | None = None         # remembered reduced pool slot count
+    loaded_R: int = 0                   # leading residents whose slots hold their data
+    J: int = 0                          # streamed loads numbered since the last plan change (cross-run)
+    carried: list = field(default_factory=list)   # [(seg, slot)] prefetched for the next run
+    carried_R: int = 0                  # the resident prefix the carried prefetches were planned for
     status: int = OK
     R: int = 0
     d: int = 0
@@ -174,6 +205,8 @@ class Sim:
                 self._free(p.shared_total)
                 self.status = ERR_OOM
                 return ERR_OOM
+            if chosen.P < p.P:
+                self.slot_cap = chosen.P
             p = chosen
         self.plan = p
         self.R = p.R
@@ -213,53 +246,128 @@ class Sim:
                 self._emit(-1, SHARED_LOAD, sid, -1, b)
                 self.stats.shared_loads += 1
                 self.stats.bytes_loaded += b
-            for i in range(self.R):
-                if not pool and not self._alloc(sz[i]):
-                    self.R = i          # the prefix ends where memory ran out
-                    break
-                self._emit(-1, LOAD_RESIDENT, i, i, lb(i))
-                self.stats.resident_loads += 1
-                self.stats.bytes_loaded += lb(i)
+        if self.carried and self.carried_R != self.R:
+            self._release_carried()      # planned for another ring: stale
+        for i in range(self.loaded_R, self.R):      # residents without their data yet
+            if not pool and not self._alloc(sz[i]):
+                self.R = i          # the prefix ends where memory ran out
+                break
+            self._emit(-1, LOAD_RESIDENT, i, i, lb(i))
+            self.stats.resident_loads += 1
+            self.stats.bytes_loaded += lb(i)
+        self.loaded_R = self.R
         R = self.R                      # this run's resident prefix and ring
         M = N - R
         Q = min(self.d + 1, M) if M > 0 else 0
         d = min(self.d, M)
+        J0 = self.J if self.cross_run else 0
+        # the window reaches into the next run only with a full ring of d + 1 slots
+        reach = M + d if (self.cross_run and M > d) else M
         self.cur_R = R
-        next_load = 0
-        prefetched = set()
+        prefetched = {seg for seg, _ in self.carried}   # issued by the previous run
+        next_load = len(self.carried)
+        self.carried = []
         for k in range(N):
             streamed_upto = max(0, k - R + 1)       # streamed segments with index <= k
             if d >= 1 and self.async_ok:
-                while next_load < M and next_load < streamed_upto + d:
-                    seg = R + next_load
-                    if self.fail_async or (not pool and not self._alloc_evicting(sz[seg], k)):
+                while next_load < reach and next_load < streamed_upto + d:
+                    seg = R + next_load % M
+                    if next_load >= M and not pool and not self._alloc(sz[seg]):
+                        break            # the next run's loads never evict: that run loads them itself
+                    if next_load < M and (self.fail_async or (not pool and not self._alloc_evicting(sz[seg], k))):
                         self._fallback()
                         fell_back = True
                         d = 0
                         break
-                    self._emit(k, PREFETCH, seg, R + next_load % Q, lb(seg))
+                    slot = R + (J0 + next_load) % Q
+                    self._emit(k, PREFETCH, seg, slot, lb(seg))
                     self.stats.prefetch_queued += 1
                     self.stats.bytes_loaded += lb(seg)
-                    prefetched.add(seg)
+                    if next_load < M:
+                        prefetched.add(seg)
+                    else:
+                        self.carried.append((seg, slot))
                     next_load += 1
             if k >= R and k not in prefetched:
                 if not pool and not self._alloc_evicting(sz[k], k):
                     ret = ERR_OOM
                     break
-                self._emit(k, LOAD_SYNC, k, R + (k - R) % Q, lb(k))
+                self._emit(k, LOAD_SYNC, k, R + (J0 + k - R) % Q, lb(k))
                 self.stats.sync_loads += 1
                 self.stats.bytes_loaded += lb(k)
                 next_load = k - R + 1
-            self._emit(k, ACTIVATE, k, k if k < R else R + (k - R) % Q, 0)
+            self._emit(k, ACTIVATE, k, k if k < R else R + (J0 + k - R) % Q, 0)
             if k in prefetched:
                 self.stats.prefetch_activated += 1
             if not pool and k >= R:
                 self._free(sz[k])
         self.R = self.cur_R
+        self.loaded_R = min(self.loaded_R, self.R)
+        self.carried_R = R
+        if self.cross_run:
+            self.J = J0 + M
         self.run += 1
         if ret != OK:
             return ret
         return WARN_SYNC_FALLBACK if fell_back else OK
+
+    def replan(self, depth: int, resident: int, max_vram: int) -> int:
+        """New controls between runs (the next run uses them). Returns the plan's status."""
+        assert self.plan is not None
+        self.depth, self.resident, self.max_vram = depth, resident, max_vram
+        self._release_carried()
+        shared_b = [b for _, b in self.shared]
+        old = self.plan
+        p = plan_slots(self.seg_slot_bytes, shared_b, depth, resident, max_vram, slot_cap=self.slot_cap)
+        if self.use_pool and p.P != old.P:
+            # the pool is given back and allocated at the new count: every slot is emptied
+            self._evict_residents_down_to(0)
+            self._free(old.P * old.S)
+            chosen = None
+            for cap in range(p.P, 0, -1):
+                q = p if cap == p.P else plan_slots(self.seg_slot_bytes, shared_b, depth, resident,
+                                                    max_vram, slot_cap=cap)
+                q.warn_mandatory = p.warn_mandatory
+                if self._alloc(q.P * q.S):
+                    chosen = q
+                    break
+                self.stats.pool_degradations += 1
+            if chosen is None:
+                self.plan = None
+                self.status = ERR_OOM
+                return ERR_OOM
+            if chosen.P < p.P:
+                self.slot_cap = chosen.P
+            p = chosen
+        else:
+            self._evict_residents_down_to(p.R)     # stale residents, from the end of the prefix
+        self.plan = p
+        self.R = p.R                  # a grown prefix is allocated and loaded at the next run
+        self.loaded_R = min(self.loaded_R, p.R)
+        self.d = p.d_req if self.async_ok else 0
+        self.J = 0
+        if p.warn_mandatory:
+            self.warnings.add(WARN_MANDATORY_SLOT)
+        self.status = WARN_MANDATORY_SLOT if p.warn_mandatory else OK
+        return self.status
+
+    def _evict_residents_down_to(self, keep: int) -> None:
+        """Release residents keep .. loaded_R - 1, last first (before the next run's first step)."""
+        for r in range(self.loaded_R - 1, keep - 1, -1):
+            self._emit(-1, EVICT, r, r, 0)
+            self.stats.evictions += 1
+            if not self.use_pool:
+                self._free(self.seg_slot_bytes[r])
+        self.loaded_R = min(self.loaded_R, keep)
+
+    def _release_carried(self) -> None:
+        """Prefetches issued for a run whose plan no longer holds: give back their slots."""
+        for seg, slot in self.carried:
+            self._emit(-1, EVICT, seg, slot, 0)
+            self.stats.evictions += 1
+            if not self.use_pool:
+                self._free(self.seg_slot_bytes[seg])
+        self.carried = []
 
     def _fallback(self) -> None:
         """Asynchronous transfer unavailable or a prefetch allocation failed:
@@ -286,12 +394,12 @@ class Sim:
 
 
 def simulate(seg_slot_bytes, shared=(), depth=0, resident=-1, max_vram=0, use_pool=1, runs=1,
-             alloc_cap=None, fail_async=False, load_bytes=None):
+             alloc_cap=None, fail_async=False, load_bytes=None, cross_run=False):
     """Register then run ``runs`` passes. Returns (sim, [status per run]).
 
     ``load_bytes`` is None or a list (per run) of per-segment byte counts."""
     sim = Sim(list(seg_slot_bytes), list(shared), depth, resident, max_vram, use_pool,
-              alloc_cap=alloc_cap, fail_async=fail_async)
+              alloc_cap=alloc_cap, fail_async=fail_async, cross_run=cross_run)
     st = sim.register()
     if st < 0:
         return sim, [st]
@@ -299,4 +407,22 @@ def simulate(seg_slot_bytes, shared=(), depth=0, resident=-1, max_vram=0, use_po
     for r in range(runs):
         lb = None if load_bytes is None else (lambda s, r=r: load_bytes[r][s])
         out.append(sim.run_once(lb))
+    return sim, out
+
+
+def simulate_script(seg_slot_bytes, shared=(), depth=0, resident=-1, max_vram=0, use_pool=1,
+                    script=(), alloc_cap=None, fail_async=False, cross_run=False):
+    """Register, then follow ``script``: ("run",) for one pass or ("replan", depth, resident,
+    max_vram). Returns (sim, [status per script step]); stops at the first error."""
+    sim = Sim(list(seg_slot_bytes), list(shared), depth, resident, max_vram, use_pool,
+              alloc_cap=alloc_cap, fail_async=fail_async, cross_run=cross_run)
+    st = sim.register()
+    if st < 0:
+        return sim, [st]
+    out = []
+    for step in script:
+        st = sim.run_once() if step[0] == "run" else sim.replan(*step[1:])
+        out.append(st)
+        if st < 0:
+            break
     return sim, out
