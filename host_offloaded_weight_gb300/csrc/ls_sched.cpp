@@ -67,6 +67,7 @@ void Scheduler::configure(const ls_params& p, const std::vector<int64_t>& seg_sl
     std::sort(shared_.begin(), shared_.end());
     cap_ = p.test_alloc_cap_bytes;
     fail_async_ = p.test_fail_async != 0;
+    cross_run_ = p.cross_run_prefetch != 0;
 }
 
 void Scheduler::emit(int step, int kind, int seg, int slot, int64_t bytes) {
@@ -105,29 +106,84 @@ ls_status Scheduler::register_memory(Executor& ex) {
             return LS_ERR_OOM;
         }
     }
-    if (prm_.use_pool) {
-        bool ok = false;
-        for (int cap = p.P; cap >= 1; --cap) {
-            Plan q = cap == p.P ? p
-                                : make_plan(N, S, shared_total, prm_.prefetch_depth,
-                                            prm_.resident_layers, prm_.max_vram_bytes, cap);
-            q.mandatory = mandatory;
-            int64_t bytes = (int64_t)q.P * q.S;
-            if (alloc_bytes(bytes)) {
-                if (ex.alloc_pool(q.P, q.S)) {
-                    p = q;
-                    ok = true;
-                    break;
-                }
-                live_ -= bytes;
-            }
-            ++n_degrade;
-        }
-        if (!ok) return LS_ERR_OOM;
-    }
+    if (prm_.use_pool && !alloc_pool_degrading(ex, p)) return LS_ERR_OOM;
     plan_ = p;
     R_ = p.R;
     d_ = p.d_fit;
+    loaded_R_ = 0;
+    return mandatory ? LS_WARN_MANDATORY_SLOT : LS_OK;
+}
+
+// The pool for plan p, or for fewer slots of the same size (re-planned for that many) when
+// the allocation fails; a reduced count is remembered for later plans. p becomes the plan
+// that got its pool.
+bool Scheduler::alloc_pool_degrading(Executor& ex, Plan& p) {
+    const bool mandatory = p.mandatory;
+    for (int cap = p.P; cap >= 1; --cap) {
+        Plan q = cap == p.P ? p
+                            : make_plan(p.N, p.S, p.shared_total, prm_.prefetch_depth, prm_.resident_layers,
+                                        prm_.max_vram_bytes, cap);
+        q.mandatory = mandatory;
+        const int64_t bytes = (int64_t)q.P * q.S;
+        if (alloc_bytes(bytes)) {
+            if (ex.alloc_pool(q.P, q.S)) {
+                if (q.P < p.P) slot_cap_ = q.P;
+                p = q;
+                return true;
+            }
+            live_ -= bytes;
+        }
+        ++n_degrade;
+    }
+    return false;
+}
+
+void Scheduler::release_carried(Executor& ex) {
+    for (auto& cs : carried_) {
+        emit(-1, LS_EV_EVICT, cs.first, cs.second, 0);
+        ++n_evict;
+        ex.evict(cs.first, cs.second);
+        if (!prm_.use_pool) live_ -= seg_slot_[cs.first];
+    }
+    carried_.clear();
+}
+
+void Scheduler::evict_residents_down_to(Executor& ex, int keep) {
+    for (int r = loaded_R_ - 1; r >= keep; --r) {
+        emit(-1, LS_EV_EVICT, r, r, 0);
+        ++n_evict;
+        ex.evict(r, r);
+        if (!prm_.use_pool) live_ -= seg_slot_[r];
+    }
+    loaded_R_ = std::min(loaded_R_, keep);
+}
+
+ls_status Scheduler::replan(Executor& ex, int depth, int resident, int64_t max_vram) {
+    if (!usable_) return LS_ERR_STATE;
+    prm_.prefetch_depth = depth;
+    prm_.resident_layers = resident;
+    prm_.max_vram_bytes = max_vram;
+    release_carried(ex);
+    Plan p = make_plan(plan_.N, plan_.S, plan_.shared_total, depth, resident, max_vram, slot_cap_);
+    const bool mandatory = p.mandatory;
+    if (prm_.use_pool && p.P != plan_.P) {
+        // another slot count: the pool is given back first, so every slot empties
+        evict_residents_down_to(ex, 0);
+        ex.free_pool();
+        live_ -= (int64_t)plan_.P * plan_.S;
+        if (!alloc_pool_degrading(ex, p)) {
+            usable_ = false;
+            return LS_ERR_OOM;
+        }
+    } else {
+        evict_residents_down_to(ex, p.R);  // stale residents, from the end of the prefix
+    }
+    plan_ = p;
+    R_ = p.R;  // a grown prefix is allocated and loaded at the next run
+    loaded_R_ = std::min(loaded_R_, p.R);
+    d_ = async_ok_ ? p.d_fit : 0;
+    J_ = 0;
+    if (mandatory) warnings |= 1 << LS_WARN_MANDATORY_SLOT;
     return mandatory ? LS_WARN_MANDATORY_SLOT : LS_OK;
 }
 
@@ -148,6 +204,7 @@ bool Scheduler::alloc_seg_evicting(Executor& ex, int seg, int step, int& cur_R) 
 }
 
 ls_status Scheduler::run(Executor& ex, const int64_t* load_bytes) {
+    if (!usable_) return LS_ERR_STATE;
     const int N = plan_.N;
     const bool pool = prm_.use_pool != 0;
     auto lb = [&](int s) { return load_bytes ? load_bytes[s] : seg_slot_[s]; };
@@ -159,50 +216,70 @@ ls_status Scheduler::run(Executor& ex, const int64_t* load_bytes) {
             ++n_shared;
             bytes_loaded += s.second;
         }
-        for (int i = 0; i < R_; ++i) {
-            if (!pool) {
-                if (!alloc_bytes(seg_slot_[i])) {
-                    R_ = i;
-                    break;
-                }
-                if (!ex.alloc_segment(i, seg_slot_[i])) {
-                    live_ -= seg_slot_[i];
-                    R_ = i;
-                    break;
-                }
-            }
-            emit(-1, LS_EV_LOAD_RESIDENT, i, i, lb(i));
-            ex.load(i, i, LS_EV_LOAD_RESIDENT, lb(i));
-            ++n_resident;
-            bytes_loaded += lb(i);
-        }
     }
+    if (!carried_.empty() && carried_R_ != R_) release_carried(ex);  // planned for another ring
+    for (int i = loaded_R_; i < R_; ++i) {  // residents that hold no data yet
+        if (!pool) {
+            if (!alloc_bytes(seg_slot_[i])) {
+                R_ = i;
+                break;
+            }
+            if (!ex.alloc_segment(i, seg_slot_[i])) {
+                live_ -= seg_slot_[i];
+                R_ = i;
+                break;
+            }
+        }
+        emit(-1, LS_EV_LOAD_RESIDENT, i, i, lb(i));
+        ex.load(i, i, LS_EV_LOAD_RESIDENT, lb(i));
+        ++n_resident;
+        bytes_loaded += lb(i);
+    }
+    loaded_R_ = R_;
     const int R = R_;
     const int M = N - R;
     const int Q = M > 0 ? std::min(d_ + 1, M) : 0;
     int d = std::min(d_, M);
+    const int64_t J0 = cross_run_ ? J_ : 0;
+    // the window reaches into the next run only with a full ring of d + 1 slots
+    const int reach = (cross_run_ && M > d) ? M + d : M;
+    auto ring_slot = [&](int64_t j) { return R + (int)((J0 + j) % Q); };
     int cur_R = R;
-    int next_load = 0;
     std::vector<char> queued(N, 0);
+    for (auto& cs : carried_) queued[cs.first] = 1;  // issued by the previous run
+    int next_load = (int)carried_.size();
+    carried_.clear();
     bool fell_back = false;
     ls_status st = LS_OK;
     for (int k = 0; k < N; ++k) {
         const int streamed_upto = std::max(0, k - R + 1);
         if (d >= 1 && async_ok_) {
-            while (next_load < M && next_load < streamed_upto + d) {
-                const int seg = R + next_load;
-                if (fail_async_ || (!pool && !alloc_seg_evicting(ex, seg, k, cur_R))) {
+            while (next_load < reach && next_load < streamed_upto + d) {
+                const int seg = R + next_load % M;
+                if (next_load >= M) {
+                    // the next run's loads never evict: without room that run loads them itself
+                    if (!pool) {
+                        if (!alloc_bytes(seg_slot_[seg])) break;
+                        if (!ex.alloc_segment(seg, seg_slot_[seg])) {
+                            live_ -= seg_slot_[seg];
+                            break;
+                        }
+                    }
+                } else if (fail_async_ || (!pool && !alloc_seg_evicting(ex, seg, k, cur_R))) {
                     fallback();
                     fell_back = true;
                     d = 0;
                     break;
                 }
-                const int slot = R + next_load % Q;
+                const int slot = ring_slot(next_load);
                 emit(k, LS_EV_PREFETCH, seg, slot, lb(seg));
                 ex.load(seg, slot, LS_EV_PREFETCH, lb(seg));
                 ++n_prefetch;
                 bytes_loaded += lb(seg);
-                queued[seg] = 1;
+                if (next_load < M)
+                    queued[seg] = 1;
+                else
+                    carried_.push_back({seg, slot});
                 ++next_load;
             }
         }
@@ -211,14 +288,14 @@ ls_status Scheduler::run(Executor& ex, const int64_t* load_bytes) {
                 st = LS_ERR_OOM;
                 break;
             }
-            const int slot = R + (k - R) % Q;
+            const int slot = ring_slot(k - R);
             emit(k, LS_EV_LOAD_SYNC, k, slot, lb(k));
             ex.load(k, slot, LS_EV_LOAD_SYNC, lb(k));
             ++n_sync;
             bytes_loaded += lb(k);
             next_load = k - R + 1;
         }
-        const int slot = k < R ? k : R + (k - R) % Q;
+        const int slot = k < R ? k : ring_slot(k - R);
         emit(k, LS_EV_ACTIVATE, k, slot, 0);
         ex.activate(k, slot, queued[k] != 0);
         if (queued[k]) ++n_prefetch_activated;
@@ -228,6 +305,9 @@ ls_status Scheduler::run(Executor& ex, const int64_t* load_bytes) {
         }
     }
     R_ = cur_R;
+    loaded_R_ = std::min(loaded_R_, R_);
+    carried_R_ = R;
+    if (cross_run_) J_ = J0 + M;
     ++run_;
     if (st != LS_OK) return st;
     return fell_back ? LS_WARN_SYNC_FALLBACK : LS_OK;

@@ -16,9 +16,17 @@
 //   Per step k: queue prefetches until the loads issued reach (streamed
 //   segments <= k) + d; load k synchronously if it was not queued; activate k.
 //   A failing pool is retried with fewer slots of the same size (re-planned
-//   for that many); pool off, a failing load first evicts the last resident
-//   already computed in this run, a failing prefetch then falls back to
-//   synchronous loads for good, a failing synchronous load fails the run.
+//   for that many, and the reduced count is remembered); pool off, a failing
+//   load first evicts the last resident already computed in this run, a
+//   failing prefetch then falls back to synchronous loads for good, a failing
+//   synchronous load fails the run.
+// Plan changes between runs (replan): prefetches issued for the next run are
+//   released, residents the new plan does not hold are released from the end of
+//   the prefix; the pool is kept at the same slot count and reallocated
+//   otherwise (emptying every slot); each run first loads the residents that
+//   hold no data yet. Cross-run window (opt-in): the window of the last steps
+//   reaches into the next run's first streamed segments when the ring is a full
+//   d + 1 slots; load numbers then continue across runs (slot R + (J mod Q)).
 #pragma once
 #include <cstdint>
 #include <vector>
@@ -54,7 +62,8 @@ struct Executor {
     virtual void load_shared(int shared_id) = 0;
     virtual void load(int seg, int slot, int kind, int64_t bytes) = 0;   // kind = LS_EV_*
     virtual void activate(int seg, int slot, bool via_copy_queue) = 0;
-    virtual void evict(int seg, int slot) = 0;
+    virtual void evict(int seg, int slot) = 0;              // resident, or a stale prefetch
+    virtual void free_pool() = 0;                           // before a pool of another size
 };
 
 class Scheduler {
@@ -64,6 +73,9 @@ public:
                    const std::vector<std::pair<int, int64_t>>& shared);
     ls_status register_memory(Executor& ex);                 // plan + shared region + pool
     ls_status run(Executor& ex, const int64_t* load_bytes);  // one pass; load_bytes[N] or null
+    // New controls for the next run; LS_ERR_OOM (no pool at all) leaves the scheduler unusable.
+    ls_status replan(Executor& ex, int depth, int resident, int64_t max_vram);
+    bool usable() const { return usable_; }
     const Plan& plan() const { return plan_; }
     const std::vector<ls_sched_event>& log() const { return log_; }
     void fill_stats(ls_stats& s) const;
@@ -79,6 +91,9 @@ private:
         return true;
     }
     bool alloc_seg_evicting(Executor& ex, int seg, int step, int& cur_R);
+    bool alloc_pool_degrading(Executor& ex, Plan& p);
+    void release_carried(Executor& ex);
+    void evict_residents_down_to(Executor& ex, int keep);
     void emit(int step, int kind, int seg, int slot, int64_t bytes);
     void fallback();
 
@@ -87,7 +102,12 @@ private:
     std::vector<std::pair<int, int64_t>> shared_;
     Plan plan_;
     int R_ = 0, d_ = 0, run_ = 0;
-    bool async_ok_ = true, fail_async_ = false;
+    bool async_ok_ = true, fail_async_ = false, cross_run_ = false, usable_ = true;
+    int slot_cap_ = -1;                            // remembered reduced pool slot count
+    int loaded_R_ = 0;                             // leading residents holding their data
+    int64_t J_ = 0;                                // streamed loads since the last plan change
+    std::vector<std::pair<int, int>> carried_;     // (segment, slot) prefetched for the next run
+    int carried_R_ = 0;
     int64_t cap_ = 0, live_ = 0;
     std::vector<ls_sched_event> log_;
 

@@ -530,6 +530,11 @@ struct GpuExec : Executor {
         dev_free(c, c->seg_buf[seg], (size_t)c->segs[seg].slot_bytes, rc.s);
         c->seg_buf[seg] = nullptr;
     }
+    void free_pool() override {
+        dev_free(c, c->pool, (size_t)c->pool_bytes, c->copy_stream);
+        c->pool = nullptr;
+        c->pool_bytes = 0;
+    }
 };
 
 struct DryExec : Executor {
@@ -542,6 +547,7 @@ struct DryExec : Executor {
     void load(int, int, int, int64_t) override {}
     void activate(int, int, bool) override {}
     void evict(int, int) override {}
+    void free_pool() override {}
 };
 
 ls_status check_params(const ls_params* p, ls_params* out, std::string* why) {
@@ -577,6 +583,7 @@ ls_status check_params(const ls_params* p, ls_params* out, std::string* why) {
         return LS_ERR_INVALID_ARG;
     }
     if ((d.alloc_fn == nullptr) != (d.free_fn == nullptr)) { *why = "alloc_fn and free_fn go together"; return LS_ERR_INVALID_ARG; }
+    if (d.cross_run_prefetch != 0 && d.cross_run_prefetch != 1) { *why = "cross_run_prefetch must be 0 or 1"; return LS_ERR_INVALID_ARG; }
     *out = d;
     return LS_OK;
 }
@@ -839,6 +846,7 @@ void ls_params_init(ls_params* p) {
     p->copy_ctas = 0;
     p->reserve_sms = -1;
     p->device = -1;
+    p->cross_run_prefetch = 0;
 }
 
 const char* ls_status_string(ls_status s) {
@@ -1001,15 +1009,20 @@ static ls_status register_impl(ls_ctx* c, const ls_segment_desc* segs, int32_t n
     for (int s = 0; s < n; ++s) seg_slot[s] = c->segs[s].slot_bytes;
     std::vector<std::pair<int, int64_t>> shared_bytes;
     for (auto& s : c->shared) shared_bytes.push_back({s.id, (int64_t)s.bytes});
-    c->sched.configure(c->prm, seg_slot, shared_bytes);
+    {
+        ls_params sp = c->prm;
+        // a MoE segment's next loads depend on the next run's routing: no cross-run window
+        if (c->kind == LS_KIND_MOE_SWIGLU_BF16) sp.cross_run_prefetch = 0;
+        c->sched.configure(sp, seg_slot, shared_bytes);
+    }
     GpuExec ex(c);
     ls_status plan_st = c->sched.register_memory(ex);
     if (plan_st < 0) {
         set_err(c, "could not allocate the parameter memory (not even one slot)");
         return plan_st;
     }
-    const Plan& p = c->sched.plan();
-    const int P = std::max(1, p.P);
+    // per-slot words and events for any plan a later ls_replan may choose (P <= N)
+    const int P = std::max(1, n);
     CK(cudaMalloc(&c->ready, sizeof(uint32_t) * P));
     CK(cudaMalloc(&c->tickets, sizeof(uint32_t) * P));
     CK(cudaMemset(c->ready, 0, sizeof(uint32_t) * P));
@@ -1130,6 +1143,39 @@ ls_status ls_sync(ls_ctx* c) {
         return LS_ERR_CUDA;
     }
     return LS_OK;
+}
+
+ls_status ls_replan(ls_ctx* c, int32_t prefetch_depth, int32_t resident_layers, int64_t max_vram_bytes) {
+    if (!c) return LS_ERR_INVALID_ARG;
+    if (!c->registered) {
+        set_err(c, "ls_replan before ls_register_segments");
+        return LS_ERR_STATE;
+    }
+    if (!c->pending.empty()) {
+        set_err(c, "ls_replan: passes are queued; call ls_sync first");
+        return LS_ERR_STATE;
+    }
+    if (prefetch_depth < 0 || resident_layers < -1 || max_vram_bytes < 0) {
+        set_err(c, "ls_replan: depth and budget must be >= 0, resident_layers >= -1");
+        return LS_ERR_INVALID_ARG;
+    }
+    CK(cudaSetDevice(c->device));
+    // queued copies (a cross-run prefetch) land before their slots change hands
+    CK(cudaStreamSynchronize(c->copy_stream));
+    GpuExec ex(c);
+    ex.rc = RunCtx{nullptr, nullptr, 0, c->copy_stream, 0};
+    const ls_status st = c->sched.replan(ex, prefetch_depth, resident_layers, max_vram_bytes);
+    CK(cudaStreamSynchronize(c->copy_stream));  // releases and the new pool are in place
+    if (c->cuda_err != cudaSuccess) {
+        set_err(c, "ls_replan: %s", cudaGetErrorString(c->cuda_err));
+        c->cuda_err = cudaSuccess;
+        return LS_ERR_CUDA;
+    }
+    c->prm.prefetch_depth = prefetch_depth;
+    c->prm.resident_layers = resident_layers;
+    c->prm.max_vram_bytes = max_vram_bytes;
+    if (st == LS_ERR_OOM) set_err(c, "ls_replan: not even a one-slot pool could be allocated; the context cannot run");
+    return st;
 }
 
 ls_status ls_run(ls_ctx* c, const void* x_dev, void* y_dev, int64_t tokens, void* stream,
@@ -1291,6 +1337,66 @@ void ls_ctx_destroy(ls_ctx* c) {
     if (!c) return;
     release_resources(c);
     delete c;
+}
+
+static void copy_out(const Scheduler& sched, bool planned, ls_sched_event* events, int64_t cap, int64_t* n_events,
+                     ls_stats* stats, ls_status* bad) {
+    const auto& log = sched.log();
+    *n_events = (int64_t)log.size();
+    const int64_t m = std::min<int64_t>(cap, (int64_t)log.size());
+    if (m > 0) memcpy(events, log.data(), sizeof(ls_sched_event) * m);
+    if (stats) {
+        if (stats->struct_size < offsetof(ls_stats, slot_bytes)) {
+            *bad = LS_ERR_INVALID_ARG;
+            return;
+        }
+        ls_stats s;
+        memset(&s, 0, sizeof(s));
+        if (planned) sched.fill_stats(s);
+        s.copy_path = LS_COPY_AUTO;
+        const uint32_t sz = std::min<uint32_t>(stats->struct_size, sizeof(s));
+        memcpy(stats, &s, sz);
+        stats->struct_size = sz;
+    }
+}
+
+ls_status ls_simulate_script(const ls_params* params, const int64_t* seg_slot_bytes, int32_t n,
+                             const int64_t* shared_bytes, const int32_t* shared_ids, int32_t n_shared,
+                             const int64_t* script, int32_t n_steps, ls_sched_event* events, int64_t cap,
+                             int64_t* n_events, ls_stats* stats, ls_status* step_status) {
+    ls_params p;
+    std::string why;
+    ls_status st = check_params(params, &p, &why);
+    if (st != LS_OK) return st;
+    if (!seg_slot_bytes || n < 1 || n_steps < 0 || (n_steps > 0 && !script) ||
+        (n_shared > 0 && (!shared_bytes || !shared_ids)) || !n_events || (cap > 0 && !events))
+        return LS_ERR_INVALID_ARG;
+    std::vector<int64_t> seg(seg_slot_bytes, seg_slot_bytes + n);
+    for (int64_t b : seg)
+        if (b <= 0) return LS_ERR_INVALID_ARG;
+    std::vector<std::pair<int, int64_t>> sh;
+    for (int i = 0; i < n_shared; ++i) sh.push_back({shared_ids[i], shared_bytes[i]});
+    Scheduler sched;
+    sched.configure(p, seg, sh);
+    DryExec ex;
+    ls_status reg = sched.register_memory(ex);
+    if (reg >= 0) {
+        for (int i = 0; i < n_steps; ++i) {
+            const int64_t* op = script + 4 * (int64_t)i;
+            ls_status rs;
+            if (op[0] == 0)
+                rs = sched.run(ex, nullptr);
+            else if (op[0] == 1 && op[1] >= 0 && op[2] >= -1 && op[3] >= 0)
+                rs = sched.replan(ex, (int)op[1], (int)op[2], op[3]);
+            else
+                rs = LS_ERR_INVALID_ARG;
+            if (step_status) step_status[i] = rs;
+            if (rs < 0) break;
+        }
+    }
+    ls_status bad = LS_OK;
+    copy_out(sched, reg >= 0 && sched.usable(), events, cap, n_events, stats, &bad);
+    return bad != LS_OK ? bad : reg;
 }
 
 ls_status ls_simulate(const ls_params* params, const int64_t* seg_slot_bytes, int32_t n, const int64_t* shared_bytes,

@@ -43,7 +43,8 @@ class ls_params(C.Structure):
                 ("reserve_sms", C.c_int32), ("device", C.c_int32),
                 ("alloc_fn", ALLOC_FN), ("free_fn", FREE_FN), ("alloc_user", C.c_void_p),
                 ("test_alloc_cap_bytes", C.c_int64), ("test_fail_async", C.c_int32),
-                ("test_drop_publish", C.c_int32), ("kernel_timing", C.c_int32)]
+                ("test_drop_publish", C.c_int32), ("kernel_timing", C.c_int32),
+                ("cross_run_prefetch", C.c_int32)]
 
 
 class ls_tensor_desc(C.Structure):
@@ -105,6 +106,10 @@ _sig = {
     "ls_get_schedule": (_I32, [_P, C.POINTER(ls_sched_event), _I64, C.POINTER(_I64)]),
     "ls_get_stats": (_I32, [_P, C.POINTER(ls_stats)]),
     "ls_set_kernel_timing": (_I32, [_P, _I32]),
+    "ls_replan": (_I32, [_P, _I32, _I32, _I64]),
+    "ls_simulate_script": (_I32, [C.POINTER(ls_params), C.POINTER(_I64), _I32, C.POINTER(_I64),
+                                  C.POINTER(_I32), _I32, C.POINTER(_I64), _I32, C.POINTER(ls_sched_event),
+                                  _I64, C.POINTER(_I64), C.POINTER(ls_stats), C.POINTER(_I32)]),
     "ls_get_kernel_times": (_I32, [_P, C.POINTER(ls_kernel_time), _I32, C.POINTER(_I32), _I32]),
     "ls_get_trace": (_I32, [_P, C.POINTER(ls_trace_event), _I64, C.POINTER(_I64)]),
     "ls_ctx_destroy": (None, [_P]),
@@ -298,6 +303,11 @@ def ls_get_stats(ctx: Ctx) -> dict:
     return _stats_dict(s)
 
 
+def ls_replan(ctx: Ctx, prefetch_depth: int, resident_layers: int, max_vram_bytes: int) -> int:
+    """New streaming controls for the next run (see include/ls_api.h)."""
+    return _check(_lib.ls_replan(ctx.handle, prefetch_depth, resident_layers, max_vram_bytes), ctx)
+
+
 def ls_set_kernel_timing(ctx: Ctx, mode: int) -> int:
     return _check(_lib.ls_set_kernel_timing(ctx.handle, mode), ctx)
 
@@ -352,6 +362,31 @@ def ls_simulate(params: ls_params, seg_slot_bytes, shared=(), runs: int = 1, loa
     status = _lib.ls_simulate(C.byref(params), seg, n, sb, sid, len(shared), runs, lb, buf,
                               total.value, C.byref(total), C.byref(st), rs)
     return status, _events(buf, total.value), _stats_dict(st), list(rs[:runs])
+
+
+def ls_simulate_script(params: ls_params, seg_slot_bytes, script, shared=()):
+    """ls_simulate along a script of ("run",) and ("replan", depth, resident, max_vram)
+    steps. Returns (status, events, stats, step_status)."""
+    n = len(seg_slot_bytes)
+    seg = (_I64 * n)(*seg_slot_bytes)
+    sb = (_I64 * max(1, len(shared)))(*[b for _, b in shared])
+    sid = (_I32 * max(1, len(shared)))(*[i for i, _ in shared])
+    flat = []
+    for step in script:
+        flat += [0, 0, 0, 0] if step[0] == "run" else [1, int(step[1]), int(step[2]), int(step[3])]
+    sc = (_I64 * max(1, len(flat)))(*flat)
+    total = _I64()
+    st = ls_stats()
+    st.struct_size = C.sizeof(ls_stats)
+    ss = (_I32 * max(1, len(script)))(*([1 << 30] * max(1, len(script))))
+    status = _lib.ls_simulate_script(C.byref(params), seg, n, sb, sid, len(shared), sc, len(script), None, 0,
+                                     C.byref(total), C.byref(st), ss)
+    buf = (ls_sched_event * max(1, total.value))()
+    ss = (_I32 * max(1, len(script)))(*([1 << 30] * max(1, len(script))))
+    status = _lib.ls_simulate_script(C.byref(params), seg, n, sb, sid, len(shared), sc, len(script), buf,
+                                     total.value, C.byref(total), C.byref(st), ss)
+    steps = [v for v in ss[:len(script)] if v != 1 << 30]
+    return status, _events(buf, total.value), _stats_dict(st), steps
 
 
 # ------------------------------------------------------------------ ls_kernels.h

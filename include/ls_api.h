@@ -73,11 +73,13 @@ enum { LS_DTYPE_F32 = 0, LS_DTYPE_BF16 = 1 };
 /* Schedule event kinds (ls_sched_event.kind). */
 enum {
     LS_EV_SHARED_LOAD = 0,   /* a deduplicated shared tensor copied into the shared region (run 0) */
-    LS_EV_LOAD_RESIDENT = 1, /* a resident-prefix segment copied synchronously (run 0) */
+    LS_EV_LOAD_RESIDENT = 1, /* a resident-prefix segment copied synchronously before a run's first
+                                step (run 0, or the first run after a plan change grew the prefix) */
     LS_EV_LOAD_SYNC = 2,     /* a streamed segment copied on the compute stream right before use */
     LS_EV_PREFETCH = 3,      /* a streamed segment queued on the copy stream ahead of use */
     LS_EV_ACTIVATE = 4,      /* the segment's compute was issued, reading its slot */
-    LS_EV_EVICT = 5          /* a resident was released under memory pressure (pool off) */
+    LS_EV_EVICT = 5          /* a resident released under memory pressure (pool off, at a step) or at a
+                                plan change (step -1), or a stale cross-run prefetch (step -1) */
 };
 
 enum { LS_COPY_AUTO = 0, LS_COPY_KERNEL = 1, LS_COPY_ENGINE = 2 };
@@ -116,6 +118,13 @@ typedef struct ls_params {
     int32_t test_drop_publish;    /* the Nth publish (1-based, over the context's life) leaves its ready word down */
     int32_t kernel_timing;        /* 1 = bracket every launch with CUDA events (see ls_get_kernel_times);
                                      2 = also keep a per-launch trace (see ls_get_trace) */
+    int32_t cross_run_prefetch;   /* 1 = the prefetch window crosses the run boundary: the last steps of
+                                     a run also queue the next run's first streamed segments (when the
+                                     ring is a full depth + 1 slots; never for the MoE kind, whose next
+                                     loads depend on the next run's routing). 0 (default) = every run
+                                     starts its window afresh ("feat: prefetch streamed layers during
+                                     compute", maintainer review: no cross-forward state). The prefetch
+                                     of a run that never comes is released at ls_replan or destroy. */
 } ls_params;
 
 /* One tensor of a segment: host memory owned by the caller, kept alive and
@@ -268,6 +277,27 @@ ls_status ls_get_stats(ls_ctx* ctx, ls_stats* out);
  * mode outside 0..2. The pages define no such call: it is instrumentation. */
 ls_status ls_set_kernel_timing(ls_ctx* ctx, int32_t mode);
 
+/* New streaming controls between runs ("feat: prefetch streamed layers during
+ * compute", Summary: residents are evicted from the end of the prefix under
+ * memory pressure, and stale residents and prefetches are released when the
+ * plan changes; "feat: pool VRAM for streamed layer", Summary: a sufficiently
+ * large pool is reused and reduced caps are remembered). The next run plans
+ * with the same rules as ls_register_segments, under any remembered reduced
+ * pool slot count; a remembered synchronous fallback stays. Before that run's
+ * first step:
+ *  - prefetches already queued for it (cross_run_prefetch) are released;
+ *  - residents beyond the new prefix are released, last first (LS_EV_EVICT, step -1);
+ *  - pool on: the pool is kept when its slot count does not change. Otherwise it
+ *    is freed and a pool of the new count is allocated (fewer slots on failure).
+ *    That empties every slot, so the whole new prefix is loaded again;
+ *  - newly resident segments are loaded (LS_EV_LOAD_RESIDENT).
+ * Returns LS_OK or LS_WARN_MANDATORY_SLOT (the new budget is below one slot);
+ * LS_ERR_STATE while passes from ls_run_async await ls_sync;
+ * LS_ERR_INVALID_ARG for a negative depth or budget or a resident cap below -1;
+ * LS_ERR_OOM when not even a one-slot pool can be allocated, after which the
+ * context cannot run (destroy it). Blocks until queued copies finish. */
+ls_status ls_replan(ls_ctx* ctx, int32_t prefetch_depth, int32_t resident_layers, int64_t max_vram_bytes);
+
 /* Copy up to cap kernel-time records into out; *n_out = number of classes.
  * reset != 0 clears the accumulators afterwards. */
 ls_status ls_get_kernel_times(ls_ctx* ctx, ls_kernel_time* out, int32_t cap, int32_t* n_out, int32_t reset);
@@ -290,6 +320,16 @@ const char* ls_last_error(const ls_ctx* ctx);
  * the segment's footprint) or [runs][n] bytes per load. run_status[runs]
  * receives each run's status (LS_ERR_OOM at registration leaves it untouched).
  * events: up to cap written; *n_events = total. */
+/* ls_simulate driven by a script instead of a run count: script[4 * i ..] =
+ * {op, depth, resident, max_vram_bytes}, op 0 = one run (the other three
+ * ignored), op 1 = ls_replan with those controls. step_status[n_steps] receives
+ * each step's status; the script stops at the first error. Loads move each
+ * segment's footprint. Other arguments as for ls_simulate. */
+ls_status ls_simulate_script(const ls_params* params, const int64_t* seg_slot_bytes, int32_t n,
+                             const int64_t* shared_bytes, const int32_t* shared_ids, int32_t n_shared,
+                             const int64_t* script, int32_t n_steps, ls_sched_event* events, int64_t cap,
+                             int64_t* n_events, ls_stats* stats, ls_status* step_status);
+
 ls_status ls_simulate(const ls_params* params, const int64_t* seg_slot_bytes, int32_t n,
                       const int64_t* shared_bytes, const int32_t* shared_ids, int32_t n_shared,
                       int32_t runs, const int64_t* load_bytes, ls_sched_event* events,

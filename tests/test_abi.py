@@ -4,6 +4,7 @@ events as the independent policy simulator."""
 import ctypes
 import itertools
 import os
+import random
 import re
 import subprocess
 
@@ -119,3 +120,50 @@ def test_native_scheduler_matches_simulator_failures():
 def test_native_scheduler_per_run_load_bytes():
     load = [[10, 20, 30, 40], [11, 21, 31, 41]]
     _compare([100] * 4, [], 1, 1, 1000, 1, runs=2, load=load)
+
+
+def _compare_script(seg, shared, depth, resident, budget, pool, script, cap=None, fail_async=False,
+                    cross=False):
+    """The library's scheduler and the policy simulator follow the same script of runs and
+    plan changes: same events, same per-step statuses, same counters."""
+    p = L.ls_params_init(prefetch_depth=depth, resident_layers=resident, max_vram_bytes=budget,
+                         use_pool=pool, test_alloc_cap_bytes=cap or 0, test_fail_async=int(fail_async),
+                         cross_run_prefetch=int(cross))
+    st, ev, stats, steps = L.ls_simulate_script(p, seg, script, shared)
+    sim, ref = pol.simulate_script(seg, shared, depth, resident, budget, use_pool=pool, script=script,
+                                      alloc_cap=cap, fail_async=fail_async, cross_run=cross)
+    ctx = (seg, shared, depth, resident, budget, pool, script, cap, fail_async, cross)
+    if sim.plan is None and not ref:
+        assert st == sim.status, ctx
+        return
+    assert steps == ref, ctx
+    assert ev == sim.events, ctx
+    if sim.plan is not None:
+        assert stats["evictions"] == sim.stats.evictions, ctx
+        assert stats["prefetch_queued"] == sim.stats.prefetch_queued, ctx
+        assert stats["prefetch_activated"] == sim.stats.prefetch_activated, ctx
+        assert stats["resident_loads"] == sim.stats.resident_loads, ctx
+        assert stats["pool_degradations"] == sim.stats.pool_degradations, ctx
+
+
+def test_native_scheduler_matches_simulator_plan_changes():
+    rng = random.Random(11)
+    n = 0
+    for _ in range(1500):
+        N = rng.randint(1, 7)
+        seg = [rng.choice([64, 100, 128]) for _ in range(N)]
+        S = max(seg)
+        shared = [] if rng.random() < 0.7 else [(3, rng.choice([40, 200]))]
+        sh = sum((b + 255) // 256 * 256 for _, b in shared)
+
+        def controls():
+            return (rng.randint(0, N), rng.randint(-1, N),
+                    rng.choice([0, sh + rng.randint(1, N + 2) * S, rng.randint(0, sh + (N + 2) * S)]))
+        d0, r0, b0 = controls()
+        script = [("run",) if rng.random() < 0.6 else ("replan",) + controls() for _ in range(rng.randint(1, 6))]
+        script.append(("run",))
+        cap = None if rng.random() < 0.6 else sh + rng.randint(1, N + 2) * S
+        _compare_script(seg, shared, d0, r0, b0, rng.randint(0, 1), script, cap=cap,
+                        fail_async=rng.random() < 0.15, cross=rng.random() < 0.5)
+        n += 1
+    assert n == 1500

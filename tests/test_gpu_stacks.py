@@ -309,6 +309,107 @@ def test_kernel_timing_switch():
         L.ls_ctx_destroy(ctx)
 
 
+# ------------------------------------------------------------------ plan changes, cross-run window
+def _sched_script(cfg, hs, depth, resident, budget, pool, script, cross=False):
+    seg = [synth.segment_slot_bytes(cfg)] * len(hs.segments)
+    shared = [(i, v.nbytes) for i, v in enumerate(hs.shared_views)]
+    exact = sum(t.nbytes for t in synth.segment_tensors(cfg))
+    sim, st = policy.simulate_script(seg, shared, depth, resident, budget, use_pool=pool, script=script,
+                                     cross_run=cross)
+    # a load moves the segment's exact private bytes, not its aligned footprint
+    ev = [(r, k, kind, sg, sl, exact if kind in (policy.PREFETCH, policy.LOAD_SYNC, policy.LOAD_RESIDENT) else b)
+          for (r, k, kind, sg, sl, b) in sim.events]
+    return ev, st
+
+
+@pytest.mark.parametrize("pool", [1, 0])
+def test_replan_between_runs_keeps_the_bits(pool):
+    """Budget shrinks and grows between runs ("releases stale residents and prefetches when
+    the graph plan changes"; "evicts residents from the end of the resident prefix"): every
+    run's output equals the all-resident output bit for bit, and the executed schedule is the
+    simulator's."""
+    cfg = SMALL["ffn"]
+    hs = synth.HostStack(cfg)
+    S = synth.segment_slot_bytes(cfg)
+    ref, _, _, _, _ = _run(cfg, hs, runs=1, max_vram_bytes=0)
+    steps = [("run",), ("replan", 1, -1, 4 * S), ("run",), ("replan", 1, -1, 2 * S), ("run",),
+             ("replan", 2, 1, 5 * S), ("run",), ("replan", 1, -1, 0), ("run",), ("replan", 1, -1, S // 2),
+             ("run",)]
+    ctx, _ = make_ctx(cfg, hs, prefetch_depth=1, resident_layers=-1, max_vram_bytes=3 * S, use_pool=pool)
+    try:
+        x = x_dev(cfg)
+        got = []
+        for st in steps:
+            if st[0] == "run":
+                y = torch.empty_like(x)
+                L.ls_run(ctx, x, y, cfg.tokens)
+                got.append(y)
+            else:
+                L.ls_replan(ctx, *st[1:])
+        torch.cuda.synchronize()
+        for y in got:
+            assert torch.equal(y.view(torch.int16), ref.view(torch.int16))
+        ev, sst = _sched_script(cfg, hs, 1, -1, 3 * S, pool, steps)
+        assert L.ls_get_schedule(ctx) == ev
+        assert L.ls_get_stats(ctx)["residents"] == 0
+    finally:
+        L.ls_ctx_destroy(ctx)
+
+
+@pytest.mark.parametrize("pool", [1, 0])
+def test_cross_run_window_matches_simulator_and_bits(pool):
+    """The opt-in cross-run window queues the next run's first streamed segment during the
+    last step; outputs stay identical, the schedule is the simulator's, and a plan change
+    releases the queued prefetch."""
+    cfg = SMALL["ffn"]
+    hs = synth.HostStack(cfg)
+    S = synth.segment_slot_bytes(cfg)
+    ref, _, _, _, _ = _run(cfg, hs, runs=1, max_vram_bytes=0)
+    ctx, _ = make_ctx(cfg, hs, prefetch_depth=1, resident_layers=0, max_vram_bytes=2 * S, use_pool=pool,
+                      cross_run_prefetch=1)
+    try:
+        x = x_dev(cfg)
+        ys = [torch.empty_like(x) for _ in range(3)]
+        for y in ys:
+            L.ls_run_async(ctx, x, y, cfg.tokens)
+        L.ls_sync(ctx)
+        L.ls_replan(ctx, 1, 0, 3 * S)
+        y4 = torch.empty_like(x)
+        L.ls_run(ctx, x, y4, cfg.tokens)
+        torch.cuda.synchronize()
+        for y in ys + [y4]:
+            assert torch.equal(y.view(torch.int16), ref.view(torch.int16))
+        steps = [("run",)] * 3 + [("replan", 1, 0, 3 * S), ("run",)]
+        ev, _ = _sched_script(cfg, hs, 1, 0, 2 * S, pool, steps, cross=True)
+        assert L.ls_get_schedule(ctx) == ev
+        kinds = [e[2] for e in ev if e[0] == 3 and e[1] == -1]
+        assert kinds[0] == policy.EVICT                         # the stale cross-run prefetch
+        assert L.ls_get_stats(ctx)["sync_loads"] == 0
+    finally:
+        L.ls_ctx_destroy(ctx)
+
+
+def test_replan_refused_while_passes_are_queued():
+    cfg = SMALL["ffn"]
+    hs = synth.HostStack(cfg)
+    S = synth.segment_slot_bytes(cfg)
+    ctx, _ = make_ctx(cfg, hs, prefetch_depth=1, max_vram_bytes=3 * S, use_pool=1)
+    try:
+        x = x_dev(cfg)
+        y = torch.empty_like(x)
+        L.ls_run_async(ctx, x, y, cfg.tokens)
+        with pytest.raises(L.LsError) as e:
+            L.ls_replan(ctx, 1, -1, 2 * S)
+        assert e.value.status == L.LS_ERR_STATE
+        L.ls_sync(ctx)
+        with pytest.raises(L.LsError) as e:
+            L.ls_replan(ctx, -1, -1, 2 * S)
+        assert e.value.status == L.LS_ERR_INVALID_ARG
+        assert L.ls_replan(ctx, 1, -1, 2 * S) == L.LS_OK
+    finally:
+        L.ls_ctx_destroy(ctx)
+
+
 # ------------------------------------------------------------------ MoE
 def _moe_cfg(layers, tokens, experts=128, hidden=2048, ffn=768, k=8):
     c = synth.MOE.with_(n_segments=layers, tokens=tokens, n_experts=experts, hidden=hidden, ffn=ffn, top_k=k)
