@@ -248,7 +248,8 @@ def run_ours(args, cfg, world, rank, local):
     p = L.ls_params_init(prefetch_depth=cfg.prefetch_depth, resident_layers=cfg.resident_layers,
                          max_vram_bytes=cfg.max_vram_bytes, use_pool=cfg.use_pool,
                          copy_path={"auto": 0, "kernel": 1, "engine": 2}[args.copy_path],
-                         copy_ctas=args.copy_ctas, reserve_sms=args.reserve_sms, kernel_timing=0)
+                         copy_ctas=args.copy_ctas, reserve_sms=args.reserve_sms, kernel_timing=0,
+                         cross_run_prefetch=int(args.cross_run))
     ctx = L.ls_ctx_create(p)
     L.ls_register_segments(ctx, hs.segments, hs.shared_map)
     T = cfg.tokens
@@ -359,6 +360,7 @@ def run_ours(args, cfg, world, rank, local):
                             "pool_slots": stats["pool_slots"], "slot_bytes": stats["slot_bytes"],
                             "warnings": stats["warnings"]},
                    "parallelism": f"replicas{world}" if world > 1 else "single",
+                   "cross_run_prefetch": bool(args.cross_run),
                    "l2": "flushed between timed passes (256 MB write)"},
         "overlap_eff": max(link_bytes / (link_peak * 1e9), flops / (tc_peak * 1e12)) / mean_s,
         "link_gbs": link_bytes / mean_s / 1e9, "link_peak_gbs": link_peak,
@@ -414,6 +416,8 @@ def main() -> int:
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--prefetch-depth", type=int, default=None,
                     help="override the workload's prefetch depth (the planner re-derives residents)")
+    ap.add_argument("--cross-run", action="store_true",
+                    help="let the prefetch window cross the pass boundary (off by default, as in the pages)")
     ap.add_argument("--max-vram-bytes", type=int, default=None,
                     help="override the workload's parameter budget (e.g. a one-slot run)")
     args = ap.parse_args()
