@@ -265,11 +265,15 @@ def run_ours(args, cfg, world, rank, local):
     gpu_id = "GPU-" + str(torch.cuda.get_device_properties(local).uuid)
     sampler = ClockSampler(gpu_id)   # started early: its start-up must not overlap the timed region
     time.sleep(1.5)
-    for _ in range(args.warmup):
-        L.ls_run(ctx, x, y, T, s, logits=logits, top_k=cfg.top_k)
+    for _ in range(args.warmup):   # with --graph the warm-up also captures the pass
+        if args.graph:
+            L.ls_run_graph(ctx, x, y, T, s)
+            L.ls_sync(ctx)
+        else:
+            L.ls_run(ctx, x, y, T, s, logits=logits, top_k=cfg.top_k)
     n_ev0 = len(L.ls_get_schedule(ctx))
 
-    def timed_passes():
+    def timed_passes(graph=False):
         ev = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True))
               for _ in range(args.steps)]
         if world > 1:
@@ -278,7 +282,10 @@ def run_ours(args, cfg, world, rank, local):
         for i in range(args.steps):
             flush.zero_()                    # write 256 MB (> 129 MB L2) between timed passes
             ev[i][0].record(s)
-            L.ls_run_async(ctx, x, y, T, s, logits=logits, top_k=cfg.top_k)
+            if graph:
+                L.ls_run_graph(ctx, x, y, T, s)
+            else:
+                L.ls_run_async(ctx, x, y, T, s, logits=logits, top_k=cfg.top_k)
             ev[i][1].record(s)
         L.ls_sync(ctx)
         torch.cuda.synchronize()
@@ -287,7 +294,7 @@ def run_ours(args, cfg, world, rank, local):
         return [a.elapsed_time(b) for a, b in ev]
 
     # throughput: passes as a user runs them (no per-launch events in the stream)
-    step_ms = timed_passes()
+    step_ms = timed_passes(graph=args.graph)
     sched = L.ls_get_schedule(ctx)[n_ev0:]
     # kernel times: the same K passes again with every launch bracketed by events
     L.ls_set_kernel_timing(ctx, 1)
@@ -361,6 +368,7 @@ def run_ours(args, cfg, world, rank, local):
                             "warnings": stats["warnings"]},
                    "parallelism": f"replicas{world}" if world > 1 else "single",
                    "cross_run_prefetch": bool(args.cross_run),
+                   "cuda_graph": bool(args.graph),
                    "l2": "flushed between timed passes (256 MB write)"},
         "overlap_eff": max(link_bytes / (link_peak * 1e9), flops / (tc_peak * 1e12)) / mean_s,
         "link_gbs": link_bytes / mean_s / 1e9, "link_peak_gbs": link_peak,
@@ -416,6 +424,8 @@ def main() -> int:
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--prefetch-depth", type=int, default=None,
                     help="override the workload's prefetch depth (the planner re-derives residents)")
+    ap.add_argument("--graph", action="store_true",
+                    help="issue the timed passes as replays of a captured CUDA graph (ls_run_graph)")
     ap.add_argument("--cross-run", action="store_true",
                     help="let the prefetch window cross the pass boundary (off by default, as in the pages)")
     ap.add_argument("--max-vram-bytes", type=int, default=None,
@@ -429,6 +439,8 @@ def main() -> int:
         cfg = cfg.with_(prefetch_depth=args.prefetch_depth)
     if args.max_vram_bytes is not None:
         cfg = cfg.with_(max_vram_bytes=args.max_vram_bytes)
+    if args.graph and (cfg.kind == synth.KIND_MOE_SWIGLU_BF16 or args.cross_run):
+        ap.error("--graph needs a kind without per-pass routing and no --cross-run")
     if args.impl == "reference":
         return run_reference(args, cfg, world, rank)
     return run_ours(args, cfg, world, rank, local)

@@ -85,10 +85,12 @@ __global__ void publish_kernel(uint32_t* ready, uint32_t epoch, int publish) {
 }
 
 __global__ void wait_ready_kernel(const uint32_t* ready, uint32_t epoch, uint64_t limit_ns,
-                                  uint32_t* err_word, uint32_t code) {
-    // the GEMM behind this wait may be placed now: it reads the weights only after
-    // this kernel has completed (its grid-dependency wait), never before
-    asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
+                                  uint32_t* err_word, uint32_t code, int early_dependents) {
+    // The GEMM behind this wait may be placed now (it reads the weights only after
+    // this kernel has completed) - but only when the copy this waits for needs no SM:
+    // placed GEMM CTAs fill every SM, and a copy or publish kernel could then never
+    // run, so the wait would run out instead of ending.
+    if (early_dependents) asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
     if (threadIdx.x != 0) return;
     if (*(volatile uint32_t*)err_word) return;
     if (ld_acquire_gpu(ready) == epoch) return;
@@ -127,7 +129,8 @@ cudaError_t launch_copy_h2slot(const CopyRange* ranges_dev, int n_ranges, int64_
 // operation: it runs in stream order after the copy, behind a memory barrier,
 // and needs no SM, so it is not held up by GEMM CTAs that fill every SM (a
 // publish kernel was, and the next copy queued behind it). If the driver does
-// not offer stream memory operations, a one-thread kernel publishes instead.
+// not offer stream memory operations, or the stream is being captured into a
+// graph (stream_op false), a one-thread kernel publishes instead.
 typedef CUresult (*WriteValueFn)(CUstream, CUdeviceptr, cuuint32_t, unsigned int);
 
 static WriteValueFn write_value_fn() {
@@ -144,10 +147,20 @@ static WriteValueFn write_value_fn() {
     return fn;
 }
 
-cudaError_t launch_publish(uint32_t* ready, uint32_t epoch, bool publish, cudaStream_t s) {
+static bool use_mem_op = true;
+
+bool publish_needs_no_sm() { return use_mem_op && write_value_fn() != nullptr; }
+
+cudaError_t launch_publish(uint32_t* ready, uint32_t epoch, bool publish, cudaStream_t s, bool stream_op,
+                           bool capturing) {
     if (!publish) return cudaSuccess;  // the drop hook: the word stays down
-    static bool use_mem_op = true;
-    if (use_mem_op) {
+    if (capturing && stream_op) {     // a graph node; a refusal fails the capture, which is retried
+        WriteValueFn fn = write_value_fn();
+        if (fn && fn((CUstream)s, (CUdeviceptr)ready, epoch, CU_STREAM_WRITE_VALUE_DEFAULT) == CUDA_SUCCESS)
+            return cudaSuccess;
+        return cudaErrorStreamCaptureUnsupported;
+    }
+    if (use_mem_op && stream_op) {
         WriteValueFn fn = write_value_fn();
         if (fn && fn((CUstream)s, (CUdeviceptr)ready, epoch, CU_STREAM_WRITE_VALUE_DEFAULT) == CUDA_SUCCESS)
             return cudaSuccess;
@@ -158,8 +171,8 @@ cudaError_t launch_publish(uint32_t* ready, uint32_t epoch, bool publish, cudaSt
 }
 
 cudaError_t launch_wait_ready(const uint32_t* ready, uint32_t epoch, uint64_t limit_ns,
-                              uint32_t* err_word, uint32_t code, cudaStream_t s) {
-    wait_ready_kernel<<<1, 32, 0, s>>>(ready, epoch, limit_ns, err_word, code);
+                              uint32_t* err_word, uint32_t code, cudaStream_t s, bool early_dependents) {
+    wait_ready_kernel<<<1, 32, 0, s>>>(ready, epoch, limit_ns, err_word, code, early_dependents ? 1 : 0);
     return cudaGetLastError();
 }
 

@@ -19,9 +19,14 @@ cudaError_t launch_copy_h2slot(const CopyRange* ranges_dev, int n_ranges, int64_
                                void* dst_base, const uint8_t* group_mask_dev, int ranges_per_group, uint32_t* ready,
                                uint32_t* ticket, uint32_t epoch, bool publish, int ctas,
                                cudaStream_t s);
-cudaError_t launch_publish(uint32_t* ready, uint32_t epoch, bool publish, cudaStream_t s);
+cudaError_t launch_publish(uint32_t* ready, uint32_t epoch, bool publish, cudaStream_t s,
+                           bool stream_op = true, bool capturing = false);
+// early_dependents: let the next kernel be placed while this one waits - only when the
+// awaited copy needs no SM (copy engine + stream-operation publish).
 cudaError_t launch_wait_ready(const uint32_t* ready, uint32_t epoch, uint64_t limit_ns,
-                              uint32_t* err_word, uint32_t code, cudaStream_t s);
+                              uint32_t* err_word, uint32_t code, cudaStream_t s, bool early_dependents = false);
+// True when a publish after a copy-engine load is a stream memory operation (no SM).
+bool publish_needs_no_sm();
 
 // ---------------------------------------------------------------- fp32 linear + GELU
 cudaError_t launch_linear_gelu_f32(const float* x, const float* w, const float* b, float* y, int T,

@@ -78,6 +78,14 @@ public:
     bool usable() const { return usable_; }
     const Plan& plan() const { return plan_; }
     const std::vector<ls_sched_event>& log() const { return log_; }
+    // A copy of the scheduler state without the event log (to predict a run cheaply).
+    Scheduler without_log() {
+        std::vector<ls_sched_event> keep;
+        keep.swap(log_);
+        Scheduler copy = *this;
+        log_.swap(keep);
+        return copy;
+    }
     void fill_stats(ls_stats& s) const;
     int residents() const { return R_; }
     int depth() const { return d_; }

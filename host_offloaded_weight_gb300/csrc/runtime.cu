@@ -140,6 +140,18 @@ struct ls_ctx {
     size_t tev_used = 0;
     int cur_seg = -1;
     std::vector<ls_trace_event> trace;
+    // graph replay of a steady-state pass (ls_run_graph)
+    bool capturing = false;               // issuing into a stream capture
+    bool capture_stream_ops = true;       // publish inside a capture as a stream memory operation
+    cudaStream_t graph_stream = nullptr;
+    cudaGraph_t graph = nullptr;
+    cudaGraphExec_t graph_exec = nullptr;
+    cudaEvent_t graph_in = nullptr, graph_out = nullptr, graph_fork = nullptr, graph_join = nullptr;
+    const void* graph_x = nullptr;
+    void* graph_y = nullptr;
+    int64_t graph_T = 0;
+    std::vector<ls_sched_event> graph_events;  // the captured pass's schedule (run field 0)
+    int64_t graph_captures = 0, graph_replays = 0;
 };
 
 namespace {
@@ -296,7 +308,8 @@ void issue_copy(ls_ctx* c, int seg, void* dst, int slot, uint32_t epoch, cudaStr
         }
     }
     flush();
-    track(c, launch_publish(c->ready + slot, epoch, publish, s));
+    track(c, launch_publish(c->ready + slot, epoch, publish, s, !c->capturing || c->capture_stream_ops,
+                            c->capturing));
 }
 
 // --------------------------------------------------------------------------- compute
@@ -343,7 +356,11 @@ void compute_segment(ls_ctx* c, const RunCtx& rc, int seg, bool wait) {
     // nothing, so the copy it waits for can always find SMs to run on.
     auto wait_slot = [&]() {
         KTime kt(c, "wait_ready", rc.s);
-        track(c, launch_wait_ready(c->ready + slot, epoch, rc.wait_ns, c->err_word_dev, code, rc.s));
+        // the GEMM behind it may be placed early only if its copy needs no SM (no copy or
+        // publish kernel that the placed CTAs could starve)
+        const bool early = c->copy_path == LS_COPY_ENGINE && publish_needs_no_sm() &&
+                           (!c->capturing || c->capture_stream_ops);
+        track(c, launch_wait_ready(c->ready + slot, epoch, rc.wait_ns, c->err_word_dev, code, rc.s, early));
     };
     GemmDesc w0;
     w0.err_word = c->err_word_dev;
@@ -1054,9 +1071,19 @@ static ls_status register_impl(ls_ctx* c, const ls_segment_desc* segs, int32_t n
     return plan_st;
 }
 
-ls_status ls_run_async(ls_ctx* c, const void* x_dev, void* y_dev, int64_t tokens, void* stream,
-                       const ls_moe_routing* routing) {
-    if (!c) return LS_ERR_INVALID_ARG;
+static void destroy_graph(ls_ctx* c) {
+    if (c->graph_exec) cudaGraphExecDestroy(c->graph_exec);
+    if (c->graph) cudaGraphDestroy(c->graph);
+    c->graph_exec = nullptr;
+    c->graph = nullptr;
+    c->graph_events.clear();
+    cudaGetLastError();
+}
+
+// Checks, workspaces and (MoE) routing of one pass on the caller's stream; fills the
+// bytes each load will move. The pass itself is issued by the caller of this.
+static ls_status prepare_pass(ls_ctx* c, const void* x_dev, void* y_dev, int64_t tokens, cudaStream_t s,
+                              const ls_moe_routing* routing, std::vector<int64_t>& load_bytes) {
     if (!c->registered) {
         set_err(c, "ls_run before ls_register_segments");
         return LS_ERR_STATE;
@@ -1076,16 +1103,16 @@ ls_status ls_run_async(ls_ctx* c, const void* x_dev, void* y_dev, int64_t tokens
         return LS_ERR_INVALID_ARG;
     }
     CK(cudaSetDevice(c->device));
-    cudaStream_t s = (cudaStream_t)stream;
     if (tokens > c->ws_tokens) {
         ls_status sy = ls_sync(c);  // workspaces are about to be replaced
         if (sy < 0) return sy;
+        destroy_graph(c);           // a captured pass points at the old ones
     }
     ls_status st = ensure_workspace(c, tokens);
     if (st != LS_OK) return st;
     if (std::find(c->pending.begin(), c->pending.end(), s) == c->pending.end()) c->pending.push_back(s);
     CK(cudaStreamWaitEvent(s, c->run_done, 0));  // passes share workspaces: keep them in order
-    std::vector<int64_t> load_bytes(c->N);
+    load_bytes.assign(c->N, 0);
     for (int i = 0; i < c->N; ++i) load_bytes[i] = c->segs[i].load_bytes;
     if (moe) {
         c->top_k = routing->top_k;
@@ -1104,12 +1131,144 @@ ls_status ls_run_async(ls_ctx* c, const void* x_dev, void* y_dev, int64_t tokens
             load_bytes[l] = used * eb;
         }
     }
+    return LS_OK;
+}
+
+ls_status ls_run_async(ls_ctx* c, const void* x_dev, void* y_dev, int64_t tokens, void* stream,
+                       const ls_moe_routing* routing) {
+    if (!c) return LS_ERR_INVALID_ARG;
+    cudaStream_t s = (cudaStream_t)stream;
+    std::vector<int64_t> load_bytes;
+    ls_status pst = prepare_pass(c, x_dev, y_dev, tokens, s, routing, load_bytes);
+    if (pst != LS_OK) return pst;
     GpuExec ex(c);
     ex.rc = RunCtx{x_dev, y_dev, tokens, s, (uint64_t)c->prm.wait_limit_ms * 1000000ull};
     ls_status rs = c->sched.run(ex, load_bytes.data());
     track(c, cudaEventRecord(c->run_done, s));
     if (rs < 0) set_err(c, "run %d: %s", c->sched.runs() - 1, ls_status_string(rs));
     return rs;
+}
+
+static bool same_events(const std::vector<ls_sched_event>& a, const std::vector<ls_sched_event>& b) {
+    if (a.size() != b.size()) return false;
+    for (size_t i = 0; i < a.size(); ++i)
+        if (a[i].step != b[i].step || a[i].kind != b[i].kind || a[i].segment != b[i].segment ||
+            a[i].slot != b[i].slot || a[i].bytes != b[i].bytes)
+            return false;
+    return true;
+}
+
+ls_status ls_run_graph(ls_ctx* c, const void* x_dev, void* y_dev, int64_t tokens, void* stream) {
+    if (!c) return LS_ERR_INVALID_ARG;
+    if (c->registered && (c->kind == LS_KIND_MOE_SWIGLU_BF16 || !c->prm.use_pool || c->prm.cross_run_prefetch)) {
+        set_err(c, "ls_run_graph needs the pool, no cross-run window and a kind without per-pass routing");
+        return LS_ERR_UNSUPPORTED;
+    }
+    cudaStream_t s = (cudaStream_t)stream;
+    std::vector<int64_t> lb;
+    ls_status pst = prepare_pass(c, x_dev, y_dev, tokens, s, nullptr, lb);
+    if (pst != LS_OK) return pst;
+    // the schedule this pass will follow, from a copy of the scheduler
+    Scheduler probe = c->sched.without_log();
+    DryExec dex;
+    const ls_status prs = probe.run(dex, lb.data());
+    std::vector<ls_sched_event> ev(probe.log().begin(), probe.log().end());
+    bool steady = prs == LS_OK;
+    for (auto& e : ev) {
+        e.run = 0;
+        steady = steady && (e.kind == LS_EV_PREFETCH || e.kind == LS_EV_LOAD_SYNC || e.kind == LS_EV_ACTIVATE);
+    }
+    if (!steady) {  // shared or resident loads, evictions, a fallback: an ordinary pass
+        GpuExec ex(c);
+        ex.rc = RunCtx{x_dev, y_dev, tokens, s, (uint64_t)c->prm.wait_limit_ms * 1000000ull};
+        ls_status rs = c->sched.run(ex, lb.data());
+        track(c, cudaEventRecord(c->run_done, s));
+        if (rs < 0) set_err(c, "run %d: %s", c->sched.runs() - 1, ls_status_string(rs));
+        return rs;
+    }
+    if (!c->graph_stream) {
+        CK(cudaStreamCreateWithFlags(&c->graph_stream, cudaStreamNonBlocking));
+        for (cudaEvent_t* e : {&c->graph_in, &c->graph_out, &c->graph_fork, &c->graph_join})
+            CK(cudaEventCreateWithFlags(e, cudaEventDisableTiming));
+    }
+    if (std::find(c->pending.begin(), c->pending.end(), c->graph_stream) == c->pending.end())
+        c->pending.push_back(c->graph_stream);
+    CK(cudaEventRecord(c->graph_in, s));
+    CK(cudaStreamWaitEvent(c->graph_stream, c->graph_in, 0));
+    const bool reuse = c->graph_exec && c->graph_x == x_dev && c->graph_y == y_dev && c->graph_T == tokens &&
+                       same_events(ev, c->graph_events);
+    if (reuse) {
+        c->sched.run(dex, lb.data());  // the log and counters advance as for an issued pass
+        ++c->graph_replays;
+    } else {
+        destroy_graph(c);
+        // what a capture advances without running anything: restored if it has to be redone
+        const Scheduler saved_sched = c->sched;
+        const auto saved_slot_epoch = c->slot_epoch;
+        const auto saved_seg_epoch = c->seg_epoch;
+        const auto saved_seg_ptr = c->seg_ptr;
+        const auto saved_seg_slot = c->seg_slot;
+        const auto saved_publishes = c->publishes;
+        const int saved_timing = c->prm.kernel_timing;
+        cudaError_t e = cudaSuccess;
+        ls_status rs = LS_OK;
+        for (int attempt = 0; attempt < 2; ++attempt) {
+            c->prm.kernel_timing = 0;
+            c->capturing = true;
+            cudaStream_t gs = c->graph_stream;
+            rs = LS_OK;
+            e = cudaStreamBeginCapture(gs, cudaStreamCaptureModeThreadLocal);
+            if (e == cudaSuccess) {
+                // ready words restart at every replay: the pass's epochs are fixed in the graph
+                track(c, cudaMemsetAsync(c->ready, 0, sizeof(uint32_t) * std::max(1, c->N), gs));
+                track(c, cudaEventRecord(c->graph_fork, gs));
+                track(c, cudaStreamWaitEvent(c->copy_stream, c->graph_fork, 0));  // the copy stream joins
+                for (cudaEvent_t f : c->slot_free) track(c, cudaEventRecord(f, gs));
+                GpuExec ex(c);
+                ex.rc = RunCtx{x_dev, y_dev, tokens, gs, (uint64_t)c->prm.wait_limit_ms * 1000000ull};
+                rs = c->sched.run(ex, lb.data());
+                track(c, cudaEventRecord(c->graph_join, c->copy_stream));
+                track(c, cudaStreamWaitEvent(gs, c->graph_join, 0));
+                cudaGraph_t g = nullptr;
+                e = cudaStreamEndCapture(gs, &g);
+                c->graph = g;
+            }
+            c->capturing = false;
+            c->prm.kernel_timing = saved_timing;
+            if (e == cudaSuccess && c->cuda_err == cudaSuccess)
+                e = cudaGraphInstantiate(&c->graph_exec, c->graph, 0);
+            if (e == cudaSuccess && c->cuda_err == cudaSuccess && rs == LS_OK) break;
+            // failed: nothing ran; put the bookkeeping back as before the capture
+            if (e == cudaSuccess) e = c->cuda_err;
+            c->cuda_err = cudaSuccess;
+            cudaGetLastError();
+            destroy_graph(c);
+            c->sched = saved_sched;
+            c->slot_epoch = saved_slot_epoch;
+            c->seg_epoch = saved_seg_epoch;
+            c->seg_ptr = saved_seg_ptr;
+            c->seg_slot = saved_seg_slot;
+            c->publishes = saved_publishes;
+            if (attempt == 0 && c->capture_stream_ops) {
+                c->capture_stream_ops = false;  // the driver refused the memory operation in a graph
+                continue;
+            }
+            set_err(c, "run %d: graph capture failed: %s", c->sched.runs(), cudaGetErrorString(e));
+            return LS_ERR_CUDA;
+        }
+        c->graph_x = x_dev;
+        c->graph_y = y_dev;
+        c->graph_T = tokens;
+        c->graph_events = ev;
+        ++c->graph_captures;
+    }
+    CK(cudaGraphLaunch(c->graph_exec, c->graph_stream));
+    CK(cudaEventRecord(c->graph_out, c->graph_stream));
+    CK(cudaStreamWaitEvent(s, c->graph_out, 0));
+    // slot events were last recorded inside the capture: record them again in plain stream order
+    for (cudaEvent_t f : c->slot_free) track(c, cudaEventRecord(f, s));
+    track(c, cudaEventRecord(c->run_done, s));
+    return LS_OK;
 }
 
 ls_status ls_sync(ls_ctx* c) {
@@ -1164,6 +1323,7 @@ ls_status ls_replan(ls_ctx* c, int32_t prefetch_depth, int32_t resident_layers, 
     CK(cudaStreamSynchronize(c->copy_stream));
     GpuExec ex(c);
     ex.rc = RunCtx{nullptr, nullptr, 0, c->copy_stream, 0};
+    destroy_graph(c);
     const ls_status st = c->sched.replan(ex, prefetch_depth, resident_layers, max_vram_bytes);
     CK(cudaStreamSynchronize(c->copy_stream));  // releases and the new pool are in place
     if (c->cuda_err != cudaSuccess) {
@@ -1252,6 +1412,8 @@ ls_status ls_get_stats(ls_ctx* c, ls_stats* out) {
     s.copy_path = c->copy_path;
     s.copy_kernel_gbs = c->gbs_kernel;
     s.copy_engine_gbs = c->gbs_engine;
+    s.graph_captures = c->graph_captures;
+    s.graph_replays = c->graph_replays;
     const uint32_t n = std::min<uint32_t>(out->struct_size, sizeof(s));
     memcpy(out, &s, n);
     out->struct_size = n;
@@ -1321,6 +1483,10 @@ static void release_resources(ls_ctx* c) {
         if (c->run_done) cudaEventDestroy(c->run_done);
         if (c->copy_stream) cudaStreamDestroy(c->copy_stream);
         if (c->own_stream) cudaStreamDestroy(c->own_stream);
+        destroy_graph(c);
+        for (cudaEvent_t e : {c->graph_in, c->graph_out, c->graph_fork, c->graph_join})
+            if (e) cudaEventDestroy(e);
+        if (c->graph_stream) cudaStreamDestroy(c->graph_stream);
         for (auto& r : c->host_registered) cudaHostUnregister(r.first);
         cudaGetLastError();
     }

@@ -90,7 +90,8 @@ class ls_stats(C.Structure):
                 ("shared_loads", C.c_int64), ("evictions", C.c_int64),
                 ("sync_fallbacks", C.c_int64), ("pool_degradations", C.c_int64),
                 ("bytes_loaded", C.c_int64), ("copy_kernel_gbs", C.c_double),
-                ("copy_engine_gbs", C.c_double)]
+                ("copy_engine_gbs", C.c_double), ("graph_captures", C.c_int64),
+                ("graph_replays", C.c_int64)]
 
 
 _P = C.c_void_p
@@ -107,6 +108,7 @@ _sig = {
     "ls_get_stats": (_I32, [_P, C.POINTER(ls_stats)]),
     "ls_set_kernel_timing": (_I32, [_P, _I32]),
     "ls_replan": (_I32, [_P, _I32, _I32, _I64]),
+    "ls_run_graph": (_I32, [_P, _P, _P, _I64, _P]),
     "ls_simulate_script": (_I32, [C.POINTER(ls_params), C.POINTER(_I64), _I32, C.POINTER(_I64),
                                   C.POINTER(_I32), _I32, C.POINTER(_I64), _I32, C.POINTER(ls_sched_event),
                                   _I64, C.POINTER(_I64), C.POINTER(ls_stats), C.POINTER(_I32)]),
@@ -301,6 +303,11 @@ def ls_get_stats(ctx: Ctx) -> dict:
     s.struct_size = C.sizeof(ls_stats)
     _check(_lib.ls_get_stats(ctx.handle, C.byref(s)), ctx)
     return _stats_dict(s)
+
+
+def ls_run_graph(ctx: Ctx, x, y, tokens: int, stream=None) -> int:
+    """One pass issued as a CUDA graph replay once the pass is steady (see include/ls_api.h)."""
+    return _check(_lib.ls_run_graph(ctx.handle, _ptr(x), _ptr(y), tokens, _stream(stream)), ctx)
 
 
 def ls_replan(ctx: Ctx, prefetch_depth: int, resident_layers: int, max_vram_bytes: int) -> int:

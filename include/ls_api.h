@@ -195,6 +195,8 @@ typedef struct ls_stats {
     int64_t bytes_loaded;
     double copy_kernel_gbs;    /* registration-time timing of both copy paths (0 if not timed) */
     double copy_engine_gbs;
+    int64_t graph_captures;    /* passes captured into a CUDA graph by ls_run_graph */
+    int64_t graph_replays;     /* passes issued as a replay of the captured graph */
 } ls_stats;
 
 /* Per-kernel timing, accumulated over runs while params.kernel_timing is on.
@@ -276,6 +278,22 @@ ls_status ls_get_stats(ls_ctx* ctx, ls_stats* out);
  * by ls_run_async have not been collected by ls_sync; LS_ERR_INVALID_ARG for a
  * mode outside 0..2. The pages define no such call: it is instrumentation. */
 ls_status ls_set_kernel_timing(ls_ctx* ctx, int32_t mode);
+
+/* One pass, like ls_run_async, issued as a CUDA graph: the first steady-state
+ * pass (no shared, resident or synchronous-fallback work left) is captured with
+ * its copy and compute streams, and later passes replay it while x_dev, y_dev,
+ * tokens and the pass's schedule stay the same (a change re-captures). This
+ * removes the host's per-launch cost, which dominates passes of small stacks
+ * ("layer split: overlap the stages' hand-off", Summary: host launch and sync on
+ * the critical path). The graph sets the slots' ready words to 0 at its start,
+ * then raises them with the epochs fixed at capture. Passes that are not steady
+ * (the first runs, after a plan change) run as ordinary passes.
+ * The schedule log and counters advance as for ls_run_async. LS_ERR_UNSUPPORTED
+ * for the MoE kind (routing is read back on the host every pass), with the pool
+ * off, or with cross_run_prefetch; other errors as for ls_run_async. The graph is
+ * dropped at ls_replan, at ls_ctx_destroy and when a larger token count replaces
+ * the workspaces. Complete with ls_sync. */
+ls_status ls_run_graph(ls_ctx* ctx, const void* x_dev, void* y_dev, int64_t tokens, void* stream);
 
 /* New streaming controls between runs ("feat: prefetch streamed layers during
  * compute", Summary: residents are evicted from the end of the prefix under

@@ -122,6 +122,32 @@ def test_dit_stack_full_size():
     assert np.array_equal(_bits(y0), _bits(y1))
 
 
+@pytest.mark.parametrize("copy_path,graph", [(1, False), (1, True), (2, True)])
+def test_dit_stack_full_size_other_issue_paths(copy_path, graph):
+    """The full DiT stack, whose GEMMs fill every SM, with the copy kernel and with graph
+    passes (where the ready word is raised by a publish kernel). The GEMM behind a hand-off
+    wait must not be placed early there: its CTAs would leave the copy or publish kernel no
+    SM and the wait would run out. Same bits as the copy engine's ordinary passes."""
+    cfg = synth.DIT
+    hs = synth.HostStack(cfg)
+    ref, *_ = _run(cfg, hs, runs=1, copy_path=2)
+    ctx, _ = make_ctx(cfg, hs, copy_path=copy_path)
+    try:
+        x = x_dev(cfg)
+        y = torch.empty_like(x)
+        for _ in range(4):
+            if graph:
+                L.ls_run_graph(ctx, x, y, cfg.tokens)
+            else:
+                L.ls_run_async(ctx, x, y, cfg.tokens)
+        L.ls_sync(ctx)
+        assert np.array_equal(_bits(y), _bits(ref))
+        if graph:
+            assert L.ls_get_stats(ctx)["graph_replays"] == 3
+    finally:
+        L.ls_ctx_destroy(ctx)
+
+
 def test_shared_projection_stack_full_size():
     cfg = synth.SHARED
     hs = synth.HostStack(cfg)
@@ -406,6 +432,84 @@ def test_replan_refused_while_passes_are_queued():
             L.ls_replan(ctx, -1, -1, 2 * S)
         assert e.value.status == L.LS_ERR_INVALID_ARG
         assert L.ls_replan(ctx, 1, -1, 2 * S) == L.LS_OK
+    finally:
+        L.ls_ctx_destroy(ctx)
+
+
+# ------------------------------------------------------------------ CUDA-graph passes (NEXT-3)
+GRAPH_CASES = {"tiny": synth.TINY, "ffn": SMALL["ffn"], "proj": SMALL["proj"], "swiglu": SMALL["swiglu"]}
+
+
+@pytest.mark.parametrize("name", sorted(GRAPH_CASES))
+@pytest.mark.parametrize("copy_path", [2, 1])
+def test_graph_passes_keep_bits_and_schedule(name, copy_path):
+    """Passes issued through ls_run_graph: the first steady pass is captured, the rest are
+    replays; every output equals an ordinary pass's bit for bit and the schedule log is the
+    simulator's, run for run."""
+    cfg = GRAPH_CASES[name]
+    hs = synth.HostStack(cfg)
+    ref, _, _, _, _ = _run(cfg, hs, runs=1)
+    runs = 6
+    ctx, _ = make_ctx(cfg, hs, copy_path=copy_path)
+    try:
+        x = x_dev(cfg)
+        ys = [torch.empty_like(x) for _ in range(runs)]
+        y = torch.empty_like(x)
+        for i in range(runs):
+            L.ls_run_graph(ctx, x, y, cfg.tokens)
+            ys[i].copy_(y)
+        L.ls_sync(ctx)
+        for yi in ys:
+            assert torch.equal(_bits_t(yi), _bits_t(ref))
+        sim, _ = _sim_events(cfg, hs, cfg.prefetch_depth, cfg.resident_layers, cfg.max_vram_bytes,
+                             cfg.use_pool, runs)
+        assert L.ls_get_schedule(ctx) == [tuple(e) for e in sim.events]
+        st = L.ls_get_stats(ctx)
+        first = 1 if (hs.shared_views or sim.plan.R > 0) else 0   # run 0 loads shared/residents
+        assert st["graph_captures"] == 1 and st["graph_replays"] == runs - first - 1
+    finally:
+        L.ls_ctx_destroy(ctx)
+
+
+def _bits_t(t):
+    return t.view(torch.int16) if t.dtype == torch.bfloat16 else t.view(torch.int32)
+
+
+def test_graph_recaptured_after_changes():
+    cfg = SMALL["ffn"]
+    hs = synth.HostStack(cfg)
+    S = synth.segment_slot_bytes(cfg)
+    ref, _, _, _, _ = _run(cfg, hs, runs=1)
+    ctx, _ = make_ctx(cfg, hs)
+    try:
+        x = x_dev(cfg)
+        y1, y2 = torch.empty_like(x), torch.empty_like(x)
+        for y in (y1, y1, y2, y2):          # a new output buffer: captured again
+            L.ls_run_graph(ctx, x, y, cfg.tokens)
+        L.ls_sync(ctx)
+        assert L.ls_get_stats(ctx)["graph_captures"] == 2
+        L.ls_replan(ctx, 1, -1, 3 * S)      # the plan changes: the graph is dropped
+        for _ in range(3):
+            L.ls_run_graph(ctx, x, y1, cfg.tokens)
+        L.ls_sync(ctx)
+        st = L.ls_get_stats(ctx)
+        assert st["graph_captures"] == 3
+        assert torch.equal(_bits_t(y1), _bits_t(ref)) and torch.equal(_bits_t(y2), _bits_t(ref))
+        L.ls_run(ctx, x, y2, cfg.tokens)    # an ordinary pass after replays
+        assert torch.equal(_bits_t(y2), _bits_t(ref))
+    finally:
+        L.ls_ctx_destroy(ctx)
+
+
+def test_graph_refused_for_moe():
+    cfg = _moe_cfg(2, 64, experts=8, hidden=256, ffn=128, k=2)
+    hs = synth.HostStack(cfg)
+    ctx, _ = make_ctx(cfg, hs)
+    try:
+        x = x_dev(cfg)
+        with pytest.raises(L.LsError) as e:
+            L.ls_run_graph(ctx, x, torch.empty_like(x), cfg.tokens)
+        assert e.value.status == L.LS_ERR_UNSUPPORTED
     finally:
         L.ls_ctx_destroy(ctx)
 
