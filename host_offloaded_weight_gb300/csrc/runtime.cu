@@ -293,7 +293,7 @@ void issue_copy(ls_ctx* c, int seg, void* dst, int slot, uint32_t epoch, cudaStr
     for (size_t i = 0; i < sr.t.size(); ++i) {
         const TensorRec& t = sr.t[i];
         if (t.shared_id >= 0) continue;
-        if (moe && c->moe_used_host && !c->moe_used_host[(int64_t)seg * c->E + i / 3]) {
+        if (moe && expert_mask && !c->moe_used_host[(int64_t)seg * c->E + i / 3]) {
             flush();
             continue;
         }
@@ -524,8 +524,11 @@ struct GpuExec : Executor {
         c->seg_epoch[seg] = epoch;
         c->seg_ptr[seg] = dst;
         c->seg_slot[seg] = slot;
-        const uint8_t* mask =
-            c->kind == LS_KIND_MOE_SWIGLU_BF16 ? c->moe_used + (int64_t)seg * c->E : nullptr;
+        // a streamed MoE load moves the experts routed in this pass; a resident keeps all of
+        // them, since later passes may route to any
+        const uint8_t* mask = c->kind == LS_KIND_MOE_SWIGLU_BF16 && kind != LS_EV_LOAD_RESIDENT
+                                  ? c->moe_used + (int64_t)seg * c->E
+                                  : nullptr;
         const bool kern = c->copy_path == LS_COPY_KERNEL;
         if (kind == LS_EV_PREFETCH) {
             track(c, cudaStreamWaitEvent(c->copy_stream, c->slot_free[slot], 0));
@@ -1125,7 +1128,8 @@ static ls_status prepare_pass(ls_ctx* c, const void* x_dev, void* y_dev, int64_t
         CK(cudaMemcpyAsync(c->moe_used_host, c->moe_used, (size_t)c->N * E, cudaMemcpyDeviceToHost, s));
         CK(cudaStreamSynchronize(s));
         const int64_t eb = c->segs[0].slot_bytes / E;
-        for (int l = 0; l < c->N; ++l) {
+        const int R = c->sched.residents();  // residents are loaded whole (see GpuExec::load)
+        for (int l = R; l < c->N; ++l) {
             int64_t used = 0;
             for (int e = 0; e < E; ++e) used += c->moe_used_host[(int64_t)l * E + e];
             load_bytes[l] = used * eb;

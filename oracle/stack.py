@@ -23,11 +23,13 @@ def shared_f64(cfg):
     return [F.as_f64(a, s.dtype) for a, s in zip(synth.draw_shared(cfg), synth.shared_tensors(cfg))]
 
 
-def apply_segment(cfg, seg: int, x: np.ndarray, rows=None, tensors=None, shared=None):
-    """y = segment_seg(x) for the given rows of the stack's token set."""
+def apply_segment(cfg, seg: int, x: np.ndarray, rows=None, tensors=None, shared=None, logits=None):
+    """y = segment_seg(x) for the given rows of the stack's token set. ``logits``: this
+    MoE layer's router logits for all tokens (default: the drawn ones)."""
     k = cfg.kind
     if k == synth.KIND_MOE_SWIGLU_BF16:
-        logits = synth.draw_logits(cfg, seg)
+        if logits is None:
+            logits = synth.draw_logits(cfg, seg)
         if rows is not None:
             logits = logits[rows]
         cache: dict = {}
@@ -52,10 +54,11 @@ def apply_segment(cfg, seg: int, x: np.ndarray, rows=None, tensors=None, shared=
     raise ValueError(k)
 
 
-def stack_forward(cfg, rows=None, x=None, n_segments=None):
+def stack_forward(cfg, rows=None, x=None, n_segments=None, logits=None):
     """fp64 output of the stack for token ``rows`` (all rows when None).
 
-    ``x`` overrides the drawn input (float64 [len(rows), hidden])."""
+    ``x`` overrides the drawn input (float64 [len(rows), hidden]); ``logits`` the MoE router
+    logits ([layers] of [tokens, experts])."""
     if x is None:
         xa = synth.draw_x(cfg)
         if rows is not None:
@@ -63,5 +66,6 @@ def stack_forward(cfg, rows=None, x=None, n_segments=None):
         x = F.as_f64(xa, cfg.dtype)
     shared = shared_f64(cfg)[0] if cfg.kind == synth.KIND_FFN_GELU_SHARED_BF16 else None
     for s in range(cfg.n_segments if n_segments is None else n_segments):
-        x = apply_segment(cfg, s, x, rows=rows, shared=shared)
+        x = apply_segment(cfg, s, x, rows=rows, shared=shared,
+                          logits=None if logits is None else logits[s])
     return x

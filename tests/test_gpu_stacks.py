@@ -542,6 +542,41 @@ def test_moe_small_all_rows():
     assert np.array_equal(_bits(y0), _bits(y))
 
 
+def test_moe_residents_follow_routing_changes():
+    """Resident MoE layers hold every expert: a later pass that routes to other experts
+    still matches the oracle (a resident loaded with only the first pass's routed experts
+    would not), and streamed layers move only their routed experts in each pass."""
+    cfg = _moe_cfg(4, 64, experts=8, hidden=256, ffn=128, k=2)
+    S = synth.segment_slot_bytes(cfg)
+    cfg = cfg.with_(max_vram_bytes=4 * S, resident_layers=2)
+    hs = synth.HostStack(cfg)
+    lg_a_dev, lg_a = logits_dev(cfg)
+    lg_b = -lg_a                          # a different top-k in every row
+    lg_b_dev = torch.from_numpy(lg_b).cuda()
+    ctx, _ = make_ctx(cfg, hs)
+    try:
+        x = x_dev(cfg)
+        ya, yb = torch.empty_like(x), torch.empty_like(x)
+        L.ls_run(ctx, x, ya, cfg.tokens, logits=lg_a_dev, top_k=cfg.top_k)
+        L.ls_run(ctx, x, yb, cfg.tokens, logits=lg_b_dev, top_k=cfg.top_k)
+        torch.cuda.synchronize()
+        assert L.ls_get_stats(ctx)["residents"] == 2
+        assert rel_err(to_f64(ya), ostack.stack_forward(cfg, logits=list(lg_a))) <= BOUND
+        assert rel_err(to_f64(yb), ostack.stack_forward(cfg, logits=list(lg_b))) <= BOUND
+        from oracle import forward as F
+        eb = S // cfg.n_experts
+        exact = sum(t.nbytes for t in synth.segment_tensors(cfg))
+        load = []
+        for lg in (lg_a, lg_b):
+            row = [exact if l < 2 else len(np.unique(F.route_topk(lg[l], cfg.top_k)[0])) * eb
+                   for l in range(cfg.n_segments)]
+            load.append(row)
+        sim, _ = _sim_events(cfg, hs, cfg.prefetch_depth, 2, cfg.max_vram_bytes, 1, 2, load=load)
+        assert L.ls_get_schedule(ctx) == [tuple(e) for e in sim.events]
+    finally:
+        L.ls_ctx_destroy(ctx)
+
+
 def test_moe_full_expert_shapes_sampled_rows():
     cfg = _moe_cfg(4, 2048)
     hs = synth.HostStack(cfg)
