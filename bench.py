@@ -249,7 +249,8 @@ def run_ours(args, cfg, world, rank, local):
                          max_vram_bytes=cfg.max_vram_bytes, use_pool=cfg.use_pool,
                          copy_path={"auto": 0, "kernel": 1, "engine": 2}[args.copy_path],
                          copy_ctas=args.copy_ctas, reserve_sms=args.reserve_sms, kernel_timing=0,
-                         cross_run_prefetch=int(args.cross_run))
+                         cross_run_prefetch=int(args.cross_run),
+                         expert_cache_bytes=int(args.expert_cache_gb * 2**30))
     ctx = L.ls_ctx_create(p)
     L.ls_register_segments(ctx, hs.segments, hs.shared_map)
     T = cfg.tokens
@@ -369,6 +370,7 @@ def run_ours(args, cfg, world, rank, local):
                    "parallelism": f"replicas{world}" if world > 1 else "single",
                    "cross_run_prefetch": bool(args.cross_run),
                    "cuda_graph": bool(args.graph),
+                   "expert_cache_bytes": int(args.expert_cache_gb * 2**30),
                    "l2": "flushed between timed passes (256 MB write)"},
         "overlap_eff": max(link_bytes / (link_peak * 1e9), flops / (tc_peak * 1e12)) / mean_s,
         "link_gbs": link_bytes / mean_s / 1e9, "link_peak_gbs": link_peak,
@@ -385,6 +387,8 @@ def run_ours(args, cfg, world, rank, local):
         "clocks": {k: clocks[k] for k in ("sm_mhz", "sm_max_mhz", "reasons")},
         "e2e": {"value": e2e_tokens / e2e_max, "unit": UNIT, "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h},
         "copy_paths_gbs": {"kernel": stats["copy_kernel_gbs"], "engine": stats["copy_engine_gbs"]},
+        "expert_cache": {"hits": stats["expert_cache_hits"], "host_loads": stats["expert_host_loads"]}
+        if cfg.kind == synth.KIND_MOE_SWIGLU_BF16 else None,
     }
     L.ls_ctx_destroy(ctx)
     del hs
@@ -424,6 +428,8 @@ def main() -> int:
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--prefetch-depth", type=int, default=None,
                     help="override the workload's prefetch depth (the planner re-derives residents)")
+    ap.add_argument("--expert-cache-gb", type=float, default=0.0,
+                    help="MoE: device memory (GiB) for hot experts of streamed layers, beyond the budget")
     ap.add_argument("--graph", action="store_true",
                     help="issue the timed passes as replays of a captured CUDA graph (ls_run_graph)")
     ap.add_argument("--cross-run", action="store_true",

@@ -16,6 +16,7 @@
 #include <cuda_runtime.h>
 
 #include <algorithm>
+#include <tuple>
 #include <cstdarg>
 #include <cstdio>
 #include <cstring>
@@ -117,7 +118,17 @@ struct ls_ctx {
     int* moe_table = nullptr;
     int* moe_bounds = nullptr;
     uint8_t* moe_used = nullptr;
-    uint8_t* moe_used_host = nullptr;
+    uint8_t* moe_used_host = nullptr;      // mapped: routed experts, then the ones to copy from the host
+    uint8_t* moe_used_host_dev = nullptr;  // its device address (the copy kernel's expert mask)
+    // expert cache of streamed MoE layers
+    void* ecache = nullptr;
+    int ecache_K = 0;
+    int64_t ecache_eb = 0;                 // bytes of one expert blob (G, U, D)
+    std::vector<int64_t> ecache_counts;    // [N * E] earlier passes in which the pair was routed
+    std::vector<int> ecache_slot;          // [N * E] cache slot of a hot pair, else -1
+    std::vector<char> ecache_filled;       // [N * E] its blob is in the cache
+    std::vector<std::vector<std::pair<int, int>>> ecache_hits, ecache_fills;  // per layer, this pass
+    int64_t n_ecache_hits = 0, n_ecache_host = 0;
     void* moe_xs = nullptr;
     void* moe_hs = nullptr;
     float* moe_y = nullptr;
@@ -273,11 +284,24 @@ void issue_copy(ls_ctx* c, int seg, void* dst, int slot, uint32_t epoch, cudaStr
                 const uint8_t* expert_mask) {
     SegRec& sr = c->segs[seg];
     const bool publish = !(c->prm.test_drop_publish > 0 && ++c->publishes == c->prm.test_drop_publish);
+    // expert cache: hits are copied in device memory ahead of the host copy and its publish;
+    // hot experts that come from the host this time are copied into the cache afterwards
+    const bool cached = c->ecache_K > 0 && expert_mask;
+    auto cache_copies = [&](const std::vector<std::pair<int, int>>& list, bool into_slot) {
+        for (auto& h : list) {
+            uint8_t* sl = (uint8_t*)dst + (int64_t)h.first * c->ecache_eb;
+            uint8_t* ca = (uint8_t*)c->ecache + (int64_t)h.second * c->ecache_eb;
+            track(c, cudaMemcpyAsync(into_slot ? sl : ca, into_slot ? ca : sl, (size_t)c->ecache_eb,
+                                     cudaMemcpyDeviceToDevice, s));
+        }
+    };
+    if (cached) cache_copies(c->ecache_hits[seg], true);
     if (use_kernel && sr.kernel_ok) {
         KTime kt(c, "copy_h2slot", s);
         track(c, launch_copy_h2slot(sr.ranges_dev, sr.n_ranges, sr.n_chunks, dst, expert_mask,
                                     expert_mask ? 3 : 1, c->ready + slot, c->tickets + slot, epoch,
                                     publish, c->copy_ctas, s));
+        if (cached) cache_copies(c->ecache_fills[seg], false);
         return;
     }
     // copy engine: one copy per tensor (contiguous neighbours merged), then publish
@@ -310,6 +334,7 @@ void issue_copy(ls_ctx* c, int seg, void* dst, int slot, uint32_t epoch, cudaStr
     flush();
     track(c, launch_publish(c->ready + slot, epoch, publish, s, !c->capturing || c->capture_stream_ops,
                             c->capturing));
+    if (cached) cache_copies(c->ecache_fills[seg], false);
 }
 
 // --------------------------------------------------------------------------- compute
@@ -356,10 +381,11 @@ void compute_segment(ls_ctx* c, const RunCtx& rc, int seg, bool wait) {
     // nothing, so the copy it waits for can always find SMs to run on.
     auto wait_slot = [&]() {
         KTime kt(c, "wait_ready", rc.s);
-        // the GEMM behind it may be placed early only if its copy needs no SM (no copy or
-        // publish kernel that the placed CTAs could starve)
+        // the GEMM behind it may be placed early only if nothing on the copy stream needs an
+        // SM (no copy or publish kernel that the placed CTAs could starve; device-to-device
+        // copies of the expert cache may run as kernels too)
         const bool early = c->copy_path == LS_COPY_ENGINE && publish_needs_no_sm() &&
-                           (!c->capturing || c->capture_stream_ops);
+                           (!c->capturing || c->capture_stream_ops) && c->ecache_K == 0;
         track(c, launch_wait_ready(c->ready + slot, epoch, rc.wait_ns, c->err_word_dev, code, rc.s, early));
     };
     GemmDesc w0;
@@ -527,7 +553,7 @@ struct GpuExec : Executor {
         // a streamed MoE load moves the experts routed in this pass; a resident keeps all of
         // them, since later passes may route to any
         const uint8_t* mask = c->kind == LS_KIND_MOE_SWIGLU_BF16 && kind != LS_EV_LOAD_RESIDENT
-                                  ? c->moe_used + (int64_t)seg * c->E
+                                  ? c->moe_used_host_dev + (int64_t)seg * c->E
                                   : nullptr;
         const bool kern = c->copy_path == LS_COPY_KERNEL;
         if (kind == LS_EV_PREFETCH) {
@@ -604,6 +630,7 @@ ls_status check_params(const ls_params* p, ls_params* out, std::string* why) {
     }
     if ((d.alloc_fn == nullptr) != (d.free_fn == nullptr)) { *why = "alloc_fn and free_fn go together"; return LS_ERR_INVALID_ARG; }
     if (d.cross_run_prefetch != 0 && d.cross_run_prefetch != 1) { *why = "cross_run_prefetch must be 0 or 1"; return LS_ERR_INVALID_ARG; }
+    if (d.expert_cache_bytes < 0) { *why = "expert_cache_bytes < 0"; return LS_ERR_INVALID_ARG; }
     *out = d;
     return LS_OK;
 }
@@ -1057,8 +1084,26 @@ static ls_status register_impl(ls_ctx* c, const ls_segment_desc* segs, int32_t n
     if (c->kind == LS_KIND_MOE_SWIGLU_BF16) {
         CK(cudaMalloc(&c->moe_bounds, sizeof(int) * (size_t)n * (c->E + 1)));
         CK(cudaMalloc(&c->moe_used, (size_t)n * c->E));
-        CK(cudaHostAlloc((void**)&c->moe_used_host, (size_t)n * c->E, cudaHostAllocDefault));
+        CK(cudaHostAlloc((void**)&c->moe_used_host, (size_t)n * c->E, cudaHostAllocMapped));
+        CK(cudaHostGetDevicePointer((void**)&c->moe_used_host_dev, c->moe_used_host, 0));
         memset(c->moe_used_host, 1, (size_t)n * c->E);
+        if (c->prm.expert_cache_bytes > 0) {
+            c->ecache_eb = c->segs[0].slot_bytes / c->E;
+            const int64_t k = std::min<int64_t>(c->prm.expert_cache_bytes / c->ecache_eb, (int64_t)n * c->E);
+            if (k > 0) {
+                c->ecache = dev_alloc(c, (size_t)(k * c->ecache_eb), c->copy_stream);
+                if (!c->ecache) {
+                    set_err(c, "could not allocate the expert cache (%lld bytes)", (long long)(k * c->ecache_eb));
+                    return LS_ERR_OOM;
+                }
+                c->ecache_K = (int)k;
+                c->ecache_counts.assign((size_t)n * c->E, 0);
+                c->ecache_slot.assign((size_t)n * c->E, -1);
+                c->ecache_filled.assign((size_t)n * c->E, 0);
+                c->ecache_hits.assign(n, {});
+                c->ecache_fills.assign(n, {});
+            }
+        }
     }
     const int sms = gemm_num_sms();
     c->copy_ctas = c->prm.copy_ctas > 0 ? c->prm.copy_ctas : sms;
@@ -1081,6 +1126,65 @@ static void destroy_graph(ls_ctx* c) {
     c->graph = nullptr;
     c->graph_events.clear();
     cudaGetLastError();
+}
+
+// The expert cache's decisions for the pass whose routing moe_used_host holds: the hot set
+// is the K pairs of streamed layers routed in the most earlier passes (ties to the lower
+// layer, then expert); leaving pairs give back their slot, entering ones take the lowest
+// free slots in rank order; a routed hot pair is a hit once filled, else it is filled from
+// this pass's host copy. Hits are then cleared from moe_used_host, which becomes the set of
+// experts to copy from the host.
+static void ecache_plan_pass(ls_ctx* c) {
+    const int N = c->N, E = c->E, R = c->sched.residents();
+    std::vector<std::tuple<int64_t, int, int>> cand;
+    for (int l = R; l < N; ++l)
+        for (int e = 0; e < E; ++e)
+            if (c->ecache_counts[(size_t)l * E + e] > 0) cand.emplace_back(-c->ecache_counts[(size_t)l * E + e], l, e);
+    std::sort(cand.begin(), cand.end());
+    if ((int)cand.size() > c->ecache_K) cand.resize(c->ecache_K);
+    std::vector<char> hot((size_t)N * E, 0);
+    for (auto& t : cand) hot[(size_t)std::get<1>(t) * E + std::get<2>(t)] = 1;
+    std::vector<int> free_slots;
+    std::vector<char> taken(c->ecache_K, 0);
+    for (size_t i = 0; i < hot.size(); ++i) {
+        if (c->ecache_slot[i] >= 0 && !hot[i]) {
+            c->ecache_slot[i] = -1;
+            c->ecache_filled[i] = 0;
+        }
+        if (c->ecache_slot[i] >= 0) taken[c->ecache_slot[i]] = 1;
+    }
+    for (int k = c->ecache_K - 1; k >= 0; --k)
+        if (!taken[k]) free_slots.push_back(k);  // popped from the back: lowest first
+    for (int l = 0; l < N; ++l) {
+        c->ecache_hits[l].clear();
+        c->ecache_fills[l].clear();
+    }
+    for (auto& t : cand) {
+        const int l = std::get<1>(t), e = std::get<2>(t);
+        const size_t i = (size_t)l * E + e;
+        if (c->ecache_slot[i] < 0) {
+            c->ecache_slot[i] = free_slots.back();
+            free_slots.pop_back();
+        }
+    }
+    for (int l = R; l < N; ++l)
+        for (int e = 0; e < E; ++e) c->ecache_counts[(size_t)l * E + e] += c->moe_used_host[(size_t)l * E + e];
+    for (int l = R; l < N; ++l)
+        for (int e = 0; e < E; ++e) {
+            const size_t i = (size_t)l * E + e;
+            if (!c->moe_used_host[i]) continue;
+            if (hot[i] && c->ecache_filled[i]) {
+                c->ecache_hits[l].push_back({e, c->ecache_slot[i]});
+                c->moe_used_host[i] = 0;
+                ++c->n_ecache_hits;
+            } else {
+                if (hot[i]) {
+                    c->ecache_fills[l].push_back({e, c->ecache_slot[i]});
+                    c->ecache_filled[i] = 1;
+                }
+                ++c->n_ecache_host;
+            }
+        }
 }
 
 // Checks, workspaces and (MoE) routing of one pass on the caller's stream; fills the
@@ -1127,6 +1231,7 @@ static ls_status prepare_pass(ls_ctx* c, const void* x_dev, void* y_dev, int64_t
         }
         CK(cudaMemcpyAsync(c->moe_used_host, c->moe_used, (size_t)c->N * E, cudaMemcpyDeviceToHost, s));
         CK(cudaStreamSynchronize(s));
+        if (c->ecache_K > 0) ecache_plan_pass(c);
         const int64_t eb = c->segs[0].slot_bytes / E;
         const int R = c->sched.residents();  // residents are loaded whole (see GpuExec::load)
         for (int l = R; l < c->N; ++l) {
@@ -1418,6 +1523,8 @@ ls_status ls_get_stats(ls_ctx* c, ls_stats* out) {
     s.copy_engine_gbs = c->gbs_engine;
     s.graph_captures = c->graph_captures;
     s.graph_replays = c->graph_replays;
+    s.expert_cache_hits = c->n_ecache_hits;
+    s.expert_host_loads = c->n_ecache_host;
     const uint32_t n = std::min<uint32_t>(out->struct_size, sizeof(s));
     memcpy(out, &s, n);
     out->struct_size = n;
@@ -1467,6 +1574,7 @@ static void release_resources(ls_ctx* c) {
             if (c->seg_buf[s]) dev_free(c, c->seg_buf[s], (size_t)c->segs[s].slot_bytes, c->copy_stream);
         if (c->pool) dev_free(c, c->pool, (size_t)c->pool_bytes, c->copy_stream);
         if (c->shared_dev) dev_free(c, c->shared_dev, 0, c->copy_stream);
+        if (c->ecache) dev_free(c, c->ecache, (size_t)(c->ecache_K * c->ecache_eb), c->copy_stream);
         if (c->copy_stream) cudaStreamSynchronize(c->copy_stream);
         for (auto& sr : c->segs)
             if (sr.ranges_dev) cudaFree(sr.ranges_dev);

@@ -44,7 +44,7 @@ class ls_params(C.Structure):
                 ("alloc_fn", ALLOC_FN), ("free_fn", FREE_FN), ("alloc_user", C.c_void_p),
                 ("test_alloc_cap_bytes", C.c_int64), ("test_fail_async", C.c_int32),
                 ("test_drop_publish", C.c_int32), ("kernel_timing", C.c_int32),
-                ("cross_run_prefetch", C.c_int32)]
+                ("cross_run_prefetch", C.c_int32), ("expert_cache_bytes", C.c_int64)]
 
 
 class ls_tensor_desc(C.Structure):
@@ -91,7 +91,8 @@ class ls_stats(C.Structure):
                 ("sync_fallbacks", C.c_int64), ("pool_degradations", C.c_int64),
                 ("bytes_loaded", C.c_int64), ("copy_kernel_gbs", C.c_double),
                 ("copy_engine_gbs", C.c_double), ("graph_captures", C.c_int64),
-                ("graph_replays", C.c_int64)]
+                ("graph_replays", C.c_int64), ("expert_cache_hits", C.c_int64),
+                ("expert_host_loads", C.c_int64)]
 
 
 _P = C.c_void_p

@@ -125,6 +125,14 @@ typedef struct ls_params {
                                      starts its window afresh ("feat: prefetch streamed layers during
                                      compute", maintainer review: no cross-forward state). The prefetch
                                      of a run that never comes is released at ls_replan or destroy. */
+    int64_t expert_cache_bytes;   /* MoE kind: device memory for hot experts of streamed layers, on top of
+                                     max_vram_bytes (0 = none). It holds K = bytes / expert-blob bytes
+                                     experts: in each pass, the K (layer, expert) pairs routed in the most
+                                     earlier passes (ties to the lower layer, then expert); a hot expert is
+                                     copied in when its layer next loads it from the host, and a routed
+                                     expert found there is copied within device memory instead of over
+                                     the host link. Bits are unchanged; the schedule's load bytes count
+                                     the host copies only. */
 } ls_params;
 
 /* One tensor of a segment: host memory owned by the caller, kept alive and
@@ -197,6 +205,8 @@ typedef struct ls_stats {
     double copy_engine_gbs;
     int64_t graph_captures;    /* passes captured into a CUDA graph by ls_run_graph */
     int64_t graph_replays;     /* passes issued as a replay of the captured graph */
+    int64_t expert_cache_hits; /* routed experts of streamed layers served from the expert cache */
+    int64_t expert_host_loads; /* routed experts of streamed layers copied from the host */
 } ls_stats;
 
 /* Per-kernel timing, accumulated over runs while params.kernel_timing is on.

@@ -577,6 +577,54 @@ def test_moe_residents_follow_routing_changes():
         L.ls_ctx_destroy(ctx)
 
 
+@pytest.mark.parametrize("copy_path", [2, 1])
+def test_moe_expert_cache_matches_oracle_policy(copy_path):
+    """Expert cache of the streamed layers: hot experts come from device memory, the
+    schedule's load bytes are the oracle policy's host copies, and the bits equal a run
+    without the cache."""
+    from oracle import expert_cache, forward as F
+    cfg = _moe_cfg(4, 64, experts=8, hidden=256, ffn=128, k=2)
+    S = synth.segment_slot_bytes(cfg)
+    eb = S // cfg.n_experts
+    K = 6
+    hs = synth.HostStack(cfg)
+    rng = np.random.default_rng(9)
+    bias = np.array([3.0, 2.0, 1.5, 0.5, 0, 0, 0, 0], np.float32)   # data-dependent routing: skewed
+    passes = [(rng.standard_normal((cfg.n_segments, cfg.tokens, cfg.n_experts)).astype(np.float32) + bias)
+              for _ in range(5)]
+    outs = {}
+    for cache in (0, K * eb):
+        ctx, _ = make_ctx(cfg, hs, expert_cache_bytes=cache, copy_path=copy_path)
+        try:
+            x = x_dev(cfg)
+            ys = []
+            for lg in passes:
+                y = torch.empty_like(x)
+                L.ls_run(ctx, x, y, cfg.tokens, logits=torch.from_numpy(lg).cuda(), top_k=cfg.top_k)
+                ys.append(y)
+            torch.cuda.synchronize()
+            outs[cache] = (ys, L.ls_get_schedule(ctx), L.ls_get_stats(ctx))
+        finally:
+            L.ls_ctx_destroy(ctx)
+    ys, sched, st = outs[K * eb]
+    for y, y0 in zip(ys, outs[0][0]):
+        assert torch.equal(y.view(torch.int16), y0.view(torch.int16))
+    assert rel_err(to_f64(ys[-1]), ostack.stack_forward(cfg, logits=list(passes[-1]))) <= BOUND
+    used = []
+    for lg in passes:
+        u = np.zeros((cfg.n_segments, cfg.n_experts), bool)
+        for l in range(cfg.n_segments):
+            u[l, np.unique(F.route_topk(lg[l], cfg.top_k)[0])] = True
+        used.append(u)
+    plan = expert_cache.cache_passes(used, K, 0)
+    load = [[int(host[l].sum()) * eb for l in range(cfg.n_segments)] for host, *_ in plan]
+    sim, _ = _sim_events(cfg, hs, 1, 0, cfg.max_vram_bytes, 1, len(passes), load=load)
+    assert sched == [tuple(e) for e in sim.events]
+    hits = sum(int(h.sum()) for _, h, _, _ in plan)
+    assert hits > 0 and st["expert_cache_hits"] == hits
+    assert st["expert_host_loads"] == sum(int(h.sum()) for h, *_ in plan)
+
+
 def test_moe_full_expert_shapes_sampled_rows():
     cfg = _moe_cfg(4, 2048)
     hs = synth.HostStack(cfg)
