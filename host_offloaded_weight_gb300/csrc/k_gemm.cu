@@ -594,16 +594,21 @@ constexpr int S2_B = 128 * 64 * 2;             // this CTA's half (128 rows) of 
 constexpr int S2_STAGE = S2_A + S2_B;
 constexpr int S2_STG_BF = 32 * 32 * 2;         // 32x32 bf16 output staging tile (64-byte rows)
 constexpr int S2_STG_F32 = 32 * 32 * 4;        // 32x32 fp32 output staging tile (128-byte rows)
-// Residual epilogues also write the fp32 copy: they give up one mainloop stage
-// and single-buffer their staging tiles; the others double-buffer theirs.
+// Residual epilogues also write the fp32 copy: they give up one mainloop stage and
+// run 8 epilogue warps (their residual registers need 168 per thread, the cap of a
+// 10-warp CTA). The others run 16 epilogue warps (4 per TMEM lane quarter, 96
+// registers) so that more warps hide each other's latencies; every epilogue warp
+// single-buffers its staging tiles.
 __host__ __device__ constexpr bool s2_out_f32(int epi) { return epi == EPI_BIAS_RESID || epi == EPI_RESID; }
 __host__ __device__ constexpr int s2_stages(int epi) { return s2_out_f32(epi) ? 5 : 6; }
-__host__ __device__ constexpr int s2_nbuf(int epi) { return s2_out_f32(epi) ? 1 : 2; }
+__host__ __device__ constexpr int s2_nbuf(int) { return 1; }
+__host__ __device__ constexpr int s2_epi_warps(int epi) { return s2_out_f32(epi) ? 8 : 16; }
+__host__ __device__ constexpr int s2_threads(int epi) { return 64 + 32 * s2_epi_warps(epi); }
 __host__ __device__ constexpr int s2_warp_bytes(int epi) {
     return s2_nbuf(epi) * (S2_STG_BF + (s2_out_f32(epi) ? S2_STG_F32 : 0));
 }
 __host__ __device__ constexpr int s2_smem_bytes(int epi) {
-    return s2_stages(epi) * S2_STAGE + EPI_WARPS * s2_warp_bytes(epi) + 1024 + 256;
+    return s2_stages(epi) * S2_STAGE + s2_epi_warps(epi) * s2_warp_bytes(epi) + 1024 + 256;
 }
 static_assert(s2_smem_bytes(EPI_BIAS_RESID) <= 232448 && s2_smem_bytes(EPI_STORE) <= 232448, "shared memory");
 
@@ -715,7 +720,7 @@ __device__ __forceinline__ float4 ld_shared_f4(uint32_t addr) {
 }
 
 template <int EPI, bool DUAL>
-__global__ void __launch_bounds__(NUM_THREADS, 1) gemm_bf16_tc2(const __grid_constant__ GemmParams p) {
+__global__ void __launch_bounds__(s2_threads(EPI), 1) gemm_bf16_tc2(const __grid_constant__ GemmParams p) {
     extern __shared__ uint8_t smem_raw[];
     const uint32_t raw = smem_u32(smem_raw);
     const uint32_t base = (raw + 1023u) & ~1023u;
@@ -725,7 +730,8 @@ __global__ void __launch_bounds__(NUM_THREADS, 1) gemm_bf16_tc2(const __grid_con
     constexpr bool OUT32 = s2_out_f32(EPI);
     constexpr int NBUF = s2_nbuf(EPI);
     const uint32_t stg0 = base + S2_STAGES * S2_STAGE;  // epilogue staging tiles, WSB bytes per warp
-    const uint32_t bar0 = stg0 + EPI_WARPS * WSB;
+    constexpr int EW = s2_epi_warps(EPI);
+    const uint32_t bar0 = stg0 + EW * WSB;
     auto full_bar = [&](int s) { return bar0 + 8u * s; };
     auto empty_bar = [&](int s) { return bar0 + 8u * (S2_STAGES + s); };
     auto tfull_bar = [&](int b) { return bar0 + 8u * (2 * S2_STAGES + b); };
@@ -747,7 +753,7 @@ __global__ void __launch_bounds__(NUM_THREADS, 1) gemm_bf16_tc2(const __grid_con
         }
         for (int b = 0; b < 2; ++b) {
             mbar_init(tfull_bar(b), 1);
-            mbar_init(tempty_bar(b), 2 * EPI_WARPS);
+            mbar_init(tempty_bar(b), 2 * EW);
         }
         mbar_init(done_bar, 1);
         asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
@@ -841,7 +847,7 @@ __global__ void __launch_bounds__(NUM_THREADS, 1) gemm_bf16_tc2(const __grid_con
         }
     } else {
         // Epilogue: warp (q, half) owns TMEM lanes q*32.. (its 32 output rows, one per
-        // thread) and half of the tile's 32-column chunks. A chunk is finished in
+        // thread) and a 4/EW share of the tile's 32-column chunks. A chunk is finished in
         // registers, written into a swizzled staging tile and sent out by one bulk
         // tensor store that runs while the warp moves on; the tensor map clips
         // rows >= M and columns >= N.
@@ -855,7 +861,7 @@ __global__ void __launch_bounds__(NUM_THREADS, 1) gemm_bf16_tc2(const __grid_con
             if (want32) tma_prefetch_desc(&p.tmC32);
         }
         constexpr int CHUNKS = DUAL ? ACC_COLS / 64 : ACC_COLS / 32;
-        constexpr int PER_WARP = CHUNKS / (EPI_WARPS / 4);
+        constexpr int PER_WARP = CHUNKS / (EW / 4);
         const int c_begin = half * PER_WARP;
         // Residual epilogues read the residual while the accumulator is still being
         // computed: coalesced loads (8 lanes cover one row's 32 columns, 4 rows per
@@ -1081,7 +1087,7 @@ cudaError_t launch_t2(const GemmParams& p, int clusters, cudaStream_t s) {
     }
     cudaLaunchConfig_t cfg = {};
     cfg.gridDim = dim3(2 * clusters);
-    cfg.blockDim = dim3(NUM_THREADS);
+    cfg.blockDim = dim3(s2_threads(EPI));
     cfg.dynamicSmemBytes = s2_smem_bytes(EPI);
     cfg.stream = s;
     cudaLaunchAttribute at[2];
