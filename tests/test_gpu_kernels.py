@@ -168,6 +168,46 @@ def test_gemm_long_k_bits_independent_of_grid(epi):
         assert torch.equal(out.view(torch.int16), ref.view(torch.int16)), ctas
 
 
+# Tiles about 100 k-blocks long with ragged M and N; the second shape's K ends in a
+# partial k-block.
+VERY_LONG_K_SHAPES = [(1000, 1032, 6400), (300, 520, 6200)]
+
+
+@pytest.mark.parametrize("M,N,K", VERY_LONG_K_SHAPES)
+@pytest.mark.parametrize("epi", [L.LSK_EPI_STORE, L.LSK_EPI_BIAS_GELU, L.LSK_EPI_BIAS_RESID,
+                                 L.LSK_EPI_SWIGLU, L.LSK_EPI_RESID])
+def test_gemm_very_long_k_vs_oracle(M, N, K, epi):
+    test_gemm_epilogues_vs_oracle(M, N, K, epi)
+
+
+@pytest.mark.parametrize("epi", [L.LSK_EPI_BIAS_RESID, L.LSK_EPI_RESID])
+def test_gemm_very_long_k_fp32_residual_stream(epi):
+    test_gemm_fp32_residual_stream(1000, 1032, 6400, epi)
+
+
+@pytest.mark.parametrize("epi", [L.LSK_EPI_STORE, L.LSK_EPI_SWIGLU, L.LSK_EPI_BIAS_RESID])
+def test_gemm_very_long_k_bits_independent_of_grid(epi):
+    """Fewer clusters take more tiles each and produce the same bits (residual epilogue
+    included)."""
+    M, N, K = 1000, 1032, 6400
+    b_rows = 2 * N if epi == L.LSK_EPI_SWIGLU else N
+    ab, _ = rand_bf16((M, K), 51)
+    bb, _ = rand_bf16((b_rows, K), 52, 1.0 / np.sqrt(K))
+    biasb, _ = rand_bf16((N,), 53, 0.5)
+    rb, _ = rand_bf16((M, N), 54, 1.0)
+    A, B = bf16_dev(ab), bf16_dev(bb)
+    kw = dict(b_rows=b_rows, b2_row_off=N if epi == L.LSK_EPI_SWIGLU else 0, bias=bf16_dev(biasb),
+              resid=bf16_dev(rb))
+    ref = torch.empty((M, N), dtype=torch.bfloat16, device="cuda")
+    L.lsk_gemm_bf16(epi, A, B, ref, M, N, K, max_ctas=0, **kw)
+    for ctas in (2, 6, 38, 0):
+        out = torch.full_like(ref, float("nan"))
+        L.lsk_gemm_bf16(epi, A, B, out, M, N, K, max_ctas=ctas, **kw)
+        torch.cuda.synchronize()
+        _no_device_error()
+        assert torch.equal(out.view(torch.int16), ref.view(torch.int16)), ctas
+
+
 @pytest.mark.parametrize("M,N,K", [(4096, 4096, 1024), (4096, 1024, 4096)])
 def test_gemm_full_size_sampled_rows(M, N, K):
     """The stack's own GEMM shapes in the launch configuration ls_run uses,
