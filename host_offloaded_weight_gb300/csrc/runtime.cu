@@ -1496,10 +1496,15 @@ ls_status ls_run_host(ls_ctx* c, const void* x_host, void* y_host, int64_t token
         r.logits = c->stage_logits;
         r.top_k = routing_host->top_k;
     }
-    ls_status st = ls_run(c, c->stage_x, c->stage_y, tokens, c->own_stream, moe ? &r : nullptr);
-    if (st < 0) return st;
+    // the pass, then the copy back in the same stream, then a single synchronisation
+    ls_status st = ls_run_async(c, c->stage_x, c->stage_y, tokens, c->own_stream, moe ? &r : nullptr);
+    if (st < 0) {
+        ls_sync(c);
+        return st;
+    }
     CK(cudaMemcpyAsync(y_host, c->stage_y, xb, cudaMemcpyDeviceToHost, c->own_stream));
-    CK(cudaStreamSynchronize(c->own_stream));
+    const ls_status sy = ls_sync(c);
+    if (sy < 0) return sy;
     return st;
 }
 
