@@ -411,8 +411,8 @@ def run_ours(args, cfg, world, rank, local):
 # DRAM bytes (read + write) per launch from ncu captures of the current kernels
 # (profiles/gemm_pair_dit_ffn_12x1024x4096.md); absent = not captured.
 TRAFFIC: dict = {
-    ("dit_ffn_12x1024x4096", "gemm_up"): 16_813_568 + 530_688,
-    ("dit_ffn_12x1024x4096", "gemm_down"): 50_393_088 + 1_800_192,
+    ("dit_ffn_12x1024x4096", "gemm_up"): 16_812_800 + 527_360,
+    ("dit_ffn_12x1024x4096", "gemm_down"): 50_413_312 + 2_203_648,
 }
 
 

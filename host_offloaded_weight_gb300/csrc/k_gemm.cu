@@ -37,6 +37,8 @@
 #include "common.cuh"
 #include "kernels.h"
 
+#include <algorithm>
+#include <cstdint>
 #include <mutex>
 #include <unordered_map>
 
@@ -193,6 +195,21 @@ __device__ __forceinline__ void tmem_ld32(uint32_t taddr, uint32_t (&r)[32]) {
 }
 __device__ __forceinline__ void tmem_ld_wait() {
     asm volatile("tcgen05.wait::ld.sync.aligned;" ::: "memory");
+}
+// Lane l of the warp writes r[0..31] into its TMEM lane, 32 consecutive columns from taddr.
+__device__ __forceinline__ void tmem_st32(uint32_t taddr, const uint32_t (&r)[32]) {
+    asm volatile(
+        "tcgen05.st.sync.aligned.32x32b.x32.b32 [%0], "
+        "{%1,%2,%3,%4,%5,%6,%7,%8,%9,%10,%11,%12,%13,%14,%15,%16,"
+        "%17,%18,%19,%20,%21,%22,%23,%24,%25,%26,%27,%28,%29,%30,%31,%32};" ::"r"(taddr),
+        "r"(r[0]), "r"(r[1]), "r"(r[2]), "r"(r[3]), "r"(r[4]), "r"(r[5]), "r"(r[6]), "r"(r[7]), "r"(r[8]),
+        "r"(r[9]), "r"(r[10]), "r"(r[11]), "r"(r[12]), "r"(r[13]), "r"(r[14]), "r"(r[15]), "r"(r[16]),
+        "r"(r[17]), "r"(r[18]), "r"(r[19]), "r"(r[20]), "r"(r[21]), "r"(r[22]), "r"(r[23]), "r"(r[24]),
+        "r"(r[25]), "r"(r[26]), "r"(r[27]), "r"(r[28]), "r"(r[29]), "r"(r[30]), "r"(r[31])
+        : "memory");
+}
+__device__ __forceinline__ void tmem_st_wait() {
+    asm volatile("tcgen05.wait::st.sync.aligned;" ::: "memory");
 }
 
 // Instruction descriptor of kind::f16: D fp32, A and B bf16, both K-major.
@@ -580,9 +597,9 @@ __global__ void __launch_bounds__(NUM_THREADS, 1) gemm_bf16_tc(const __grid_cons
 }
 
 // ------------------------------------------------------------------ pair-CTA (cta_group::2) kernel
-// A 2-CTA cluster computes a 256x256 tile: CTA r loads its 128 rows of A and
-// its 128 rows of B (for the gate/up pair: the leader the G half, the peer the
-// U half), so each SM takes in half of B; the even CTA issues
+// A 2-CTA cluster computes a 256 x BN tile: CTA r loads its 128 rows of A and
+// its BN/2 rows of B (for the gate/up pair, BN = 256: the leader 128 rows of G,
+// the peer 128 of U), so each SM takes in half of B; the even CTA issues
 // tcgen05.mma.cta_group::2 (M = 256) reading both CTAs' shared memory and
 // writing each CTA's 128 rows into that CTA's TMEM. Both CTAs' TMA loads
 // complete on the leader's full barrier; the leader's commits arrive on both
@@ -590,27 +607,33 @@ __global__ void __launch_bounds__(NUM_THREADS, 1) gemm_bf16_tc(const __grid_cons
 // barrier. All waits are bounded, and both CTAs always reach the closing
 // cluster barrier before TMEM is freed.
 constexpr int S2_A = 128 * 64 * 2;             // this CTA's 128 rows of A
-constexpr int S2_B = 128 * 64 * 2;             // this CTA's half (128 rows) of B
-constexpr int S2_STAGE = S2_A + S2_B;
+__host__ __device__ constexpr int s2_b_bytes(int bn) { return (bn / 2) * 64 * 2; }  // its BN/2 rows of B
+__host__ __device__ constexpr int s2_stage_bytes(int bn) { return S2_A + s2_b_bytes(bn); }
 constexpr int S2_STG_BF = 32 * 32 * 2;         // 32x32 bf16 output staging tile (64-byte rows)
 constexpr int S2_STG_F32 = 32 * 32 * 4;        // 32x32 fp32 output staging tile (128-byte rows)
-// Residual epilogues also write the fp32 copy: they give up one mainloop stage and
-// run 8 epilogue warps (their residual registers need 168 per thread, the cap of a
-// 10-warp CTA). The others run 16 epilogue warps (4 per TMEM lane quarter, 96
-// registers) so that more warps hide each other's latencies; every epilogue warp
-// single-buffers its staging tiles.
+// Residual epilogues also write the fp32 copy: their staging takes room from the
+// mainloop stages and they run 8 epilogue warps (their residual registers need 168
+// per thread, the cap of a 10-warp CTA). The others run 16 epilogue warps (4 per TMEM
+// lane quarter, 96 registers) so that more warps hide each other's latencies; every
+// epilogue warp single-buffers its staging tiles. The mainloop takes as many stages
+// as the rest of shared memory holds (at most 8).
 __host__ __device__ constexpr bool s2_out_f32(int epi) { return epi == EPI_BIAS_RESID || epi == EPI_RESID; }
-__host__ __device__ constexpr int s2_stages(int epi) { return s2_out_f32(epi) ? 5 : 6; }
 __host__ __device__ constexpr int s2_nbuf(int) { return 1; }
 __host__ __device__ constexpr int s2_epi_warps(int epi) { return s2_out_f32(epi) ? 8 : 16; }
 __host__ __device__ constexpr int s2_threads(int epi) { return 64 + 32 * s2_epi_warps(epi); }
 __host__ __device__ constexpr int s2_warp_bytes(int epi) {
     return s2_nbuf(epi) * (S2_STG_BF + (s2_out_f32(epi) ? S2_STG_F32 : 0));
 }
-__host__ __device__ constexpr int s2_smem_bytes(int epi) {
-    return s2_stages(epi) * S2_STAGE + s2_epi_warps(epi) * s2_warp_bytes(epi) + 1024 + 256;
+__host__ __device__ constexpr int s2_stages(int epi, int bn) {
+    return (232448 - 1024 - 256 - s2_epi_warps(epi) * s2_warp_bytes(epi)) / s2_stage_bytes(bn) < 8
+               ? (232448 - 1024 - 256 - s2_epi_warps(epi) * s2_warp_bytes(epi)) / s2_stage_bytes(bn)
+               : 8;
 }
-static_assert(s2_smem_bytes(EPI_BIAS_RESID) <= 232448 && s2_smem_bytes(EPI_STORE) <= 232448, "shared memory");
+__host__ __device__ constexpr int s2_smem_bytes(int epi, int bn) {
+    return s2_stages(epi, bn) * s2_stage_bytes(bn) + s2_epi_warps(epi) * s2_warp_bytes(epi) + 1024 + 256;
+}
+static_assert(s2_stages(EPI_BIAS_RESID, 256) == 5 && s2_stages(EPI_STORE, 256) == 6, "stages at BN = 256");
+static_assert(s2_smem_bytes(EPI_BIAS_RESID, 160) <= 232448 && s2_smem_bytes(EPI_STORE, 160) <= 232448, "shared memory");
 
 __device__ __forceinline__ uint32_t cluster_rank() {
     uint32_t r;
@@ -708,6 +731,19 @@ __device__ __forceinline__ float4 load_resid4(const GemmParams& p, int row, int 
     return make_float4(bf2f((uint16_t)(h.x & 0xffff)), bf2f((uint16_t)(h.x >> 16)), bf2f((uint16_t)(h.y & 0xffff)),
                        bf2f((uint16_t)(h.y >> 16)));
 }
+// The residual's 32 columns n0.. of one row, as fp32 bit patterns (zeros past M or N).
+__device__ __forceinline__ void load_resid_row32(const GemmParams& p, int row, int n0, uint32_t (&r)[32]) {
+    float4 x[8];
+#pragma unroll
+    for (int g = 0; g < 8; ++g) x[g] = load_resid4(p, row, n0 + 4 * g);
+#pragma unroll
+    for (int g = 0; g < 8; ++g) {
+        r[4 * g] = __float_as_uint(x[g].x);
+        r[4 * g + 1] = __float_as_uint(x[g].y);
+        r[4 * g + 2] = __float_as_uint(x[g].z);
+        r[4 * g + 3] = __float_as_uint(x[g].w);
+    }
+}
 __device__ __forceinline__ void st_shared_f4(uint32_t addr, float4 v) {
     asm volatile("st.shared.v4.f32 [%0], {%1, %2, %3, %4};" ::"r"(addr), "f"(v.x), "f"(v.y), "f"(v.z), "f"(v.w)
                  : "memory");
@@ -719,13 +755,15 @@ __device__ __forceinline__ float4 ld_shared_f4(uint32_t addr) {
     return v;
 }
 
-template <int EPI, bool DUAL>
+template <int EPI, bool DUAL, int BN>
 __global__ void __launch_bounds__(s2_threads(EPI), 1) gemm_bf16_tc2(const __grid_constant__ GemmParams p) {
+    static_assert(BN % 32 == 0 && BN >= 64 && BN <= 256 && (!DUAL || BN == 256), "tile width");
     extern __shared__ uint8_t smem_raw[];
     const uint32_t raw = smem_u32(smem_raw);
     const uint32_t base = (raw + 1023u) & ~1023u;
     uint8_t* gbase = smem_raw + (base - raw);
-    constexpr int S2_STAGES = s2_stages(EPI);
+    constexpr int S2_STAGES = s2_stages(EPI, BN);
+    constexpr int S2_STAGE = s2_stage_bytes(BN);
     constexpr int WSB = s2_warp_bytes(EPI);
     constexpr bool OUT32 = s2_out_f32(EPI);
     constexpr int NBUF = s2_nbuf(EPI);
@@ -768,7 +806,7 @@ __global__ void __launch_bounds__(s2_threads(EPI), 1) gemm_bf16_tc2(const __grid
     grid_dep_wait();
     const uint32_t tmem_base = *tmem_slot;
     const int num_m2 = (p.M + 255) / 256;
-    const int num_tiles = num_m2 * p.num_n_tiles;  // num_n_tiles counts 256 (dual: 128) columns
+    const int num_tiles = num_m2 * p.num_n_tiles;  // num_n_tiles counts BN (dual: 128) columns
     const int kb_n = p.num_k_blocks;
 
     if (warp == 0) {
@@ -782,7 +820,7 @@ __global__ void __launch_bounds__(s2_threads(EPI), 1) gemm_bf16_tc2(const __grid
                 const int m2 = t % num_m2, n = t / num_m2;
                 const int a_row = m2 * 256 + (int)rank * 128;
                 // dense: the pair covers 256 columns; gate/up pair: 128 columns of G (leader) and of U (peer)
-                const int b_row = DUAL ? n * 128 + (rank ? p.b2_row_off : 0) : n * 256 + (int)rank * 128;
+                const int b_row = DUAL ? n * 128 + (rank ? p.b2_row_off : 0) : n * BN + (int)rank * (BN / 2);
                 for (int kb = 0; kb < kb_n; ++kb, ++it) {
                     const int s = it % S2_STAGES;
                     const uint32_t ph = (uint32_t)(it / S2_STAGES) & 1u;
@@ -811,7 +849,7 @@ __global__ void __launch_bounds__(s2_threads(EPI), 1) gemm_bf16_tc2(const __grid
         }
     } else if (warp == 1) {
         if (lane == 0 && leader) {
-            constexpr uint32_t IDESC = make_idesc(256, 256);
+            constexpr uint32_t IDESC = make_idesc(256, BN);
             int it = 0, tcount = 0;
             bool ok = true;
             for (int t = cluster_id; t < num_tiles && ok; t += n_clusters, ++tcount) {
@@ -847,7 +885,8 @@ __global__ void __launch_bounds__(s2_threads(EPI), 1) gemm_bf16_tc2(const __grid
         }
     } else {
         // Epilogue: warp (q, half) owns TMEM lanes q*32.. (its 32 output rows, one per
-        // thread) and a 4/EW share of the tile's 32-column chunks. A chunk is finished in
+        // thread) and a contiguous 4/EW share of the tile's 32-column chunks (shares
+        // differ by one chunk at most when they do not divide). A chunk is finished in
         // registers, written into a swizzled staging tile and sent out by one bulk
         // tensor store that runs while the warp moves on; the tensor map clips
         // rows >= M and columns >= N.
@@ -860,9 +899,11 @@ __global__ void __launch_bounds__(s2_threads(EPI), 1) gemm_bf16_tc2(const __grid
             tma_prefetch_desc(&p.tmC);
             if (want32) tma_prefetch_desc(&p.tmC32);
         }
-        constexpr int CHUNKS = DUAL ? ACC_COLS / 64 : ACC_COLS / 32;
-        constexpr int PER_WARP = CHUNKS / (EW / 4);
-        const int c_begin = half * PER_WARP;
+        constexpr int CHUNKS = DUAL ? ACC_COLS / 64 : BN / 32;
+        constexpr int WPQ = EW / 4;                                // warps per TMEM lane quarter
+        constexpr int PER_WARP = (CHUNKS + WPQ - 1) / WPQ;         // the largest share
+        const int c_begin = half * CHUNKS / WPQ;
+        const int n_chunks = (half + 1) * CHUNKS / WPQ - c_begin;  // this warp's share
         // Residual epilogues read the residual while the accumulator is still being
         // computed: coalesced loads (8 lanes cover one row's 32 columns, 4 rows per
         // instruction) for the tile's first two chunks go out before the wait, each
@@ -879,17 +920,59 @@ __global__ void __launch_bounds__(s2_threads(EPI), 1) gemm_bf16_tc2(const __grid
             __syncwarp();
             if (lane == 0) remote_arrive(b ? leader_tempty1 : leader_tempty0);  // one arrive per warp
         };
-        int tcount = 0, sb = 0;
+        int sb = 0;
+        // Chunk output: v (row per lane) goes into the swizzled staging tiles and out by
+        // bulk tensor stores. The caller has made sure the staging tiles are free.
+        auto store_chunk = [&](float (&v)[32], int n0, int row0) {
+            const uint32_t s32 = stg + NBUF * S2_STG_BF + (uint32_t)sb * S2_STG_F32;
+            const uint32_t sbf = stg + (uint32_t)sb * S2_STG_BF;
+            // 64-byte swizzle: 16-byte unit j of row r sits at unit j ^ ((r >> 1) & 3)
+#pragma unroll
+            for (int j = 0; j < 4; ++j)
+                st_shared_v4(sbf + lane * 64 + ((j ^ ((lane >> 1) & 3)) << 4), pack_bf16(v[8 * j], v[8 * j + 1]),
+                             pack_bf16(v[8 * j + 2], v[8 * j + 3]), pack_bf16(v[8 * j + 4], v[8 * j + 5]),
+                             pack_bf16(v[8 * j + 6], v[8 * j + 7]));
+            if (want32) {
+                // 128-byte swizzle: 16-byte unit j of row r sits at unit j ^ (r & 7)
+#pragma unroll
+                for (int j = 0; j < 8; ++j)
+                    st_shared_v4(s32 + lane * 128 + ((j ^ (lane & 7)) << 4), __float_as_uint(v[4 * j]),
+                                 __float_as_uint(v[4 * j + 1]), __float_as_uint(v[4 * j + 2]),
+                                 __float_as_uint(v[4 * j + 3]));
+            }
+            fence_async_smem();
+            __syncwarp();
+            if (lane == 0) {
+                tma_store_2d(&p.tmC, sbf, n0, row0);
+                if (want32) tma_store_2d(&p.tmC32, s32, n0, row0);
+                bulk_commit();
+            }
+            if (NBUF == 2) sb ^= 1;
+        };
+        int tcount = 0;
         for (int t = cluster_id; t < num_tiles; t += n_clusters, ++tcount) {
             const int buf = tcount & 1;
             const uint32_t tph = (uint32_t)(tcount >> 1) & 1u;
             const int m2 = t % num_m2, n = t / num_m2;
             const int row0 = m2 * 256 + (int)rank * 128 + q * 32;
-            const int nbase = DUAL ? n * 128 : n * 256;
+            const int nbase = DUAL ? n * 128 : n * BN;
+            // A CTA's last tile leaves the other accumulator buffer unused: its residual
+            // goes there (row per lane, as the accumulator) while the MMAs still run, so the
+            // epilogue after the last accumulator reads no global memory.
+            const bool last = OUT32 && t + n_clusters >= num_tiles;
+            const uint32_t rbase = tmem_base + ((uint32_t)(q * 32) << 16) + (uint32_t)((buf ^ 1) * ACC_COLS);
             float4 g[2][8];
-            if (OUT32) {
+            if (last) {
+#pragma unroll 1
+                for (int i = 0; i < n_chunks; ++i) {
+                    uint32_t rr[32];
+                    load_resid_row32(p, row0 + lane, nbase + (c_begin + i) * 32, rr);
+                    tmem_st32(rbase + (c_begin + i) * 32, rr);
+                }
+                tmem_st_wait();
+            } else if (OUT32) {
                 issue(row0, nbase + c_begin * 32, g[0]);
-                issue(row0, nbase + (c_begin + 1) * 32, g[1]);
+                if (n_chunks > 1) issue(row0, nbase + (c_begin + 1) * 32, g[1]);
             }
             // warp-uniform outcome: TMEM loads and the single arrive below need every lane
             if (!__all_sync(0xffffffffu, mbar_wait(tfull_bar(buf), tph, p.err, 4, p.mbar_limit_ns) && !s_abort)) {
@@ -898,16 +981,45 @@ __global__ void __launch_bounds__(s2_threads(EPI), 1) gemm_bf16_tc2(const __grid
             }
             tc_fence_after();
             const uint32_t tbase = tmem_base + ((uint32_t)(q * 32) << 16) + (uint32_t)(buf * ACC_COLS);
+            if (last) {
+#pragma unroll 1
+                for (int i = 0; i < n_chunks; ++i) {
+                    const int c = c_begin + i;
+                    const int n0 = nbase + c * 32;
+                    uint32_t r[32], rr[32];
+                    tmem_ld32(tbase + c * 32, r);
+                    tmem_ld32(rbase + c * 32, rr);
+                    tmem_ld_wait();
+                    if (n0 < p.N && row0 < p.M) {  // uniform across the warp
+                        float v[32];
+#pragma unroll
+                        for (int j = 0; j < 32; ++j) v[j] = __uint_as_float(r[j]);
+                        if (EPI == EPI_BIAS_RESID) add_bias_row(p, n0, v);
+#pragma unroll
+                        for (int j = 0; j < 32; ++j) v[j] += __uint_as_float(rr[j]);
+                        if (lane == 0) bulk_wait_read<0>();  // the previous chunk's stores have left the staging tiles
+                        __syncwarp();
+                        store_chunk(v, n0, row0);
+                    }
+                }
+                release(buf);
+                continue;
+            }
             // unrolled only where the residual registers rotate (static indexing)
 #pragma unroll (OUT32 ? PER_WARP : 1)
             for (int i = 0; i < PER_WARP; ++i) {
+                // a fixed trip count keeps the ring's indexing static; shares one chunk
+                // short skip the last pass
+                const bool have = i < n_chunks;
                 const int c = c_begin + i;
                 const int n0 = nbase + c * 32;
                 uint32_t r[32], r2[32];
-                tmem_ld32(tbase + c * 32, r);
-                if (DUAL) tmem_ld32(tbase + ACC_COLS / 2 + c * 32, r2);
-                tmem_ld_wait();
-                if (n0 < p.N && row0 < p.M) {  // uniform across the warp
+                if (have) {
+                    tmem_ld32(tbase + c * 32, r);
+                    if (DUAL) tmem_ld32(tbase + ACC_COLS / 2 + c * 32, r2);
+                    tmem_ld_wait();
+                }
+                if (have && n0 < p.N && row0 < p.M) {  // uniform across the warp
                     float v[32];
 #pragma unroll
                     for (int j = 0; j < 32; ++j) v[j] = __uint_as_float(r[j]);
@@ -939,31 +1051,9 @@ __global__ void __launch_bounds__(s2_threads(EPI), 1) gemm_bf16_tc2(const __grid
                         if (lane == 0) bulk_wait_read<NBUF - 1>();
                         __syncwarp();
                     }
-                    const uint32_t sbf = stg + (uint32_t)sb * S2_STG_BF;
-                    // 64-byte swizzle: 16-byte unit j of row r sits at unit j ^ ((r >> 1) & 3)
-#pragma unroll
-                    for (int j = 0; j < 4; ++j)
-                        st_shared_v4(sbf + lane * 64 + ((j ^ ((lane >> 1) & 3)) << 4), pack_bf16(v[8 * j], v[8 * j + 1]),
-                                     pack_bf16(v[8 * j + 2], v[8 * j + 3]), pack_bf16(v[8 * j + 4], v[8 * j + 5]),
-                                     pack_bf16(v[8 * j + 6], v[8 * j + 7]));
-                    if (want32) {
-                        // 128-byte swizzle: 16-byte unit j of row r sits at unit j ^ (r & 7)
-#pragma unroll
-                        for (int j = 0; j < 8; ++j)
-                            st_shared_v4(s32 + lane * 128 + ((j ^ (lane & 7)) << 4), __float_as_uint(v[4 * j]),
-                                         __float_as_uint(v[4 * j + 1]), __float_as_uint(v[4 * j + 2]),
-                                         __float_as_uint(v[4 * j + 3]));
-                    }
-                    fence_async_smem();
-                    __syncwarp();
-                    if (lane == 0) {
-                        tma_store_2d(&p.tmC, sbf, n0, row0);
-                        if (want32) tma_store_2d(&p.tmC32, s32, n0, row0);
-                        bulk_commit();
-                    }
-                    if (NBUF == 2) sb ^= 1;
+                    store_chunk(v, n0, row0);
                 }
-                if (OUT32 && i + 2 < PER_WARP) issue(row0, n0 + 64, g[i & 1]);
+                if (OUT32 && i + 2 < n_chunks) issue(row0, n0 + 64, g[i & 1]);
             }
             release(buf);
         }
@@ -1076,19 +1166,20 @@ cudaError_t launch_t(const GemmParams& p, int grid, cudaStream_t s) {
     return cudaLaunchKernelEx(&cfg, kern, p);
 }
 
-template <int EPI, bool DUAL>
+template <int EPI, bool DUAL, int BN>
 cudaError_t launch_t2(const GemmParams& p, int clusters, cudaStream_t s) {
-    auto kern = gemm_bf16_tc2<EPI, DUAL>;
+    auto kern = gemm_bf16_tc2<EPI, DUAL, BN>;
     static bool attr_set = false;
     if (!attr_set) {
-        cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, s2_smem_bytes(EPI));
+        cudaError_t e =
+            cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, s2_smem_bytes(EPI, BN));
         if (e != cudaSuccess) return e;
         attr_set = true;
     }
     cudaLaunchConfig_t cfg = {};
     cfg.gridDim = dim3(2 * clusters);
     cfg.blockDim = dim3(s2_threads(EPI));
-    cfg.dynamicSmemBytes = s2_smem_bytes(EPI);
+    cfg.dynamicSmemBytes = s2_smem_bytes(EPI, BN);
     cfg.stream = s;
     cudaLaunchAttribute at[2];
     at[0].id = cudaLaunchAttributeClusterDimension;
@@ -1102,7 +1193,41 @@ cudaError_t launch_t2(const GemmParams& p, int clusters, cudaStream_t s) {
     return cudaLaunchKernelEx(&cfg, kern, p);
 }
 
+template <int EPI>
+cudaError_t launch_t2_bn(const GemmParams& p, int bn, int clusters, cudaStream_t s) {
+    switch (bn) {
+        case 256: return launch_t2<EPI, false, 256>(p, clusters, s);
+        case 224: return launch_t2<EPI, false, 224>(p, clusters, s);
+        case 192: return launch_t2<EPI, false, 192>(p, clusters, s);
+        case 160: return launch_t2<EPI, false, 160>(p, clusters, s);
+    }
+    return cudaErrorInvalidValue;
+}
+
 }  // namespace
+
+// Tile width of a dense pair GEMM. A k-block of a 256 x BN tile costs about the time
+// of BN + 1024 columns: measured on GB300, narrowing the tile from 256 to 160
+// columns shortens a k-block by only ~8 %, because the A operand (the same 16 KB
+// per CTA at any width) and the per-stage synchronisation dominate. The width taken
+// minimises waves x (BN + 1024) over all of the device's CTA pairs: the fewest
+// waves, then the narrowest tile. It depends only on the shape and the device,
+// never on the grid a call is given, so a result's bits do not depend on the grid.
+int gemm_pair_tile_n(int64_t M, int64_t N) {
+    const int64_t clusters = std::max(1, gemm_num_sms() / 2);
+    const int64_t m2 = (M + 255) / 256;
+    int best = 256;
+    int64_t best_cost = INT64_MAX;
+    for (int bn : {256, 224, 192, 160}) {
+        const int64_t tiles = m2 * ((N + bn - 1) / bn);
+        const int64_t cost = ((tiles + clusters - 1) / clusters) * (bn + 1024);
+        if (cost < best_cost) {
+            best_cost = cost;
+            best = bn;
+        }
+    }
+    return best;
+}
 
 int gemm_num_sms() {
     static int n = 0;
@@ -1169,9 +1294,11 @@ cudaError_t launch_gemm_bf16(const GemmDesc& d, int max_ctas, cudaStream_t s) {
     if (!grouped && d.M > BM) {
         // pair-CTA tiles of 256 rows; the choice depends only on the shape, so the
         // bits do not depend on the grid size
+        const int bn2 = dual ? 256 : gemm_pair_tile_n(d.M, d.N);
         if (!cached_tmap(&p.tmA, d.A, d.a_rows > 0 ? d.a_rows : d.M, d.K, d.lda, 128) ||
-            !cached_tmap(&p.tmB, d.B, d.b_rows > 0 ? d.b_rows : d.N, d.K, d.ldb, 128))
+            !cached_tmap(&p.tmB, d.B, d.b_rows > 0 ? d.b_rows : d.N, d.K, d.ldb, dual ? 128 : bn2 / 2))
             return cudaErrorInvalidValue;
+        if (!dual) p.num_n_tiles = (d.N + bn2 - 1) / bn2;
         // output views for the bulk tensor stores (32x32 boxes; clipped at M and N)
         if (!cached_tmap(&p.tmC, MapSpec{d.C, d.M, d.N, d.ldc, 32, 32, 2, 64})) return cudaErrorInvalidValue;
         if (d.C32 && !cached_tmap(&p.tmC32, MapSpec{d.C32, d.M, d.N, d.ldc, 32, 32, 4, 128}))
@@ -1181,11 +1308,11 @@ cudaError_t launch_gemm_bf16(const GemmDesc& d, int max_ctas, cudaStream_t s) {
         if (clusters > pair_tiles) clusters = pair_tiles;
         if (clusters < 1) clusters = 1;
         switch (d.epi) {
-            case EPI_STORE: return launch_t2<EPI_STORE, false>(p, clusters, s);
-            case EPI_BIAS_GELU: return launch_t2<EPI_BIAS_GELU, false>(p, clusters, s);
-            case EPI_BIAS_RESID: return launch_t2<EPI_BIAS_RESID, false>(p, clusters, s);
-            case EPI_RESID: return launch_t2<EPI_RESID, false>(p, clusters, s);
-            case EPI_SWIGLU: return launch_t2<EPI_SWIGLU, true>(p, clusters, s);
+            case EPI_STORE: return launch_t2_bn<EPI_STORE>(p, bn2, clusters, s);
+            case EPI_BIAS_GELU: return launch_t2_bn<EPI_BIAS_GELU>(p, bn2, clusters, s);
+            case EPI_BIAS_RESID: return launch_t2_bn<EPI_BIAS_RESID>(p, bn2, clusters, s);
+            case EPI_RESID: return launch_t2_bn<EPI_RESID>(p, bn2, clusters, s);
+            case EPI_SWIGLU: return launch_t2<EPI_SWIGLU, true, 256>(p, clusters, s);
         }
         return cudaErrorInvalidValue;
     }

@@ -113,6 +113,12 @@ ls_status lsk_gemm_bf16(int32_t epilogue, const void* A, const void* B, int64_t 
     return st(launch_gemm_bf16(d, max_ctas, (cudaStream_t)stream));
 }
 
+int32_t lsk_gemm_tile_n(int32_t epilogue, int32_t M, int32_t N) {
+    if (epilogue < LSK_EPI_STORE || epilogue > LSK_EPI_RESID || M < 1 || N < 1) return 0;
+    if (epilogue == LSK_EPI_SWIGLU) return 128;
+    return M > 128 ? gemm_pair_tile_n(M, N) : 256;
+}
+
 ls_status lsk_gemm_grouped_bf16(int32_t epilogue, const void* A, const void* B, int64_t b_rows, int32_t b_base_row,
                                 int32_t b_group_stride_rows, int32_t b2_row_off, const int32_t* group_bounds,
                                 int32_t n_groups, const int32_t* row_table, const float* row_weight, void* C,

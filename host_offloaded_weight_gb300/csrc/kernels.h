@@ -74,6 +74,8 @@ struct GemmDesc {
 // max_ctas <= 0: one CTA per SM.
 cudaError_t launch_gemm_bf16(const GemmDesc& d, int max_ctas, cudaStream_t s);
 int gemm_num_sms();
+// Tile width (output columns) of the dense pair-CTA GEMM for an M x N output.
+int gemm_pair_tile_n(int64_t M, int64_t N);
 
 // ---------------------------------------------------------------- MoE
 cudaError_t launch_moe_route(const float* logits, int n_layers, int T, int E, int k, int* sel,

@@ -122,6 +122,7 @@ _sig = {
                            C.POINTER(_I32), _I32, _I32, C.POINTER(_I64), C.POINTER(ls_sched_event),
                            _I64, C.POINTER(_I64), C.POINTER(ls_stats), C.POINTER(_I32)]),
     "lsk_num_sms": (_I32, []),
+    "lsk_gemm_tile_n": (_I32, [_I32, _I32, _I32]),
     "lsk_device_error": (_U32, []),
     "lsk_copy_h2slot": (_I32, [_P, _P, _U64, _I32, _P, _P, _U32, _P]),
     "lsk_wait_ready": (_I32, [_P, _U32, _I32, _P, _I32, _P]),
@@ -400,6 +401,11 @@ def ls_simulate_script(params: ls_params, seg_slot_bytes, script, shared=()):
 # ------------------------------------------------------------------ ls_kernels.h
 def lsk_num_sms() -> int:
     return _lib.lsk_num_sms()
+
+
+def lsk_gemm_tile_n(epilogue: int, M: int, N: int) -> int:
+    """Output columns of one tile of lsk_gemm_bf16 for an M x N output on this device."""
+    return _lib.lsk_gemm_tile_n(epilogue, M, N)
 
 
 def lsk_device_error() -> int:

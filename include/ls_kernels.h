@@ -93,6 +93,15 @@ ls_status lsk_gemm_bf16(int32_t epilogue, const void* A_dev, const void* B_dev, 
                         void* C_dev, void* C32_dev, int32_t M, int32_t N, int32_t K, int32_t max_ctas,
                         void* stream);
 
+/* Output columns of one tile of lsk_gemm_bf16 for this shape on the current device:
+ * the pair-CTA GEMM (M > 128, not SWIGLU) takes 256 x W tiles, W in {256, 224, 192,
+ * 160}: the fewest waves of tiles over all of the device's CTA pairs, then the
+ * narrowest tile (a k-block's time is modelled as W + 1024 columns, most of it
+ * independent of W); SWIGLU tiles cover 128 columns of each
+ * matrix, the single-CTA GEMM (M <= 128) 256 columns. Depends only on the shape and
+ * the device, not on max_ctas. Returns 0 for an invalid epilogue or shape. */
+int32_t lsk_gemm_tile_n(int32_t epilogue, int32_t M, int32_t N);
+
 /* Grouped (expert) GEMM: rows of A_dev [M,K] are sorted by group;
  * group g = rows [group_bounds[g], group_bounds[g+1]) multiplies B rows
  * starting at b_base_row + g * b_group_stride_rows (SWIGLU: second matrix

@@ -133,6 +133,66 @@ def test_gemm_bit_identical_across_grid_sizes(ctas):
     assert torch.equal(out.view(torch.int16), ref.view(torch.int16))
 
 
+# Tile widths of the pair GEMM: on a 152-SM device these shapes (ragged M and N) take
+# 256 x 160, 192, 224 and 256 tiles.
+TILE_N_SHAPES = {160: (300, 520, 200), 192: (520, 4008, 200), 224: (520, 4808, 200), 256: (520, 5608, 200)}
+
+
+def test_gemm_tile_widths_cover_every_width():
+    got = {w: L.lsk_gemm_tile_n(L.LSK_EPI_STORE, *TILE_N_SHAPES[w][:2]) for w in TILE_N_SHAPES}
+    assert all(v in (160, 192, 224, 256) for v in got.values())
+    if L.lsk_num_sms() == 152:
+        assert got == {w: w for w in TILE_N_SHAPES}
+    assert L.lsk_gemm_tile_n(L.LSK_EPI_SWIGLU, 4096, 4096) == 128
+    assert L.lsk_gemm_tile_n(L.LSK_EPI_STORE, 128, 4096) == 256   # single-CTA tiles
+    assert L.lsk_gemm_tile_n(9, 4096, 4096) == 0
+
+
+@pytest.mark.parametrize("width", sorted(TILE_N_SHAPES))
+@pytest.mark.parametrize("epi", [L.LSK_EPI_STORE, L.LSK_EPI_BIAS_GELU, L.LSK_EPI_BIAS_RESID, L.LSK_EPI_RESID])
+def test_gemm_tile_widths_vs_oracle(width, epi):
+    M, N, K = TILE_N_SHAPES[width]
+    ab, a = rand_bf16((M, K), 41, 1.0)
+    bb, b = rand_bf16((N, K), 42, 1.0 / np.sqrt(K))
+    biasb, bias = rand_bf16((N,), 43, 0.5)
+    r = np.random.default_rng(44).standard_normal((M, N)).astype(np.float32)
+    C = torch.empty((M, N), dtype=torch.bfloat16, device="cuda")
+    out32 = epi in (L.LSK_EPI_BIAS_RESID, L.LSK_EPI_RESID)
+    C32 = torch.empty((M, N), dtype=torch.float32, device="cuda") if out32 else None
+    L.lsk_gemm_bf16(epi, bf16_dev(ab), bf16_dev(bb), C, M, N, K, bias=bf16_dev(biasb),
+                    resid=torch.from_numpy(r).cuda(), C32=C32)
+    torch.cuda.synchronize()
+    _no_device_error()
+    ref = _gemm_ref(epi, a, b, bias, r.astype(np.float64), 0, N)
+    got = to_f64(C)
+    tol = 2.0 ** -8 * np.abs(ref) + 1e-5 * np.sqrt(K) * np.abs(ref).max()
+    assert np.all(np.abs(got - ref) <= tol), (epi, np.max(np.abs(got - ref) - tol))
+    if out32:
+        got32 = C32.cpu().numpy().astype(np.float64)
+        assert np.max(np.abs(got32 - ref)) <= 1e-5 * np.sqrt(K) * np.abs(ref).max()
+        assert torch.equal(C.cpu(), C32.cpu().to(torch.bfloat16))
+
+
+@pytest.mark.parametrize("width", [160, 224])
+@pytest.mark.parametrize("ctas", [2, 6, 38])
+def test_gemm_tile_widths_bits_independent_of_grid(width, ctas):
+    M, N, K = TILE_N_SHAPES[width]
+    ab, _ = rand_bf16((M, K), 45)
+    bb, _ = rand_bf16((N, K), 46, 0.1)
+    biasb, _ = rand_bf16((N,), 47, 0.5)
+    r = torch.from_numpy(np.random.default_rng(48).standard_normal((M, N)).astype(np.float32)).cuda()
+    A, B, bias = bf16_dev(ab), bf16_dev(bb), bf16_dev(biasb)
+    outs = []
+    for mc in (0, ctas):
+        C = torch.empty((M, N), dtype=torch.bfloat16, device="cuda")
+        C32 = torch.empty((M, N), dtype=torch.float32, device="cuda")
+        L.lsk_gemm_bf16(L.LSK_EPI_BIAS_RESID, A, B, C, M, N, K, bias=bias, resid=r, C32=C32, max_ctas=mc)
+        outs.append((C, C32))
+    torch.cuda.synchronize()
+    assert torch.equal(outs[0][0].view(torch.int16), outs[1][0].view(torch.int16))
+    assert torch.equal(outs[0][1].view(torch.int32), outs[1][1].view(torch.int32))
+
+
 # Longer K with ragged M and N (several waves of k-blocks per tile, partial last tiles).
 LONG_K_SHAPES = [(1000, 1032, 4096), (300, 520, 2048), (4096, 1024, 4000)]
 
