@@ -385,7 +385,8 @@ def run_ours(args, cfg, world, rank, local):
         "gpu_launches": launches,
         "step_ms": {"min": min(step_ms), "median": statistics.median(step_ms), "max": max(step_ms),
                     "all": [round(v, 4) for v in step_ms]},
-        "kernel_times_from": "a second set of the same K passes with per-launch CUDA events "
+        "kernel_times_from": "a second set of the same K passes with per-launch CUDA events and no "
+                             "programmatic dependent launch "
                              f"(mean {statistics.mean(step_ms_kt):.4f} ms per pass with the events)",
         "clocks": {k: clocks[k] for k in ("sm_mhz", "sm_max_mhz", "reasons")},
         "e2e": {"value": e2e_tokens / e2e_max, "unit": UNIT, "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h},

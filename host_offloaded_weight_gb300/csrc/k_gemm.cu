@@ -82,6 +82,7 @@ struct GemmParams {
     const float* row_weight;
     uint32_t* err;
     uint64_t mbar_limit_ns;  // bound of every internal mbarrier wait
+    int pdl;                 // host side: launch with programmatic stream serialization
 };
 
 // ------------------------------------------------------------------ PTX helpers
@@ -1162,7 +1163,7 @@ cudaError_t launch_t(const GemmParams& p, int grid, cudaStream_t s) {
     at[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
     at[0].val.programmaticStreamSerializationAllowed = 1;
     cfg.attrs = at;
-    cfg.numAttrs = 1;
+    cfg.numAttrs = p.pdl ? 1 : 0;
     return cudaLaunchKernelEx(&cfg, kern, p);
 }
 
@@ -1189,7 +1190,7 @@ cudaError_t launch_t2(const GemmParams& p, int clusters, cudaStream_t s) {
     at[1].id = cudaLaunchAttributeProgrammaticStreamSerialization;
     at[1].val.programmaticStreamSerializationAllowed = 1;
     cfg.attrs = at;
-    cfg.numAttrs = 2;
+    cfg.numAttrs = p.pdl ? 2 : 1;
     return cudaLaunchKernelEx(&cfg, kern, p);
 }
 
@@ -1283,6 +1284,7 @@ cudaError_t launch_gemm_bf16(const GemmDesc& d, int max_ctas, cudaStream_t s) {
     p.row_weight = d.row_weight;
     p.err = d.err_word;
     p.mbar_limit_ns = MBAR_LIMIT_NS;
+    p.pdl = d.pdl ? 1 : 0;
     int tiles = p.num_tiles;
     if (grouped) {
         // sum over groups of ceil(rows/BM) <= M/BM + n_groups

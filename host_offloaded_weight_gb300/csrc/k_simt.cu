@@ -66,7 +66,7 @@ linear_gelu_f32_kernel(const float* __restrict__ x, const float* __restrict__ w,
 }
 
 cudaError_t launch_linear_gelu_f32(const float* x, const float* w, const float* b, float* y, int T,
-                                   int H, int F, cudaStream_t s) {
+                                   int H, int F, cudaStream_t s, bool pdl) {
     if (T <= 0) return cudaSuccess;
     size_t smem = (size_t)SIMT_MAX_T * H * sizeof(float);
     if (smem > 200 * 1024) return cudaErrorInvalidValue;
@@ -86,7 +86,7 @@ cudaError_t launch_linear_gelu_f32(const float* x, const float* w, const float* 
     at[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
     at[0].val.programmaticStreamSerializationAllowed = 1;
     cfg.attrs = at;
-    cfg.numAttrs = 1;
+    cfg.numAttrs = pdl ? 1 : 0;
     return cudaLaunchKernelEx(&cfg, linear_gelu_f32_kernel, x, w, b, y, T, H, F);
 }
 

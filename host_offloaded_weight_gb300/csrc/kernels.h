@@ -30,7 +30,7 @@ bool publish_needs_no_sm();
 
 // ---------------------------------------------------------------- fp32 linear + GELU
 cudaError_t launch_linear_gelu_f32(const float* x, const float* w, const float* b, float* y, int T,
-                                   int H, int F, cudaStream_t s);
+                                   int H, int F, cudaStream_t s, bool pdl = true);
 
 // ---------------------------------------------------------------- tcgen05 GEMM
 enum GemmEpilogue : int {
@@ -69,6 +69,9 @@ struct GemmDesc {
     const float* row_weight = nullptr;  // EPI_SCALE_F32: weight by destination row
     int max_tiles_hint = 0;             // grouped: upper bound of tiles (grid sizing)
     uint32_t* err_word = nullptr;       // mapped host word for internal timeouts
+    // programmatic dependent launch: the prologue overlaps the previous kernel's tail.
+    // Off where events bracket each launch, so that an event pair times this kernel alone.
+    bool pdl = true;
 };
 
 // max_ctas <= 0: one CTA per SM.

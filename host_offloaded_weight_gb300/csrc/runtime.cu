@@ -376,6 +376,10 @@ void compute_segment(ls_ctx* c, const RunCtx& rc, int seg, bool wait) {
     const int slot = c->seg_slot[seg];
     const uint32_t epoch = c->seg_epoch[seg];
     const uint32_t code = DERR_HANDOFF_TIMEOUT | ((uint32_t)slot << 8);
+    // Kernels overlap their prologue with the previous kernel's tail (programmatic
+    // dependent launch) except while events bracket each launch: an event pair then
+    // times its kernel alone.
+    const bool pdl = !c->prm.kernel_timing;
     // A prefetched segment's kernels start behind a one-CTA wait on the slot's
     // ready word. The wait is its own launch: a spinning waiter must hold almost
     // nothing, so the copy it waits for can always find SMs to run on.
@@ -385,18 +389,19 @@ void compute_segment(ls_ctx* c, const RunCtx& rc, int seg, bool wait) {
         // SM (no copy or publish kernel that the placed CTAs could starve; device-to-device
         // copies of the expert cache may run as kernels too)
         const bool early = c->copy_path == LS_COPY_ENGINE && publish_needs_no_sm() &&
-                           (!c->capturing || c->capture_stream_ops) && c->ecache_K == 0;
+                           (!c->capturing || c->capture_stream_ops) && c->ecache_K == 0 && pdl;
         track(c, launch_wait_ready(c->ready + slot, epoch, rc.wait_ns, c->err_word_dev, code, rc.s, early));
     };
     GemmDesc w0;
     w0.err_word = c->err_word_dev;
+    w0.pdl = pdl;
     const int ctas = gemm_ctas(c);
     switch (c->kind) {
         case LS_KIND_LINEAR_GELU_F32: {
             if (wait) wait_slot();
             KTime kt(c, "linear_gelu_f32", rc.s);
             track(c, launch_linear_gelu_f32((const float*)xin, (const float*)tptr(c, seg, 0),
-                                            (const float*)tptr(c, seg, 1), (float*)xout, T, H, F, rc.s));
+                                            (const float*)tptr(c, seg, 1), (float*)xout, T, H, F, rc.s, pdl));
             break;
         }
         case LS_KIND_FFN_GELU_BF16:
@@ -407,6 +412,7 @@ void compute_segment(ls_ctx* c, const RunCtx& rc, int seg, bool wait) {
             if (proj) {  // reads only the resident shared projection: runs before the wait
 
                 GemmDesc g;
+                g.pdl = pdl;
                 g.epi = EPI_STORE;
                 g.A = xin; g.lda = H; g.a_rows = T;
                 g.B = tptr(c, seg, 0); g.ldb = H; g.b_rows = H;

@@ -117,7 +117,9 @@ typedef struct ls_params {
     int32_t test_fail_async;      /* the first prefetch finds asynchronous transfer unavailable */
     int32_t test_drop_publish;    /* the Nth publish (1-based, over the context's life) leaves its ready word down */
     int32_t kernel_timing;        /* 1 = bracket every launch with CUDA events (see ls_get_kernel_times);
-                                     2 = also keep a per-launch trace (see ls_get_trace) */
+                                     2 = also keep a per-launch trace (see ls_get_trace). Launches
+                                     then run without programmatic dependent launch, so that each
+                                     event pair times its kernel alone */
     int32_t cross_run_prefetch;   /* 1 = the prefetch window crosses the run boundary: the last steps of
                                      a run also queue the next run's first streamed segments (when the
                                      ring is a full depth + 1 slots; never for the MoE kind, whose next
@@ -281,10 +283,11 @@ ls_status ls_get_schedule(ls_ctx* ctx, ls_sched_event* out, int64_t cap, int64_t
 ls_status ls_get_stats(ls_ctx* ctx, ls_stats* out);
 
 /* Switch per-launch timing (the kernel_timing field of ls_params: 0, 1 or 2)
- * for the passes issued from now on. Event records between launches cost the
- * stream a little time and keep consecutive GEMMs from overlapping their
- * start-up, so a throughput measurement runs with timing off and a separate
- * set of passes collects the per-kernel times. LS_ERR_STATE while passes issued
+ * for the passes issued from now on. With timing on, kernels launch without
+ * programmatic dependent launch (a kernel placed early would otherwise start its
+ * event pair while the kernel before it still runs), and event records between
+ * launches cost the stream a little time, so a throughput measurement runs with
+ * timing off and a separate set of passes collects the per-kernel times. LS_ERR_STATE while passes issued
  * by ls_run_async have not been collected by ls_sync; LS_ERR_INVALID_ARG for a
  * mode outside 0..2. The pages define no such call: it is instrumentation. */
 ls_status ls_set_kernel_timing(ls_ctx* ctx, int32_t mode);
