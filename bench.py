@@ -234,6 +234,37 @@ def ce_link_peak(torch, nbytes=1 << 30, reps=10) -> float:
     return nbytes / (best * 1e-3) / 1e9
 
 
+def write_timeline(path, L, ctx, x, y, T, s, logits, cfg):
+    """Two back-to-back passes with events around every copy and around each segment's
+    compute kernels after its hand-off wait (launches keep programmatic dependent
+    launch); the second pass per segment, in ms from its first event, with how busy the
+    copy stream and the compute stream were."""
+    L.ls_set_kernel_timing(ctx, 3)
+    for _ in range(2):
+        L.ls_run_async(ctx, x, y, T, s, logits=logits, top_k=cfg.top_k)
+    L.ls_sync(ctx)
+    trace = L.ls_get_trace(ctx)
+    L.ls_set_kernel_timing(ctx, 0)
+    L.ls_get_kernel_times(ctx, reset=True)
+    second = trace[len(trace) // 2:]      # both passes record the same spans, in order
+    t0 = min(e[3] for e in second)
+    by_seg = {}
+    for name, stream, seg, a, b in second:
+        by_seg.setdefault(seg, []).append((name, stream, a - t0, b - t0))
+    span = max(e[4] for e in second) - t0
+    busy = {0: 0.0, 1: 0.0}
+    for name, stream, seg, a, b in second:
+        busy[stream] += b - a
+    with open(path, "w") as f:
+        f.write(f"# {cfg.name}: one pass (ms from its first event)\n")
+        f.write(f"# span {span:.3f} ms; copy stream busy {busy[1]:.3f} ms ({100 * busy[1] / span:.1f} %), "
+                f"compute kernels busy {busy[0]:.3f} ms ({100 * busy[0] / span:.1f} %)\n")
+        f.write("segment | span | stream | start | end | ms\n")
+        for seg in sorted(by_seg):
+            for name, stream, a, b in sorted(by_seg[seg], key=lambda e: e[2]):
+                f.write(f"{seg} | {name} | {'copy' if stream else 'compute'} | {a:.3f} | {b:.3f} | {b - a:.3f}\n")
+
+
 def run_ours(args, cfg, world, rank, local):
     import torch
     from host_offloaded_weight_gb300 import lstream as L
@@ -316,6 +347,8 @@ def run_ours(args, cfg, world, rank, local):
     step_ms_kt = timed_passes()
     ktimes = L.ls_get_kernel_times(ctx, reset=True)
     L.ls_set_kernel_timing(ctx, 0)
+    if args.timeline and rank == 0:
+        write_timeline(args.timeline, L, ctx, x, y, T, s, logits, cfg)
     clocks = sampler.stop()
     mean_s = statistics.mean(step_ms) / 1e3
     stats = L.ls_get_stats(ctx)
@@ -452,6 +485,9 @@ def main() -> int:
                     help="let the prefetch window cross the pass boundary (off by default, as in the pages)")
     ap.add_argument("--max-vram-bytes", type=int, default=None,
                     help="override the workload's parameter budget (e.g. a one-slot run)")
+    ap.add_argument("--timeline", default=None, metavar="FILE",
+                    help="after the measurement, trace two more passes (events around every copy and "
+                         "around each segment's compute kernels) and write the second one's timeline to FILE")
     args = ap.parse_args()
     if args.warmup < 3:
         ap.error("--warmup must be at least 3")

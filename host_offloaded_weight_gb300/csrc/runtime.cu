@@ -22,6 +22,7 @@
 #include <cstring>
 #include <map>
 #include <new>
+#include <optional>
 #include <string>
 #include <vector>
 
@@ -209,13 +210,22 @@ inline void track(ls_ctx* c, cudaError_t e) {
     if (e != cudaSuccess && c->cuda_err == cudaSuccess) c->cuda_err = e;
 }
 
-// Bracket one launch with events on its own stream (only with kernel_timing on).
+// Bracket one launch with events on its own stream (only with kernel_timing on). Modes
+// 1 and 2 bracket every launch; mode 3 brackets only the copies and, per segment, the
+// compute kernels after the hand-off wait as one "compute" span.
+inline bool ktime_on(const ls_ctx* c, const char* name) {
+    const int m = c->prm.kernel_timing;
+    const bool segment_span = strcmp(name, "compute") == 0;
+    if (m == 1 || m == 2) return !segment_span;
+    if (m == 3) return segment_span || strncmp(name, "copy_", 5) == 0;
+    return false;
+}
 struct KTime {
     ls_ctx* c;
     cudaStream_t s;
     size_t idx = (size_t)-1;
     KTime(ls_ctx* ctx, const char* name, cudaStream_t st) : c(ctx), s(st) {
-        if (!c->prm.kernel_timing) return;
+        if (!ktime_on(c, name)) return;
         int cls = -1;
         for (size_t i = 0; i < c->tclass.size(); ++i)
             if (c->tclass[i].name == name) cls = (int)i;
@@ -253,7 +263,8 @@ struct KTime {
 
 // After the run's final synchronisation: fold the recorded pairs into the classes.
 void collect_times(ls_ctx* c) {
-    if (c->prm.kernel_timing >= 2) c->trace.clear();
+    const bool tracing = c->prm.kernel_timing >= 2;
+    if (tracing) c->trace.clear();
     for (size_t i = 0; i < c->tev_used; ++i) {
         float ms = 0;
         if (cudaEventElapsedTime(&ms, c->tev[i].first, c->tev[i].second) == cudaSuccess) {
@@ -262,7 +273,7 @@ void collect_times(ls_ctx* c) {
         } else {
             cudaGetLastError();
         }
-        if (c->prm.kernel_timing >= 2) {
+        if (tracing) {
             ls_trace_event t{};
             snprintf(t.name, sizeof(t.name), "%s", c->tclass[c->tev_class[i]].name.c_str());
             t.stream = c->tev_stream[i];
@@ -377,9 +388,13 @@ void compute_segment(ls_ctx* c, const RunCtx& rc, int seg, bool wait) {
     const uint32_t epoch = c->seg_epoch[seg];
     const uint32_t code = DERR_HANDOFF_TIMEOUT | ((uint32_t)slot << 8);
     // Kernels overlap their prologue with the previous kernel's tail (programmatic
-    // dependent launch) except while events bracket each launch: an event pair then
-    // times its kernel alone.
-    const bool pdl = !c->prm.kernel_timing;
+    // dependent launch) except while events bracket each launch (timing modes 1 and 2):
+    // an event pair then times its kernel alone.
+    const bool pdl = c->prm.kernel_timing == 0 || c->prm.kernel_timing == 3;
+    std::optional<KTime> span;  // mode 3: the segment's compute kernels after the hand-off wait
+    auto open_span = [&]() {
+        if (c->prm.kernel_timing == 3 && !span) span.emplace(c, "compute", rc.s);
+    };
     // A prefetched segment's kernels start behind a one-CTA wait on the slot's
     // ready word. The wait is its own launch: a spinning waiter must hold almost
     // nothing, so the copy it waits for can always find SMs to run on.
@@ -391,11 +406,13 @@ void compute_segment(ls_ctx* c, const RunCtx& rc, int seg, bool wait) {
         const bool early = c->copy_path == LS_COPY_ENGINE && publish_needs_no_sm() &&
                            (!c->capturing || c->capture_stream_ops) && c->ecache_K == 0 && pdl;
         track(c, launch_wait_ready(c->ready + slot, epoch, rc.wait_ns, c->err_word_dev, code, rc.s, early));
+        open_span();
     };
     GemmDesc w0;
     w0.err_word = c->err_word_dev;
     w0.pdl = pdl;
     const int ctas = gemm_ctas(c);
+    if (!wait) open_span();
     switch (c->kind) {
         case LS_KIND_LINEAR_GELU_F32: {
             if (wait) wait_slot();
@@ -630,7 +647,7 @@ ls_status check_params(const ls_params* p, ls_params* out, std::string* why) {
     }
     if (d.copy_path < LS_COPY_AUTO || d.copy_path > LS_COPY_ENGINE) { *why = "bad copy_path"; return LS_ERR_INVALID_ARG; }
     if (d.copy_ctas < 0 || d.test_alloc_cap_bytes < 0 || d.test_drop_publish < 0 || d.kernel_timing < 0 ||
-        d.kernel_timing > 2) {
+        d.kernel_timing > 3) {
         *why = "negative count";
         return LS_ERR_INVALID_ARG;
     }
@@ -1551,7 +1568,7 @@ ls_status ls_get_trace(ls_ctx* c, ls_trace_event* out, int64_t cap, int64_t* n_o
 }
 
 ls_status ls_set_kernel_timing(ls_ctx* c, int32_t mode) {
-    if (!c || mode < 0 || mode > 2) return LS_ERR_INVALID_ARG;
+    if (!c || mode < 0 || mode > 3) return LS_ERR_INVALID_ARG;
     if (!c->pending.empty()) {
         set_err(c, "ls_set_kernel_timing: passes are queued; call ls_sync first");
         return LS_ERR_STATE;

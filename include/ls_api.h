@@ -119,7 +119,10 @@ typedef struct ls_params {
     int32_t kernel_timing;        /* 1 = bracket every launch with CUDA events (see ls_get_kernel_times);
                                      2 = also keep a per-launch trace (see ls_get_trace). Launches
                                      then run without programmatic dependent launch, so that each
-                                     event pair times its kernel alone */
+                                     event pair times its kernel alone.
+                                     3 = trace only the copies and, per segment, one "compute" span
+                                     from the end of the hand-off wait to the segment's last kernel;
+                                     launches keep programmatic dependent launch */
     int32_t cross_run_prefetch;   /* 1 = the prefetch window crosses the run boundary: the last steps of
                                      a run also queue the next run's first streamed segments (when the
                                      ring is a full depth + 1 slots; never for the MoE kind, whose next
@@ -282,14 +285,14 @@ ls_status ls_get_schedule(ls_ctx* ctx, ls_sched_event* out, int64_t cap, int64_t
 /* Counters and the current plan. out->struct_size must be set by the caller. */
 ls_status ls_get_stats(ls_ctx* ctx, ls_stats* out);
 
-/* Switch per-launch timing (the kernel_timing field of ls_params: 0, 1 or 2)
+/* Switch per-launch timing (the kernel_timing field of ls_params: 0 to 3)
  * for the passes issued from now on. With timing on, kernels launch without
  * programmatic dependent launch (a kernel placed early would otherwise start its
  * event pair while the kernel before it still runs), and event records between
  * launches cost the stream a little time, so a throughput measurement runs with
  * timing off and a separate set of passes collects the per-kernel times. LS_ERR_STATE while passes issued
  * by ls_run_async have not been collected by ls_sync; LS_ERR_INVALID_ARG for a
- * mode outside 0..2. The pages define no such call: it is instrumentation. */
+ * mode outside 0..3. The pages define no such call: it is instrumentation. */
 ls_status ls_set_kernel_timing(ls_ctx* ctx, int32_t mode);
 
 /* One pass, like ls_run_async, issued as a CUDA graph: the first steady-state

@@ -329,8 +329,19 @@ def test_kernel_timing_switch():
         assert kt["gemm_up"][0] == cfg.n_segments and kt["gemm_down"][0] == cfg.n_segments
         assert all(ms > 0 for _, ms in kt.values())
         assert torch.equal(y0.view(torch.int16), y1.view(torch.int16))
+        # segment spans: the copies and one compute span per segment, the same bits again
+        y2 = torch.empty_like(x)
+        L.ls_set_kernel_timing(ctx, 3)
+        L.ls_run(ctx, x, y2, cfg.tokens)
+        tr = L.ls_get_trace(ctx)
+        kt = {k: v for k, v in L.ls_get_kernel_times(ctx, reset=True).items() if v[0] > 0}
+        assert kt["compute"][0] == cfg.n_segments and set(kt) <= {"compute", "copy_engine", "copy_h2slot"}
+        spans = [e for e in tr if e[0] == "compute"]
+        assert [e[2] for e in spans] == list(range(cfg.n_segments)) and all(e[1] == 0 for e in spans)
+        assert all(e[4] >= e[3] for e in tr)
+        assert torch.equal(y0.view(torch.int16), y2.view(torch.int16))
         with pytest.raises(L.LsError):
-            L.ls_set_kernel_timing(ctx, 3)
+            L.ls_set_kernel_timing(ctx, 4)
     finally:
         L.ls_ctx_destroy(ctx)
 
