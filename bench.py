@@ -62,6 +62,23 @@ def kernel_flops(cfg, tokens) -> dict:
     return {"gemm_up": 2.0 * T * H * F, "gemm_down": 2.0 * T * H * F, "gemm_proj": 2.0 * T * H * H}
 
 
+def kernel_bytes(cfg, tokens, routed=None) -> dict:
+    """Algorithmic bytes one launch reads and writes: operands, bias, residual and outputs
+    once each (bf16 = 2 B, fp32 = 4 B). routed = experts a MoE layer moves (default all)."""
+    T, H, F = tokens, cfg.hidden, cfg.ffn
+    if cfg.kind == synth.KIND_MOE_SWIGLU_BF16:
+        e = cfg.n_experts if routed is None else routed
+        rows = T * cfg.top_k
+        return {"gemm_up": 2 * (rows * H + e * 2 * F * H + rows * F),
+                "gemm_down": 2 * (rows * F + e * H * F) + 4 * rows * H}
+    up_b = 2 * F * H * (2 if cfg.kind == synth.KIND_SWIGLU_BF16 else 1)
+    out = {"gemm_up": 2 * T * H + up_b + 2 * F + 2 * T * F,
+           "gemm_down": 2 * T * F + 2 * H * F + 2 * H + 4 * T * H + 2 * T * H + 4 * T * H}
+    if cfg.kind != synth.KIND_SWIGLU_BF16:
+        out["gemm_proj"] = 2 * T * H + 2 * H * H + 2 * T * H
+    return out
+
+
 def measured_peaks() -> tuple:
     path = os.path.join(ROOT, "MEASURED_PEAKS.json")
     try:
@@ -382,6 +399,10 @@ def run_ours(args, cfg, world, rank, local):
     dominant = max(kernels_only, key=lambda k: kt[k]["total_ms"]) if kernels_only else None
     kf = kernel_flops(cfg, T)
     per_load = link_bytes / max(1, sum(1 for e in sched if e[2] in (L.LS_EV_PREFETCH, L.LS_EV_LOAD_SYNC)) / args.steps)
+    routed = None
+    if cfg.kind == synth.KIND_MOE_SWIGLU_BF16:   # experts a streamed layer moves, on average
+        routed = per_load / (sum(t.nbytes for t in synth.segment_tensors(cfg)) / cfg.n_experts)
+    kb = kernel_bytes(cfg, T, routed)
     def roof(name):
         if name in ("copy_h2slot", "copy_engine"):
             ach = per_load / (kt[name]["avg_ms"] * 1e-3) / 1e9
@@ -395,7 +416,15 @@ def run_ours(args, cfg, world, rank, local):
                     "frac": ach / peak, "traffic": TRAFFIC.get((cfg.name, name)),
                     "peak_source": "fp32 FMA lanes x clock (152 x 128 x 2 x 2.07 GHz)"}
         if name in kf:
-            ach = kf[name] / (kt[name]["avg_ms"] * 1e-3) / 1e12
+            # below the ridge (FLOP per byte under peak FLOP/s over peak bytes/s) a launch is
+            # bound by HBM: the MoE layers' expert GEMMs, ~128 rows per expert
+            sec = kt[name]["avg_ms"] * 1e-3
+            if kf[name] / kb[name] < tc_peak * 1e12 / (hbm_peak * 1e9):
+                ach = kb[name] / sec / 1e9
+                return {"kernel": name, "bound": "hbm", "achieved": ach, "peak": hbm_peak, "unit": "GB/s",
+                        "frac": ach / hbm_peak, "traffic": TRAFFIC.get((cfg.name, name)),
+                        "algorithmic_bytes": kb[name], "peak_source": f"hbm_gbs ({peak_src})"}
+            ach = kf[name] / sec / 1e12
             return {"kernel": name, "bound": "tensor", "achieved": ach, "peak": tc_peak, "unit": "TFLOP/s",
                     "frac": ach / tc_peak, "traffic": TRAFFIC.get((cfg.name, name)),
                     "peak_source": f"bf16_tflops ({peak_src})"}

@@ -20,9 +20,9 @@
 // one thread from one fixed-order accumulation, so results do not depend on
 // the grid size or on where the weights live.
 //
-// Dense GEMMs with more than 128 rows use the pair-CTA form below (256x256 tiles
-// over a 2-CTA cluster); single-CTA 128x256 tiles serve the grouped mode and
-// short problems.
+// Dense GEMMs with more than 128 rows use the pair-CTA form below (256 x W tiles
+// over a 2-CTA cluster, W in {256, 224, 192, 160} chosen per shape, 10 or 18
+// warps); single-CTA 128x256 tiles serve the grouped mode and short problems.
 //
 // Grouped mode (expert GEMM of the MoE stack): rows of A are already sorted by
 // expert; group g owns rows [group_bounds[g], group_bounds[g+1]) and reads its
