@@ -484,10 +484,14 @@ def run_ours(args, cfg, world, rank, local):
 
 
 # DRAM bytes (read + write) per launch from ncu captures of the current kernels
-# (profiles/gemm_pair_dit_ffn_12x1024x4096.md); absent = not captured.
+# (profiles/gemm_pair_*.md); absent = not captured.
 TRAFFIC: dict = {
     ("dit_ffn_12x1024x4096", "gemm_up"): 16_812_800 + 527_360,
     ("dit_ffn_12x1024x4096", "gemm_down"): 50_413_312 + 2_203_648,
+    # profiles/gemm_pair_shared_proj_24x3072x12288.md
+    ("shared_proj_24x3072x12288", "gemm_proj"): 31_478_528 + 65_792,
+    ("shared_proj_24x3072x12288", "gemm_up"): 88_222_464 + 26_256_384,
+    ("shared_proj_24x3072x12288", "gemm_down"): 196_126_976 + 24_913_920,
 }
 
 
