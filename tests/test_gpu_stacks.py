@@ -291,6 +291,29 @@ def test_mandatory_slot_warning():
         L.ls_ctx_destroy(ctx)
 
 
+@pytest.mark.parametrize("name", ["ffn", "swiglu"])
+def test_token_count_changes_between_runs(name):
+    """One context runs passes of 1 to 300 tokens in turn: single-CTA tiles below 129
+    rows, pair tiles above, the workspaces regrown for the longest; rows are independent,
+    so each pass matches the oracle's first T rows. A pass of no tokens is refused."""
+    cfg = SMALL[name]
+    hs = synth.HostStack(cfg)
+    ref = ostack.stack_forward(cfg)
+    ctx, _ = make_ctx(cfg, hs)
+    try:
+        x = x_dev(cfg)
+        for T in [t for t in (1, 129, 64, cfg.tokens, 257, 2) if t <= cfg.tokens]:
+            y = torch.empty_like(x[:T])
+            L.ls_run(ctx, x[:T].contiguous(), y, T)
+            torch.cuda.synchronize()
+            assert rel_err(to_f64(y), ref[:T]) <= BOUND, (name, T)
+        with pytest.raises(L.LsError) as e:
+            L.ls_run(ctx, x, torch.empty_like(x), 0)
+        assert e.value.status == L.LS_ERR_INVALID_ARG
+    finally:
+        L.ls_ctx_destroy(ctx)
+
+
 def test_run_host_matches_run():
     cfg = SMALL["proj"]
     hs = synth.HostStack(cfg)
