@@ -314,6 +314,30 @@ def test_token_count_changes_between_runs(name):
         L.ls_ctx_destroy(ctx)
 
 
+def test_two_contexts_interleaved():
+    """Two contexts with different stacks, their passes interleaved on one stream: each
+    gives the bits it gives alone (the GEMMs' descriptor and attribute caches are shared
+    by all contexts of the process)."""
+    cfgs = [SMALL["ffn"], SMALL["swiglu"]]
+    hss = [synth.HostStack(c) for c in cfgs]
+    alone = [_bits(_run(c, h, runs=1)[0]) for c, h in zip(cfgs, hss)]
+    ctxs = [make_ctx(c, h)[0] for c, h in zip(cfgs, hss)]
+    try:
+        xs = [x_dev(c) for c in cfgs]
+        for _ in range(2):
+            ys = [torch.empty_like(x) for x in xs]
+            for i in (0, 1):
+                L.ls_run_async(ctxs[i], xs[i], ys[i], cfgs[i].tokens)
+            for i in (0, 1):
+                L.ls_sync(ctxs[i])
+            torch.cuda.synchronize()
+            for i in (0, 1):
+                assert np.array_equal(_bits(ys[i]), alone[i]), i
+    finally:
+        for c in ctxs:
+            L.ls_ctx_destroy(c)
+
+
 def test_run_host_matches_run():
     cfg = SMALL["proj"]
     hs = synth.HostStack(cfg)
