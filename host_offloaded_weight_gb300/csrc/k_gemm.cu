@@ -247,8 +247,9 @@ __device__ __forceinline__ Tile tile_of(const GemmParams& p, int t, const int* s
         r.n0 = n * BN;
         r.b_row = r.n0;
     } else {
-        int total_m = s_mt_prefix[p.n_groups];
-        int mt = t % total_m, n = t / total_m;
+        // column tiles innermost: the CTAs of one wave share each row tile of A (read once
+        // from DRAM instead of once per column tile) and a group's row tiles of B
+        int n = t % p.num_n_tiles, mt = t / p.num_n_tiles;
         int lo = 0, hi = p.n_groups - 1;  // last group g with prefix[g] <= mt
         while (lo < hi) {
             int mid = (lo + hi + 1) >> 1;
