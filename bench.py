@@ -363,6 +363,12 @@ def run_ours(args, cfg, world, rank, local):
     L.ls_get_kernel_times(ctx, reset=True)
     step_ms_kt = timed_passes()
     ktimes = L.ls_get_kernel_times(ctx, reset=True)
+    # segment compute spans: the same K passes with events only around each segment's
+    # compute kernels (after the hand-off wait) and the copies; launches keep programmatic
+    # dependent launch, so a span shows the kernels as the throughput passes run them
+    L.ls_set_kernel_timing(ctx, 3)
+    timed_passes()
+    spans = L.ls_get_kernel_times(ctx, reset=True)
     L.ls_set_kernel_timing(ctx, 0)
     if args.timeline and rank == 0:
         write_timeline(args.timeline, L, ctx, x, y, T, s, logits, cfg)
@@ -430,6 +436,16 @@ def run_ours(args, cfg, world, rank, local):
                     "peak_source": f"bf16_tflops ({peak_src})"}
         return None
     roofline = roof(dominant) if dominant else None
+    # the dense stacks' segment compute as the throughput passes run it (GEMMs back to back
+    # with programmatic dependent launch, the next segment's copy running meanwhile)
+    segment_compute = None
+    if cfg.kind in (synth.KIND_FFN_GELU_BF16, synth.KIND_SWIGLU_BF16) and spans.get("compute", (0, 0))[0]:
+        n_sp, ms_sp = spans["compute"]
+        ach = seg_flops(cfg, T) / (ms_sp / n_sp * 1e-3) / 1e12
+        segment_compute = {"spans": n_sp, "avg_ms": ms_sp / n_sp, "achieved": ach, "peak": tc_peak,
+                           "unit": "TFLOP/s", "frac": ach / tc_peak,
+                           "what": "both GEMMs of a segment, CUDA events from the end of its hand-off "
+                                   "wait to its last kernel, launches with programmatic dependent launch"}
     gemm_name = "gemm_down" if "gemm_down" in kt else None
     line = {
         "metric": METRIC, "value": value, "unit": UNIT, "n_gpus": world, "steps": args.steps,
@@ -455,6 +471,7 @@ def run_ours(args, cfg, world, rank, local):
         "bytes_per_step": link_bytes, "flops_per_step": flops,
         "roofline": roofline,
         "roofline_gemm": roof(gemm_name) if gemm_name else None,
+        "segment_compute": segment_compute,
         "kernels": kt,
         "gpu_launches": launches,
         "step_ms": {"min": min(step_ms), "median": statistics.median(step_ms), "max": max(step_ms),
