@@ -1210,8 +1210,9 @@ cudaError_t launch_t2_bn(const GemmParams& p, int bn, int clusters, cudaStream_t
 
 // Tile width of a dense pair GEMM. A k-block of a 256 x BN tile costs about the time
 // of BN + 1024 columns: measured on GB300, narrowing the tile from 256 to 160
-// columns shortens a k-block by only ~8 %, because the A operand (the same 16 KB
-// per CTA at any width) and the per-stage synchronisation dominate. The width taken
+// columns shortens a k-block by only ~8 %; the MMAs set the pace (with the loads
+// taken out the loop is <10 % faster) and a 160-wide instruction runs at ~75 % of
+// the 256-wide one's rate. The width taken
 // minimises waves x (BN + 1024) over all of the device's CTA pairs: the fewest
 // waves, then the narrowest tile. It depends only on the shape and the device,
 // never on the grid a call is given, so a result's bits do not depend on the grid.
