@@ -1,4 +1,4 @@
-"""The bench's per-launch FLOP and byte model, against hand counts (no GPU)."""
+"""The bench's per-launch FLOP and byte model against hand counts, and its reference arm (no GPU)."""
 import bench
 import synth
 
@@ -39,3 +39,27 @@ def test_moe_expert_gemms_sit_below_the_ridge():
     # fewer routed experts move fewer weight bytes; the row traffic stays
     kb_half = bench.kernel_bytes(cfg, T, routed=E / 2)
     assert kb_all["gemm_up"] - kb_half["gemm_up"] == 2 * (E / 2) * 2 * F * H
+
+
+def test_reference_arm_line():
+    """`bench.py --impl reference` on the host: one JSON line with the contract's keys, the
+    oracle as the timed program, the line's own value as its cpu_baseline and e2e."""
+    import json
+    import os
+    import subprocess
+    import sys
+    root = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
+    out = subprocess.run([sys.executable, "bench.py", "--impl", "reference", "--steps", "1", "--warmup", "3",
+                          "--ref-tokens", "8", "--workload", "tiny_f32_4x256"],
+                         cwd=root, capture_output=True, text=True, timeout=600)
+    assert out.returncode == 0, out.stderr[-2000:]
+    lines = [l for l in out.stdout.splitlines() if l.startswith("{")]
+    assert len(lines) == 1
+    d = json.loads(lines[0])
+    for key in ("impl", "metric", "value", "unit", "n_gpus", "steps", "warmup", "ms_per_step",
+                "higher_is_better", "scaling", "vs_baseline", "dtype", "data", "config", "cpu_baseline", "e2e"):
+        assert key in d, key
+    assert d["impl"] == "reference" and d["value"] > 0 and d["steps"] == 1
+    assert d["cpu_baseline"]["kind"] == "oracle" and d["cpu_baseline"]["value"] == d["value"]
+    assert d["e2e"]["value"] == d["value"] and d["e2e"]["h2d_bytes_per_step"] == 0
+    assert d["config"]["workload"] == "tiny_f32_4x256"
