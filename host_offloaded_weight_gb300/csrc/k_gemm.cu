@@ -64,6 +64,7 @@ struct GemmParams {
     CUtensorMap tmB;
     CUtensorMap tmC;    // pair kernel: bf16 output, 32x32 box, 64-byte swizzle
     CUtensorMap tmC32;  // pair kernel: fp32 output copy, 32x32 box, 128-byte swizzle
+    CUtensorMap tmB2;   // grouped: a second B view (the expert cache), same row pitch and box
     int M, N, K;
     int num_m_tiles, num_n_tiles, num_k_blocks, num_tiles;
     int b2_row_off;
@@ -80,6 +81,7 @@ struct GemmParams {
     int b_base_row;
     const int* row_table;
     const float* row_weight;
+    const int* group_b_row;  // grouped, optional: first B row of group g's matrix; top bit set = in tmB2
     uint32_t* err;
     uint64_t mbar_limit_ns;  // bound of every internal mbarrier wait
     int pdl;                 // host side: launch with programmatic stream serialization
@@ -234,6 +236,7 @@ struct Tile {
     int row_end;   // rows >= row_end are padding (not stored)
     int b_row;     // first B row of the tile
     int n0;        // first output column
+    int b_map;     // 1: B rows are in the second view (tmB2)
 };
 
 template <bool GROUPED, bool DUAL>
@@ -246,6 +249,7 @@ __device__ __forceinline__ Tile tile_of(const GemmParams& p, int t, const int* s
         r.row_end = p.M;
         r.n0 = n * BN;
         r.b_row = r.n0;
+        r.b_map = 0;
     } else {
         // column tiles innermost: the CTAs of one wave share each row tile of A (read once
         // from DRAM instead of once per column tile) and a group's row tiles of B
@@ -260,7 +264,14 @@ __device__ __forceinline__ Tile tile_of(const GemmParams& p, int t, const int* s
         r.a_row = g0 + (mt - s_mt_prefix[g]) * BM;
         r.row_end = p.group_bounds[g + 1];
         r.n0 = n * BN;
-        r.b_row = p.b_base_row + g * p.b_group_stride_rows + r.n0;
+        if (p.group_b_row) {  // per-group placement: the slot or the second view
+            const int v = p.group_b_row[g];
+            r.b_map = v < 0 ? 1 : 0;
+            r.b_row = (v & 0x7fffffff) + r.n0;
+        } else {
+            r.b_map = 0;
+            r.b_row = p.b_base_row + g * p.b_group_stride_rows + r.n0;
+        }
     }
     return r;
 }
@@ -466,6 +477,7 @@ __global__ void __launch_bounds__(NUM_THREADS, 1) gemm_bf16_tc(const __grid_cons
         if (lane == 0) {
             tma_prefetch_desc(&p.tmA);
             tma_prefetch_desc(&p.tmB);
+            if (GROUPED && p.group_b_row) tma_prefetch_desc(&p.tmB2);
             bool ok = true;
             int it = 0;
             uint32_t issued_mask = 0;
@@ -483,12 +495,12 @@ __global__ void __launch_bounds__(NUM_THREADS, 1) gemm_bf16_tc(const __grid_cons
                     const uint32_t sb = sa + A_BYTES;
                     mbar_expect_tx(full_bar(s), STAGE_BYTES);
                     tma_load_2d(sa, &p.tmA, full_bar(s), kb * BK, tl.a_row);
+                    const CUtensorMap* mb = (GROUPED && tl.b_map) ? &p.tmB2 : &p.tmB;
                     if (DUAL) {
-                        tma_load_2d(sb, &p.tmB, full_bar(s), kb * BK, tl.b_row);
-                        tma_load_2d(sb + B_BYTES / 2, &p.tmB, full_bar(s), kb * BK,
-                                    tl.b_row + p.b2_row_off);
+                        tma_load_2d(sb, mb, full_bar(s), kb * BK, tl.b_row);
+                        tma_load_2d(sb + B_BYTES / 2, mb, full_bar(s), kb * BK, tl.b_row + p.b2_row_off);
                     } else {
-                        tma_load_2d(sb, &p.tmB, full_bar(s), kb * BK, tl.b_row);
+                        tma_load_2d(sb, mb, full_bar(s), kb * BK, tl.b_row);
                     }
                     issued_mask |= 1u << s;
                 }
@@ -1284,6 +1296,13 @@ cudaError_t launch_gemm_bf16(const GemmDesc& d, int max_ctas, cudaStream_t s) {
     p.b_base_row = d.b_base_row;
     p.row_table = d.row_table;
     p.row_weight = d.row_weight;
+    p.group_b_row = nullptr;
+    if (d.group_b_row) {  // grouped only: B rows of some groups live in a second view
+        if (!grouped || !d.B2 || d.b2_rows < 1 || (reinterpret_cast<uintptr_t>(d.B2) & 15) ||
+            !cached_tmap(&p.tmB2, d.B2, d.b2_rows, d.K, d.ldb, BN))
+            return cudaErrorInvalidValue;
+        p.group_b_row = d.group_b_row;
+    }
     p.err = d.err_word;
     p.mbar_limit_ns = MBAR_LIMIT_NS;
     p.pdl = d.pdl ? 1 : 0;

@@ -68,6 +68,12 @@ struct GemmDesc {
     const int* row_table = nullptr;     // EPI_SCALE_F32: destination row of sorted row i
     const float* row_weight = nullptr;  // EPI_SCALE_F32: weight by destination row
     int max_tiles_hint = 0;             // grouped: upper bound of tiles (grid sizing)
+    // grouped, optional: group g's matrix starts at B row group_b_row[g] (device, [n_groups]);
+    // with the top bit set, at row (group_b_row[g] & 0x7fffffff) of B2 [b2_rows, K] instead
+    // (same ldb): experts read in place from the expert cache
+    const int* group_b_row = nullptr;
+    const void* B2 = nullptr;
+    int64_t b2_rows = 0;
     uint32_t* err_word = nullptr;       // mapped host word for internal timeouts
     // programmatic dependent launch: the prologue overlaps the previous kernel's tail.
     // Off where events bracket each launch, so that an event pair times this kernel alone.

@@ -127,6 +127,10 @@ struct ls_ctx {
     int64_t ecache_eb = 0;                 // bytes of one expert blob (G, U, D)
     std::vector<int64_t> ecache_counts;    // [N * E] earlier passes in which the pair was routed
     std::vector<int> ecache_slot;          // [N * E] cache slot of a hot pair, else -1
+    // [N][2][E] first B row of each expert's gate/up and down matrices for this pass: in the
+    // slot, or (top bit set) in the cache, where hits are read in place
+    int* ecache_rows_host = nullptr;       // pinned
+    int* ecache_rows_dev = nullptr;
     std::vector<char> ecache_filled;       // [N * E] its blob is in the cache
     std::vector<std::vector<std::pair<int, int>>> ecache_hits, ecache_fills;  // per layer, this pass
     int64_t n_ecache_hits = 0, n_ecache_host = 0;
@@ -295,8 +299,8 @@ void issue_copy(ls_ctx* c, int seg, void* dst, int slot, uint32_t epoch, cudaStr
                 const uint8_t* expert_mask) {
     SegRec& sr = c->segs[seg];
     const bool publish = !(c->prm.test_drop_publish > 0 && ++c->publishes == c->prm.test_drop_publish);
-    // expert cache: hits are copied in device memory ahead of the host copy and its publish;
-    // hot experts that come from the host this time are copied into the cache afterwards
+    // expert cache: hits stay where the cache holds them (the GEMMs read them there); hot
+    // experts that come from the host this time are copied into the cache after the publish
     const bool cached = c->ecache_K > 0 && expert_mask;
     auto cache_copies = [&](const std::vector<std::pair<int, int>>& list, bool into_slot) {
         for (auto& h : list) {
@@ -306,7 +310,6 @@ void issue_copy(ls_ctx* c, int seg, void* dst, int slot, uint32_t epoch, cudaStr
                                      cudaMemcpyDeviceToDevice, s));
         }
     };
-    if (cached) cache_copies(c->ecache_hits[seg], true);
     if (use_kernel && sr.kernel_ok) {
         KTime kt(c, "copy_h2slot", s);
         track(c, launch_copy_h2slot(sr.ranges_dev, sr.n_ranges, sr.n_chunks, dst, expert_mask,
@@ -510,6 +513,12 @@ void compute_segment(ls_ctx* c, const RunCtx& rc, int seg, bool wait) {
             g1.group_bounds = bounds; g1.n_groups = E;
             g1.b_group_stride_rows = (int)(eb / (2 * (int64_t)H));
             g1.b_base_row = 0;
+            const bool in_cache = c->ecache_K > 0 && seg >= c->sched.residents();
+            if (in_cache) {  // hot experts of streamed layers are read where the cache holds them
+                g1.group_b_row = c->ecache_rows_dev + (size_t)seg * 2 * E;
+                g1.B2 = c->ecache;
+                g1.b2_rows = (int64_t)c->ecache_K * (eb / (2 * (int64_t)H));
+            }
             {
                 KTime kt(c, "gemm_up", rc.s);
                 track(c, launch_gemm_bf16(g1, ctas, rc.s));
@@ -525,6 +534,11 @@ void compute_segment(ls_ctx* c, const RunCtx& rc, int seg, bool wait) {
             g2.b_base_row = (int)(2 * (int64_t)F * H * 2 / (2 * (int64_t)F));
             g2.row_table = table;
             g2.row_weight = c->moe_w + (int64_t)seg * rows;
+            if (in_cache) {
+                g2.group_b_row = c->ecache_rows_dev + (size_t)seg * 2 * E + E;
+                g2.B2 = c->ecache;
+                g2.b2_rows = (int64_t)c->ecache_K * (eb / (2 * (int64_t)F));
+            }
             {
                 KTime kt(c, "gemm_down", rc.s);
                 track(c, launch_gemm_bf16(g2, ctas, rc.s));
@@ -1125,6 +1139,9 @@ static ls_status register_impl(ls_ctx* c, const ls_segment_desc* segs, int32_t n
                 c->ecache_filled.assign((size_t)n * c->E, 0);
                 c->ecache_hits.assign(n, {});
                 c->ecache_fills.assign(n, {});
+                const size_t rb = sizeof(int) * (size_t)n * 2 * c->E;
+                CK(cudaHostAlloc((void**)&c->ecache_rows_host, rb, cudaHostAllocDefault));
+                CK(cudaMalloc(&c->ecache_rows_dev, rb));
             }
         }
     }
@@ -1159,6 +1176,10 @@ static void destroy_graph(ls_ctx* c) {
 // experts to copy from the host.
 static void ecache_plan_pass(ls_ctx* c) {
     const int N = c->N, E = c->E, R = c->sched.residents();
+    // B rows per expert blob in the gate/up view (rows of H elements) and the down view
+    // (rows of F elements); the down matrix starts 2F x H elements into the blob
+    const int up_rows = (int)(c->ecache_eb / (2 * (int64_t)c->H));
+    const int dn_rows = (int)(c->ecache_eb / (2 * (int64_t)c->F)), dn_base = 2 * c->H;
     std::vector<std::tuple<int64_t, int, int>> cand;
     for (int l = R; l < N; ++l)
         for (int e = 0; e < E; ++e)
@@ -1198,7 +1219,7 @@ static void ecache_plan_pass(ls_ctx* c) {
             if (!c->moe_used_host[i]) continue;
             if (hot[i] && c->ecache_filled[i]) {
                 c->ecache_hits[l].push_back({e, c->ecache_slot[i]});
-                c->moe_used_host[i] = 0;
+                c->moe_used_host[i] = 0;  // nothing to move: the GEMMs read it in the cache
                 ++c->n_ecache_hits;
             } else {
                 if (hot[i]) {
@@ -1208,6 +1229,18 @@ static void ecache_plan_pass(ls_ctx* c) {
                 ++c->n_ecache_host;
             }
         }
+    for (int l = R; l < N; ++l) {
+        int* up = c->ecache_rows_host + (size_t)l * 2 * E;
+        int* dn = up + E;
+        for (int e = 0; e < E; ++e) {
+            up[e] = e * up_rows;
+            dn[e] = dn_base + e * dn_rows;
+        }
+        for (auto& h : c->ecache_hits[l]) {
+            up[h.first] = (int)(0x80000000u | (uint32_t)(h.second * up_rows));
+            dn[h.first] = (int)(0x80000000u | (uint32_t)(dn_base + h.second * dn_rows));
+        }
+    }
 }
 
 // Checks, workspaces and (MoE) routing of one pass on the caller's stream; fills the
@@ -1254,7 +1287,13 @@ static ls_status prepare_pass(ls_ctx* c, const void* x_dev, void* y_dev, int64_t
         }
         CK(cudaMemcpyAsync(c->moe_used_host, c->moe_used, (size_t)c->N * E, cudaMemcpyDeviceToHost, s));
         CK(cudaStreamSynchronize(s));
-        if (c->ecache_K > 0) ecache_plan_pass(c);
+        if (c->ecache_K > 0) {
+            ecache_plan_pass(c);
+            // the host table is rewritten only after the next pass's routing synchronisation,
+            // which this copy precedes on the same stream
+            CK(cudaMemcpyAsync(c->ecache_rows_dev, c->ecache_rows_host, sizeof(int) * (size_t)c->N * 2 * E,
+                               cudaMemcpyHostToDevice, s));
+        }
         const int64_t eb = c->segs[0].slot_bytes / E;
         const int R = c->sched.residents();  // residents are loaded whole (see GpuExec::load)
         for (int l = R; l < c->N; ++l) {
@@ -1612,6 +1651,8 @@ static void release_resources(ls_ctx* c) {
                         (void*)c->stage_logits})
             if (p) cudaFree(p);
         if (c->moe_used_host) cudaFreeHost(c->moe_used_host);
+        if (c->ecache_rows_host) cudaFreeHost(c->ecache_rows_host);
+        if (c->ecache_rows_dev) cudaFree(c->ecache_rows_dev);
         if (c->err_word) cudaFreeHost(c->err_word);
         for (auto e : c->slot_free)
             if (e) cudaEventDestroy(e);
