@@ -213,6 +213,22 @@ def test_moe_stack_full_size():
     assert rel_err(to_f64(y)[rows], ref) <= BOUND
 
 
+@pytest.mark.skipif(os.environ.get("LS_SLOW") != "1", reason="58 GB host stack: set LS_SLOW=1")
+def test_moe_stack_full_size_expert_cache():
+    """40 GiB of expert cache at full size: the third pass reads ~4,500 hot experts in place
+    (cache rows far past 2^24) and keeps the bits of a pass without the cache."""
+    cfg = synth.MOE
+    hs = synth.HostStack(cfg)
+    lg_dev, _ = logits_dev(cfg)
+    y0, _, _, _, _ = _run(cfg, hs, logits=lg_dev, runs=1)
+    y, ev, stats, st, sts = _run(cfg, hs, logits=lg_dev, runs=3, expert_cache_bytes=40 << 30)
+    assert stats["expert_cache_hits"] > 4000
+    assert np.array_equal(_bits(y), _bits(y0))
+    rows = _rows(cfg, 4)
+    ref = _oracle_from_host(cfg, hs, rows)
+    assert rel_err(to_f64(y)[rows], ref) <= BOUND
+
+
 # ------------------------------------------------------------------ faults (host-made, bounded)
 def test_dropped_handoff_times_out_then_recovers():
     """"layer split: overlap the stages' hand-off", Changes since #936: with the
