@@ -1170,7 +1170,7 @@ static void destroy_graph(ls_ctx* c) {
 
 // The expert cache's decisions for the pass whose routing moe_used_host holds: the hot set
 // is the K pairs of streamed layers routed in the most earlier passes (ties to the lower
-// layer, then expert); leaving pairs give back their slot, entering ones take the lowest
+// expert, then layer, so that equal counts spread the cache over the layers); leaving pairs give back their slot, entering ones take the lowest
 // free slots in rank order; a routed hot pair is a hit once filled, else it is filled from
 // this pass's host copy. Hits are then cleared from moe_used_host, which becomes the set of
 // experts to copy from the host.
@@ -1183,11 +1183,11 @@ static void ecache_plan_pass(ls_ctx* c) {
     std::vector<std::tuple<int64_t, int, int>> cand;
     for (int l = R; l < N; ++l)
         for (int e = 0; e < E; ++e)
-            if (c->ecache_counts[(size_t)l * E + e] > 0) cand.emplace_back(-c->ecache_counts[(size_t)l * E + e], l, e);
+            if (c->ecache_counts[(size_t)l * E + e] > 0) cand.emplace_back(-c->ecache_counts[(size_t)l * E + e], e, l);
     std::sort(cand.begin(), cand.end());
     if ((int)cand.size() > c->ecache_K) cand.resize(c->ecache_K);
     std::vector<char> hot((size_t)N * E, 0);
-    for (auto& t : cand) hot[(size_t)std::get<1>(t) * E + std::get<2>(t)] = 1;
+    for (auto& t : cand) hot[(size_t)std::get<2>(t) * E + std::get<1>(t)] = 1;
     std::vector<int> free_slots;
     std::vector<char> taken(c->ecache_K, 0);
     for (size_t i = 0; i < hot.size(); ++i) {
@@ -1204,7 +1204,7 @@ static void ecache_plan_pass(ls_ctx* c) {
         c->ecache_fills[l].clear();
     }
     for (auto& t : cand) {
-        const int l = std::get<1>(t), e = std::get<2>(t);
+        const int e = std::get<1>(t), l = std::get<2>(t);
         const size_t i = (size_t)l * E + e;
         if (c->ecache_slot[i] < 0) {
             c->ecache_slot[i] = free_slots.back();

@@ -133,7 +133,7 @@ typedef struct ls_params {
     int64_t expert_cache_bytes;   /* MoE kind: device memory for hot experts of streamed layers, on top of
                                      max_vram_bytes (0 = none). It holds K = bytes / expert-blob bytes
                                      experts: in each pass, the K (layer, expert) pairs routed in the most
-                                     earlier passes (ties to the lower layer, then expert); a hot expert is
+                                     earlier passes (ties to the lower expert, then layer); a hot expert is
                                      copied in when its layer next loads it from the host, and a routed
                                      expert found there is copied within device memory instead of over
                                      the host link. Bits are unchanged; the schedule's load bytes count

@@ -12,8 +12,9 @@ project's reading, chosen to be deterministic and checkable:
   * counts[l][e] = the number of earlier passes in which expert e of layer l was
     routed (by any token);
   * the hot set of pass r is the K pairs (l, e) of streamed layers (l >= R) with
-    the largest counts, counts > 0 only, ties to the lower layer, then the lower
-    expert;
+    the largest counts, counts > 0 only, ties to the lower expert, then the lower
+    layer (equal counts spread the cache over the layers, so that every layer's
+    host copy shrinks and the prefetch pipeline keeps the link busy);
   * a hot pair is "filled" once its expert has been copied into the cache: when
     it is routed in a pass that starts with it hot and unfilled, its host copy
     in that pass also fills the cache. A pair that leaves the hot set is dropped;
@@ -29,9 +30,9 @@ import numpy as np
 def hot_set(counts: np.ndarray, K: int, first_streamed: int) -> list:
     """The K pairs with the largest counts (> 0) among layers >= first_streamed."""
     L, E = counts.shape
-    cand = [(-int(counts[l, e]), l, e) for l in range(first_streamed, L) for e in range(E) if counts[l, e] > 0]
+    cand = [(-int(counts[l, e]), e, l) for l in range(first_streamed, L) for e in range(E) if counts[l, e] > 0]
     cand.sort()
-    return [(l, e) for _, l, e in cand[:K]]
+    return [(l, e) for _, e, l in cand[:K]]
 
 
 def cache_passes(used: list, K: int, first_streamed: int = 0):

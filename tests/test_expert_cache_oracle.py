@@ -12,9 +12,11 @@ def _u(L, E, pairs):
     return a
 
 
-def test_hot_set_ranks_by_count_then_layer_then_expert():
+def test_hot_set_ranks_by_count_then_expert_then_layer():
     c = np.array([[2, 0, 1], [2, 3, 0]])
     assert hot_set(c, 2, 0) == [(1, 1), (0, 0)]
+    # equal counts: the lower expert first, then the lower layer (spread over the layers)
+    assert hot_set(np.ones((3, 2), int), 4, 0) == [(0, 0), (1, 0), (2, 0), (0, 1)]
     assert hot_set(c, 4, 0) == [(1, 1), (0, 0), (1, 0), (0, 2)]
     assert hot_set(c, 9, 0) == [(1, 1), (0, 0), (1, 0), (0, 2)]   # zero counts never enter
     assert hot_set(c, 2, 1) == [(1, 1), (1, 0)]                   # residents excluded
