@@ -652,10 +652,11 @@ def test_moe_residents_follow_routing_changes():
 
 
 @pytest.mark.parametrize("copy_path", [2, 1])
-def test_moe_expert_cache_matches_oracle_policy(copy_path):
+@pytest.mark.parametrize("skewed", [True, False])
+def test_moe_expert_cache_matches_oracle_policy(copy_path, skewed):
     """Expert cache of the streamed layers: hot experts come from device memory, the
     schedule's load bytes are the oracle policy's host copies, and the bits equal a run
-    without the cache."""
+    without the cache. Uniform routing makes most counts tie, which the tie rule decides."""
     from oracle import expert_cache, forward as F
     cfg = _moe_cfg(4, 64, experts=8, hidden=256, ffn=128, k=2)
     S = synth.segment_slot_bytes(cfg)
@@ -663,7 +664,7 @@ def test_moe_expert_cache_matches_oracle_policy(copy_path):
     K = 6
     hs = synth.HostStack(cfg)
     rng = np.random.default_rng(9)
-    bias = np.array([3.0, 2.0, 1.5, 0.5, 0, 0, 0, 0], np.float32)   # data-dependent routing: skewed
+    bias = np.array([3.0, 2.0, 1.5, 0.5, 0, 0, 0, 0] if skewed else [0] * 8, np.float32)   # data-dependent routing
     passes = [(rng.standard_normal((cfg.n_segments, cfg.tokens, cfg.n_experts)).astype(np.float32) + bias)
               for _ in range(5)]
     outs = {}
