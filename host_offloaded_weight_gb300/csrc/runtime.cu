@@ -1170,10 +1170,11 @@ static void destroy_graph(ls_ctx* c) {
 
 // The expert cache's decisions for the pass whose routing moe_used_host holds: the hot set
 // is the K pairs of streamed layers routed in the most earlier passes (ties to the lower
-// expert, then layer, so that equal counts spread the cache over the layers); leaving pairs give back their slot, entering ones take the lowest
-// free slots in rank order; a routed hot pair is a hit once filled, else it is filled from
-// this pass's host copy. Hits are then cleared from moe_used_host, which becomes the set of
-// experts to copy from the host.
+// expert, then layer, so that equal counts spread the cache over the layers); leaving
+// pairs give back their slot, entering ones take the lowest free slots in rank order; a
+// routed hot pair is a hit once filled, else it is filled from this pass's host copy. Hits
+// are then cleared from moe_used_host, which becomes the set of experts to copy from the
+// host, and the row tables tell the GEMMs where each expert's matrices are.
 static void ecache_plan_pass(ls_ctx* c) {
     const int N = c->N, E = c->E, R = c->sched.residents();
     // B rows per expert blob in the gate/up view (rows of H elements) and the down view
