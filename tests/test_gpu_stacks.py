@@ -354,6 +354,23 @@ def test_two_contexts_interleaved():
             L.ls_ctx_destroy(c)
 
 
+@pytest.mark.parametrize("name", sorted(SMALL))
+def test_each_segment_against_the_oracle_on_the_gpus_own_input(name):
+    """Diagnostic parity per segment: prefix stacks of 1..N segments give the GPU's bf16
+    activation after each segment; the oracle applies segment k to the GPU's own output of
+    segment k-1, which isolates that one segment's error (a bf16 rounding of its output and
+    of the residual it reads, plus fp32 accumulation)."""
+    cfg = SMALL[name]
+    outs = [to_f64(x_dev(cfg))]
+    for k in range(1, cfg.n_segments + 1):
+        hs = synth.HostStack(cfg, n_segments=k)
+        y, _, _, _, _ = _run(cfg.with_(n_segments=k), hs, runs=1)
+        outs.append(to_f64(y))
+    for k in range(1, cfg.n_segments + 1):
+        ref = ostack.apply_segment(cfg, k - 1, outs[k - 1])
+        assert rel_err(outs[k], ref) <= 6e-3, (name, k, rel_err(outs[k], ref))
+
+
 def test_run_host_matches_run():
     cfg = SMALL["proj"]
     hs = synth.HostStack(cfg)
