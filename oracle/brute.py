@@ -96,3 +96,56 @@ def replay(events: list, n_segments: int, n_slots) -> int:
         peak = max(peak, run_peak)
         assert activated == list(range(len(activated))), "segments activate in order"
     return peak
+
+
+def check_window(events: list, n_segments: int, R: int, d: int, cross_run: bool = False) -> None:
+    """Check the prefetch window along a schedule without failures, run by run.
+
+    What the pages fix for any schedule ("feat: prefetch streamed layers during compute",
+    Summary: the next d segments are loaded while the active one computes; depth 0 is
+    synchronous streaming):
+      * each streamed segment (index >= R) is loaded exactly once per run, before its
+        activation, by a PREFETCH or LOAD_SYNC of this run or (cross-run window) by a
+        PREFETCH of the run before, issued after that run had activated the segment;
+      * residents are never loaded during a run;
+      * when segment k activates, the streamed segments loaded and not yet activated,
+        k excluded, number min(d, streamed segments after k): the window is full but
+        never reaches past the run. With a cross-run window on a full ring (N - R > d)
+        the next run's first segments count too, so the number is d at every step.
+    The window here is not computed the simulator's way: it is counted from the events."""
+    M = n_segments - R
+    crossing = cross_run and M > d
+    by_run: dict = {}
+    for ev in events:
+        by_run.setdefault(ev[0], []).append(ev)
+    ahead: set = set()                 # loaded for this run, not yet activated
+    for run in sorted(by_run):
+        nxt: set = set()               # loaded in this run for the next run
+        done: set = set()
+        loads: dict = {s: 0 for s in ahead}
+        for (_, step, kind, seg, slot, _nb) in by_run[run]:
+            if kind in (PREFETCH, LOAD_SYNC):
+                assert seg >= R, f"run {run}: resident {seg} loaded during the run"
+                if seg in done:
+                    assert cross_run and kind == PREFETCH, f"run {run}: {seg} loaded after its activation"
+                    assert seg not in nxt, f"run {run}: {seg} loaded twice for the next run"
+                    nxt.add(seg)
+                else:
+                    loads[seg] = loads.get(seg, 0) + 1
+                    assert loads[seg] == 1, f"run {run}: {seg} loaded twice"
+                    ahead.add(seg)
+            elif kind == ACTIVATE:
+                k = seg
+                assert k == step and k == len(done), "segments activate in order"
+                if k >= R:
+                    assert k in ahead, f"run {run}: streamed segment {k} activated without a load"
+                    ahead.discard(k)
+                want = min(d, M if k < R else n_segments - 1 - k)
+                if crossing:
+                    want = d
+                got = len(ahead) + len(nxt)
+                assert got == want, f"run {run} step {k}: {got} loads ahead of the active segment, want {want}"
+                done.add(k)
+        assert len(done) == n_segments
+        assert not ahead, f"run {run}: loads never activated: {sorted(ahead)}"
+        ahead = nxt

@@ -5,6 +5,17 @@ depth d, ring slots Q, pool slots P) and the exact list of schedule events the
 runtime must execute. The runtime's own scheduler is separate code; tests
 compare the two event lists for equality.
 
+The simulator is written as rules, each a function of its own:
+  * ``plan_slots``  the plan in closed form: depth first, then the longest
+                    resident prefix that still fits;
+  * ``issue_step``  the prefetch window: the step at which each streamed load of
+                    a run is issued, as a formula of (R, d) and the load's number;
+  * ``ring_slot``   the slot of each streamed load, as a formula of its number;
+  * memory and failure rules, applied on top of the window's schedule: the
+    pool's degradation to fewer slots, runtime pressure with the pool off
+    (eviction from the end of the resident prefix), the synchronous fallback
+    when asynchronous transfer is unavailable, and plan changes between runs.
+
 Sources:
   "feat: prefetch streamed layers during compute" (sd.cpp #1905), Summary and
   the Effective behavior table: depth 0 is synchronous streaming, depth N asks
@@ -103,42 +114,70 @@ class Plan:
         return min(self.d_req, self.M)
 
 
-def _plan_for(N: int, S: int, shared_total: int, avail: int, depth: int, resident: int,
-              mandatory: bool) -> Plan:
-    """Depth first, then the longest resident prefix that still fits ``avail`` slots."""
-    d_fit = depth if avail >= N else min(depth, avail - 1)
-    cap = N if resident < 0 else min(resident, N)
-    R = 0
-    for r in range(cap, -1, -1):
-        if min(r + d_fit + 1, N) <= avail:
-            R = r
-            break
-    M = N - R
-    Q = min(d_fit + 1, M) if M > 0 else 0
-    return Plan(N, S, shared_total, avail, d_fit, R, Q, R + Q, mandatory)
-
-
+# ------------------------------------------------------------------ the plan
 def plan_slots(seg_slot_bytes: list, shared_bytes: list, depth: int, resident: int,
                max_vram: int, slot_cap: int | None = None) -> Plan:
-    """Plan from the budget. ``slot_cap`` is a remembered reduced slot count."""
+    """Plan from the budget (sd.cpp #1905 Summary and table; #1906 Summary and table).
+
+    ``slot_cap`` is a remembered reduced slot count. In closed form:
+      avail = slots the budget holds beside the shared region (all N when the budget
+              is 0 but a cap is remembered), at most ``slot_cap``;
+      d     = the requested depth, at most avail - 1 unless every segment fits
+              (prefetch first: the ring of d + 1 slots must fit with no residents);
+      R     = the resident cap, at most what is left beside that ring."""
     N = len(seg_slot_bytes)
     S = max(seg_slot_bytes)
     shared_total = sum(align_up(b) for b in shared_bytes)
-    if max_vram == 0 and slot_cap is None:
+    if max_vram == 0 and slot_cap is None:          # segmentation off: everything resident
         return Plan(N, S, shared_total, N, 0, N, 0, N)
     if max_vram == 0:
         avail, mandatory = N, False
     else:
-        avail = (max_vram - shared_total) // S if max_vram > shared_total else 0
+        avail = max(0, max_vram - shared_total) // S
         mandatory = avail < 1
         if mandatory:
             # below one slot: only the mandatory execution slot, no residency, no prefetch
             return Plan(N, S, shared_total, 1, 0, 0, 1, 1, True)
     if slot_cap is not None:
         avail = min(avail, slot_cap)
-    return _plan_for(N, S, shared_total, avail, depth, resident, mandatory)
+    cap = N if resident < 0 else min(resident, N)
+    if avail >= N:
+        d, R = depth, cap                        # every segment fits whatever the depth
+    else:
+        d = min(depth, avail - 1)
+        R = min(cap, avail - d - 1)
+    M = N - R
+    Q = min(d + 1, M) if M > 0 else 0
+    return Plan(N, S, shared_total, avail, d, R, Q, R + Q, mandatory)
 
 
+# ------------------------------------------------------------------ the window and the ring
+def issue_step(j: int, R: int, d: int) -> int:
+    """Step of a run at which its streamed load number j (from 0) enters the prefetch window.
+
+    The window holds the active segment and the next d streamed segments (reading 3). At
+    the steps of the resident prefix no streamed segment is active yet, so the window is
+    streamed loads 0..d-1, all issued at step 0. Later, load j enters when streamed
+    segment j - d (segment R + j - d) becomes active. Numbers j >= N - R are the next
+    run's loads (cross-run window): the same rule puts them in the last d steps."""
+    return 0 if j < d else R + j - d
+
+
+def ring_slot(J: int, R: int, Q: int) -> int:
+    """Pool slot of streamed load number J, counted over the runs that share one ring:
+    the Q ring slots follow the R resident slots and are taken in turn."""
+    return R + J % Q
+
+
+def windows(R: int, d: int, first: int, reach: int) -> dict:
+    """{step: [load numbers issued at that step, ascending]} for loads first..reach-1."""
+    out: dict = {}
+    for j in range(first, reach):
+        out.setdefault(issue_step(j, R, d), []).append(j)
+    return out
+
+
+# ------------------------------------------------------------------ state across runs
 @dataclass
 class Stats:
     prefetch_queued: int = 0
@@ -181,39 +220,7 @@ class Sim:
     stats: Stats = field(default_factory=Stats)
     warnings: set = field(default_factory=set)
 
-    # -------------------------------------------------------------- register
-    def register(self) -> int:
-        """Plan and allocate the shared region and (pool on) the slot pool."""
-        shared_b = [b for _, b in self.shared]
-        p = plan_slots(self.seg_slot_bytes, shared_b, self.depth, self.resident, self.max_vram)
-        if p.warn_mandatory:
-            self.warnings.add(WARN_MANDATORY_SLOT)
-        if not self._alloc(p.shared_total):
-            self.status = ERR_OOM
-            return ERR_OOM
-        if self.use_pool:
-            chosen = None
-            for cap in range(p.P, 0, -1):
-                q = p if cap == p.P else plan_slots(self.seg_slot_bytes, shared_b, self.depth,
-                                                    self.resident, self.max_vram, slot_cap=cap)
-                q.warn_mandatory = p.warn_mandatory
-                if self._alloc(q.P * q.S):
-                    chosen = q
-                    break
-                self.stats.pool_degradations += 1
-            if chosen is None:
-                self._free(p.shared_total)
-                self.status = ERR_OOM
-                return ERR_OOM
-            if chosen.P < p.P:
-                self.slot_cap = chosen.P
-            p = chosen
-        self.plan = p
-        self.R = p.R
-        self.d = p.d_req
-        self.status = WARN_MANDATORY_SLOT if p.warn_mandatory else OK
-        return self.status
-
+    # -------------------------------------------------------------- memory rules
     def _alloc(self, nbytes: int) -> bool:
         if nbytes == 0:
             return True
@@ -225,10 +232,84 @@ class Sim:
     def _free(self, nbytes: int) -> None:
         self.live -= nbytes
 
+    def _pool_for(self, p: Plan) -> Plan | None:
+        """Pool degradation (sd.cpp #1906 table): the pool of plan p, else the plan for at
+        most P - 1, P - 2, ..., 1 slots of the same size; each refused allocation counts one
+        degradation. None when not even one slot can be had."""
+        shared_b = [b for _, b in self.shared]
+        for cap in range(p.P, 0, -1):
+            q = p if cap == p.P else plan_slots(self.seg_slot_bytes, shared_b, self.depth, self.resident,
+                                                self.max_vram, slot_cap=cap)
+            q.warn_mandatory = p.warn_mandatory
+            if self._alloc(q.P * q.S):
+                if q.P < p.P:
+                    self.slot_cap = q.P          # a reduced cap is remembered
+                return q
+            self.stats.pool_degradations += 1
+        return None
+
+    def _alloc_evicting(self, nbytes: int, k: int) -> bool:
+        """Runtime pressure with the pool off (sd.cpp #1905 Summary): a load issued at step k
+        that does not fit evicts residents from the end of the prefix, but only ones already
+        computed in this run (index < k), so never the active segment."""
+        while not self._alloc(nbytes):
+            r = self.cur_R - 1
+            if r < 0 or r >= k:
+                return False
+            self._emit(k, EVICT, r, r, 0)
+            self._free(self.seg_slot_bytes[r])
+            self.cur_R = r
+        return True
+
+    def _fallback(self) -> None:
+        """Asynchronous transfer unavailable or a prefetch allocation failed: the rest of
+        the run and every later run stream synchronously (remembered)."""
+        self.async_ok = False
+        self.d = 0
+        self.fail_async = False
+        self.stats.sync_fallbacks += 1
+        self.warnings.add(WARN_SYNC_FALLBACK)
+
     def _emit(self, step, kind, seg, slot, nbytes):
         self.events.append((self.run, step, kind, seg, slot, nbytes))
+        st = self.stats
+        if kind in (SHARED_LOAD, LOAD_RESIDENT, LOAD_SYNC, PREFETCH):
+            st.bytes_loaded += nbytes
+        if kind == SHARED_LOAD:
+            st.shared_loads += 1
+        elif kind == LOAD_RESIDENT:
+            st.resident_loads += 1
+        elif kind == LOAD_SYNC:
+            st.sync_loads += 1
+        elif kind == PREFETCH:
+            st.prefetch_queued += 1
+        elif kind == EVICT:
+            st.evictions += 1
 
-    # -------------------------------------------------------------- run
+    # -------------------------------------------------------------- register
+    def register(self) -> int:
+        """Plan, then allocate the shared region and (pool on) the slot pool."""
+        p = plan_slots(self.seg_slot_bytes, [b for _, b in self.shared], self.depth, self.resident,
+                       self.max_vram)
+        if p.warn_mandatory:
+            self.warnings.add(WARN_MANDATORY_SLOT)
+        if not self._alloc(p.shared_total):
+            self.status = ERR_OOM
+            return ERR_OOM
+        if self.use_pool:
+            q = self._pool_for(p)
+            if q is None:
+                self._free(p.shared_total)
+                self.status = ERR_OOM
+                return ERR_OOM
+            p = q
+        self.plan = p
+        self.R = p.R
+        self.d = p.d_req
+        self.status = WARN_MANDATORY_SLOT if p.warn_mandatory else OK
+        return self.status
+
+    # -------------------------------------------------------------- one run
     def run_once(self, load_bytes=None) -> int:
         """One pass over all segments; returns the run's status.
 
@@ -239,106 +320,103 @@ class Sim:
         lb = load_bytes or (lambda s: self.seg_slot_bytes[s])
         sz = self.seg_slot_bytes
         pool = bool(self.use_pool)
-        fell_back = False
-        ret = OK
+
+        # before the first step: shared region (run 0), stale carried loads, residents
         if self.run == 0:
             for sid, b in sorted(self.shared):
                 self._emit(-1, SHARED_LOAD, sid, -1, b)
-                self.stats.shared_loads += 1
-                self.stats.bytes_loaded += b
         if self.carried and self.carried_R != self.R:
-            self._release_carried()      # planned for another ring: stale
-        for i in range(self.loaded_R, self.R):      # residents without their data yet
+            self._release_carried()          # planned for another ring: stale
+        for i in range(self.loaded_R, self.R):
             if not pool and not self._alloc(sz[i]):
-                self.R = i          # the prefix ends where memory ran out
+                self.R = i                   # the prefix ends where memory ran out
                 break
             self._emit(-1, LOAD_RESIDENT, i, i, lb(i))
-            self.stats.resident_loads += 1
-            self.stats.bytes_loaded += lb(i)
         self.loaded_R = self.R
-        R = self.R                      # this run's resident prefix and ring
+
+        # this run's ring and window
+        R = self.R
         M = N - R
-        Q = min(self.d + 1, M) if M > 0 else 0
         d = min(self.d, M)
+        Q = min(self.d + 1, M) if M > 0 else 0
         J0 = self.J if self.cross_run else 0
-        # the window reaches into the next run only with a full ring of d + 1 slots
         reach = M + d if (self.cross_run and M > d) else M
+        carried_in, self.carried = self.carried, []
+        prefetched = {seg for seg, _ in carried_in}
+        sched = windows(R, d, len(carried_in), reach) if d >= 1 and self.async_ok else {}
+        prefetching = bool(sched)
+        waiting: list = []                   # load numbers whose window is open, not yet issued
         self.cur_R = R
-        prefetched = {seg for seg, _ in self.carried}   # issued by the previous run
-        next_load = len(self.carried)
-        self.carried = []
+        status, fell_back = OK, False
+
+        def seg_of(j):
+            return R + j % M
+
         for k in range(N):
-            streamed_upto = max(0, k - R + 1)       # streamed segments with index <= k
-            if d >= 1 and self.async_ok:
-                while next_load < reach and next_load < streamed_upto + d:
-                    seg = R + next_load % M
-                    if next_load >= M and not pool and not self._alloc(sz[seg]):
-                        break            # the next run's loads never evict: that run loads them itself
-                    if next_load < M and (self.fail_async or (not pool and not self._alloc_evicting(sz[seg], k))):
+            if prefetching:
+                waiting += sched.get(k, [])
+                issued = 0
+                for j in waiting:
+                    seg = seg_of(j)
+                    if j >= M:
+                        # the next run's loads never evict; without memory a load waits for a
+                        # later step (its run loads the segment itself if none comes)
+                        if not pool and not self._alloc(sz[seg]):
+                            break
+                    elif self.fail_async or (not pool and not self._alloc_evicting(sz[seg], k)):
                         self._fallback()
-                        fell_back = True
-                        d = 0
+                        fell_back, prefetching = True, False
                         break
-                    slot = R + (J0 + next_load) % Q
+                    slot = ring_slot(J0 + j, R, Q)
                     self._emit(k, PREFETCH, seg, slot, lb(seg))
-                    self.stats.prefetch_queued += 1
-                    self.stats.bytes_loaded += lb(seg)
-                    if next_load < M:
+                    if j < M:
                         prefetched.add(seg)
                     else:
                         self.carried.append((seg, slot))
-                    next_load += 1
-            if k >= R and k not in prefetched:
+                    issued += 1
+                waiting = waiting[issued:] if prefetching else []
+            streamed = k >= R
+            slot = ring_slot(J0 + k - R, R, Q) if streamed else k
+            if streamed and k not in prefetched:
                 if not pool and not self._alloc_evicting(sz[k], k):
-                    ret = ERR_OOM
+                    status = ERR_OOM
                     break
-                self._emit(k, LOAD_SYNC, k, R + (J0 + k - R) % Q, lb(k))
-                self.stats.sync_loads += 1
-                self.stats.bytes_loaded += lb(k)
-                next_load = k - R + 1
-            self._emit(k, ACTIVATE, k, k if k < R else R + (J0 + k - R) % Q, 0)
+                self._emit(k, LOAD_SYNC, k, slot, lb(k))
+            self._emit(k, ACTIVATE, k, slot, 0)
             if k in prefetched:
                 self.stats.prefetch_activated += 1
-            if not pool and k >= R:
-                self._free(sz[k])
+            if not pool and streamed:
+                self._free(sz[k])            # its buffer goes back after its compute
+
         self.R = self.cur_R
         self.loaded_R = min(self.loaded_R, self.R)
         self.carried_R = R
         if self.cross_run:
             self.J = J0 + M
         self.run += 1
-        if ret != OK:
-            return ret
+        if status != OK:
+            return status
         return WARN_SYNC_FALLBACK if fell_back else OK
 
+    # -------------------------------------------------------------- plan changes
     def replan(self, depth: int, resident: int, max_vram: int) -> int:
         """New controls between runs (the next run uses them). Returns the plan's status."""
         assert self.plan is not None
         self.depth, self.resident, self.max_vram = depth, resident, max_vram
         self._release_carried()
-        shared_b = [b for _, b in self.shared]
         old = self.plan
-        p = plan_slots(self.seg_slot_bytes, shared_b, depth, resident, max_vram, slot_cap=self.slot_cap)
+        p = plan_slots(self.seg_slot_bytes, [b for _, b in self.shared], depth, resident, max_vram,
+                       slot_cap=self.slot_cap)
         if self.use_pool and p.P != old.P:
             # the pool is given back and allocated at the new count: every slot is emptied
             self._evict_residents_down_to(0)
             self._free(old.P * old.S)
-            chosen = None
-            for cap in range(p.P, 0, -1):
-                q = p if cap == p.P else plan_slots(self.seg_slot_bytes, shared_b, depth, resident,
-                                                    max_vram, slot_cap=cap)
-                q.warn_mandatory = p.warn_mandatory
-                if self._alloc(q.P * q.S):
-                    chosen = q
-                    break
-                self.stats.pool_degradations += 1
-            if chosen is None:
+            q = self._pool_for(p)
+            if q is None:
                 self.plan = None
                 self.status = ERR_OOM
                 return ERR_OOM
-            if chosen.P < p.P:
-                self.slot_cap = chosen.P
-            p = chosen
+            p = q
         else:
             self._evict_residents_down_to(p.R)     # stale residents, from the end of the prefix
         self.plan = p
@@ -355,7 +433,6 @@ class Sim:
         """Release residents keep .. loaded_R - 1, last first (before the next run's first step)."""
         for r in range(self.loaded_R - 1, keep - 1, -1):
             self._emit(-1, EVICT, r, r, 0)
-            self.stats.evictions += 1
             if not self.use_pool:
                 self._free(self.seg_slot_bytes[r])
         self.loaded_R = min(self.loaded_R, keep)
@@ -364,33 +441,9 @@ class Sim:
         """Prefetches issued for a run whose plan no longer holds: give back their slots."""
         for seg, slot in self.carried:
             self._emit(-1, EVICT, seg, slot, 0)
-            self.stats.evictions += 1
             if not self.use_pool:
                 self._free(self.seg_slot_bytes[seg])
         self.carried = []
-
-    def _fallback(self) -> None:
-        """Asynchronous transfer unavailable or a prefetch allocation failed:
-        continue synchronously, and remember it."""
-        self.async_ok = False
-        self.d = 0
-        self.fail_async = False
-        self.stats.sync_fallbacks += 1
-        self.warnings.add(WARN_SYNC_FALLBACK)
-
-    def _alloc_evicting(self, nbytes: int, k: int) -> bool:
-        """Allocate for a load issued at step k. Under memory pressure, evict
-        residents from the end of the prefix, but only ones already computed in
-        this run (index < k): the active segment is never evicted."""
-        while not self._alloc(nbytes):
-            r = self.cur_R - 1
-            if r < 0 or r >= k:
-                return False
-            self._emit(k, EVICT, r, r, 0)
-            self.stats.evictions += 1
-            self._free(self.seg_slot_bytes[r])
-            self.cur_R = r
-        return True
 
 
 def simulate(seg_slot_bytes, shared=(), depth=0, resident=-1, max_vram=0, use_pool=1, runs=1,

@@ -1,5 +1,7 @@
-"""Plant plausible mistakes in the plan-change, cross-run and expert-cache rules of the
-oracle (on the CPU) and check that a pin catches each one."""
+"""Plant plausible mistakes in the policy oracle (on the CPU): its plan, prefetch window,
+ring numbering, plan-change, cross-run and expert-cache rules. Each one must be caught by
+a pin that does not involve the library's own scheduler: the pages' tables and worked
+numbers, brute-force plan search, the slot replay and the window counted from events."""
 import numpy as np
 import pytest
 
@@ -7,6 +9,7 @@ from oracle import expert_cache as X
 from oracle import policy as Pol
 
 import test_expert_cache_oracle as TX
+import test_policy_oracle as TP
 import test_policy_replan as TR
 
 
@@ -66,9 +69,61 @@ def _cache_counts_this_pass(used, K, first_streamed=0):
     return out
 
 
+def _window_one_short(j, R, d):
+    return 0 if j < d - 1 else R + j - d + 1          # a window of d - 1 ahead of the active one
+
+
+def _window_one_long(j, R, d):
+    return 0 if j < d + 1 else R + j - d - 1          # d + 1 ahead: more loads than the ring holds
+
+
+def _window_ignores_residents(j, R, d):
+    return max(0, R + j - d)                          # nothing prefetched during the resident prefix
+
+
+def _window_counts_residents(j, R, d):
+    return max(0, j - d)                              # residents consume depth
+
+
+def _ring_without_resident_offset(J, R, Q):
+    return J % Q                                      # ring slots overlap the resident slots
+
+
+def _ring_one_slot_short(J, R, Q):
+    return R + J % max(1, Q - 1)                      # the ring reuses a slot one load too early
+
+
+def _plan_residents_first(seg_slot_bytes, shared_bytes, depth, resident, max_vram, slot_cap=None):
+    p = _ORIG_PLAN(seg_slot_bytes, shared_bytes, depth, resident, max_vram, slot_cap)
+    if p.warn_mandatory or p.avail >= p.N:
+        return p
+    R = min(p.N if resident < 0 else min(resident, p.N), p.avail - 1)   # residents take the room first
+    d = min(depth, p.avail - R - 1)
+    M = p.N - R
+    Q = min(d + 1, M) if M > 0 else 0
+    return Pol.Plan(p.N, p.S, p.shared_total, p.avail, d, R, Q, R + Q, p.warn_mandatory)
+
+
+def _plan_budget_rounds_up(seg_slot_bytes, shared_bytes, depth, resident, max_vram, slot_cap=None):
+    if max_vram > 0:
+        S = max(seg_slot_bytes)
+        sh = sum(Pol.align_up(b) for b in shared_bytes)
+        max_vram = sh + -(-(max_vram - sh) // S) * S if max_vram > sh else max_vram
+    return _ORIG_PLAN(seg_slot_bytes, shared_bytes, depth, resident, max_vram, slot_cap)
+
+
 _ORIG_CACHE = X.cache_passes
+_ORIG_PLAN = Pol.plan_slots
 
 MUTATIONS = {
+    "window_one_short": (Pol, "issue_step", _window_one_short),
+    "window_one_long": (Pol, "issue_step", _window_one_long),
+    "window_ignores_resident_prefix": (Pol, "issue_step", _window_ignores_residents),
+    "window_counts_residents": (Pol, "issue_step", _window_counts_residents),
+    "ring_overlaps_residents": (Pol, "ring_slot", _ring_without_resident_offset),
+    "ring_one_slot_short": (Pol, "ring_slot", _ring_one_slot_short),
+    "plan_residents_before_depth": (Pol, "plan_slots", _plan_residents_first),
+    "plan_budget_rounds_up": (Pol, "plan_slots", _plan_budget_rounds_up),
     "replan_evicts_from_the_front": (Pol.Sim, "_evict_residents_down_to", _evict_ascending),
     "stale_prefetch_not_released": (Pol.Sim, "_release_carried", _release_silently),
     "hot_set_ties_to_high_index": (X, "hot_set", _hot_ties_high),
@@ -80,7 +135,7 @@ MUTATIONS = {
 def _pins():
     """Every pin of the two test modules, with the parameters they run with."""
     out = []
-    for mod in (TR, TX):
+    for mod in (TP, TR, TX):
         for name in dir(mod):
             fn = getattr(mod, name)
             if not name.startswith("test_") or not callable(fn):
@@ -99,11 +154,12 @@ def _pins():
 @pytest.mark.parametrize("name", sorted(MUTATIONS))
 def test_policy_mutation_is_caught(name, monkeypatch):
     target, attr, fn = MUTATIONS[name]
+    orig = getattr(target, attr)
     monkeypatch.setattr(target, attr, fn)
-    if target is X:  # the pin modules imported the functions by name
-        for mod in (TX,):
-            if hasattr(mod, attr):
-                monkeypatch.setattr(mod, attr, fn)
+    # the pin modules that imported the function by name see the planted one too
+    for mod in (TP, TR, TX):
+        if getattr(mod, attr, None) is orig:
+            monkeypatch.setattr(mod, attr, fn)
     caught = []
     for pname, pin, kw in _pins():
         try:

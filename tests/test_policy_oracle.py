@@ -147,8 +147,46 @@ def test_invariants_and_brute_force_grid():
             # every streamed segment is queued once per run when d >= 1
             if p.d >= 1:
                 assert len(_kinds(sim, 1, pol.PREFETCH)) == N - p.R
+            # the window, counted from the events: full, never past the run
+            brute.check_window(sim.events, N, p.R, p.d)
             n += 1
     assert n > 1000
+
+
+def test_window_counted_from_the_events_grid():
+    """Every plan of up to 7 segments, with and without the cross-run window: each streamed
+    segment is loaded once per run before its activation, and the loads ahead of the active
+    segment number min(d, streamed segments left), or d across the run boundary."""
+    n = 0
+    for N in range(1, 8):
+        for depth, resident, slots, cross, pool in itertools.product(
+                range(0, 6), range(-1, N + 1), range(1, N + 3), (False, True), (0, 1)):
+            sim, st = pol.simulate([100] * N, [], depth, resident, slots * 100, use_pool=pool, runs=3,
+                                   cross_run=cross)
+            assert all(s >= 0 for s in st)
+            p = sim.plan
+            brute.check_window(sim.events, N, p.R, p.d, cross)
+            assert brute.replay(sim.events, N, p.P) == p.P
+            n += 1
+    assert n > 6000
+
+
+def test_window_worked_example():
+    """N = 6, two residents, depth 2 (a hand-worked schedule): loads 0 and 1 of the ring
+    (segments 2 and 3) are issued at step 0, in the resident prefix; segment 4 enters the
+    window when segment 2 activates (step 2), segment 5 at step 3; the ring of three slots
+    2, 3, 4 is taken in turn."""
+    sim, st = pol.simulate([100] * 6, [], depth=2, resident=2, max_vram=500, use_pool=1, runs=1)
+    assert (sim.plan.R, sim.plan.d, sim.plan.Q, sim.plan.P) == (2, 2, 3, 5)
+    got = [(e[1], pol.KIND_NAMES[e[2]], e[3], e[4]) for e in sim.events]
+    assert got == [
+        (-1, "LOAD_RESIDENT", 0, 0), (-1, "LOAD_RESIDENT", 1, 1),
+        (0, "PREFETCH", 2, 2), (0, "PREFETCH", 3, 3), (0, "ACTIVATE", 0, 0),
+        (1, "ACTIVATE", 1, 1),
+        (2, "PREFETCH", 4, 4), (2, "ACTIVATE", 2, 2),
+        (3, "PREFETCH", 5, 2), (3, "ACTIVATE", 3, 3),
+        (4, "ACTIVATE", 4, 4),
+        (5, "ACTIVATE", 5, 2)]
 
 
 def test_runtime_pressure_evicts_from_the_end_of_the_prefix():
