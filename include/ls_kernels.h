@@ -64,9 +64,13 @@ ls_status lsk_copy_h2slot(void* dst_dev, const void* src_host, uint64_t bytes, i
  *     before any work is queued.
  *   - Sources must be pinned and mapped, sources, dst_dev and the offsets
  *     16-byte aligned (LS_ERR_INVALID_ARG otherwise).
- *   - The first call on a device looks up the array's device address with that
- *     device current (cudaGetSymbolAddress); make that first call before any
- *     stream capture.
+ *   - The first call on a device, and the first after that device's context has
+ *     been replaced (cudaDeviceReset), looks up the array's device address with
+ *     that device current (cudaGetSymbolAddress).
+ *   - A call whose stream is being captured into a CUDA graph returns
+ *     LS_ERR_INVALID_ARG before any work is queued: the range table is staged
+ *     from the call's own stack frame, which a replay would read again long after
+ *     the call has returned.
  *   - Every call shares the one array per device and each call overwrites it
  *     (the ticket is cleared by the call itself). Calls whose work overlaps on
  *     the GPU (different streams, no ordering between them) race on the array.
