@@ -880,33 +880,51 @@ ls_status autotune_copy(ls_ctx* c) {
     return LS_OK;
 }
 
+// Waits for the work this context queued: its passes' streams, the copy stream, the
+// host-buffer stream and the graph stream. Other streams of the device are not waited on.
+void sync_ctx_streams(ls_ctx* c) {
+    for (cudaStream_t s : c->pending) cudaStreamSynchronize(s);
+    for (cudaStream_t s : {c->copy_stream, c->own_stream, c->graph_stream})
+        if (s) cudaStreamSynchronize(s);
+}
+
+// Workspaces are stream-ordered allocations on the copy stream, so replacing them
+// never synchronises the whole device (a plain cudaFree would).
+void free_workspaces(ls_ctx* c) {
+    for (void** p : {&c->act[0], &c->act[1], &c->xb, (void**)&c->xf, &c->hbuf, &c->ubuf, &c->moe_xs, &c->moe_hs,
+                     (void**)&c->moe_sel, (void**)&c->moe_w, (void**)&c->moe_table, (void**)&c->moe_y})
+        if (*p) {
+            cudaFreeAsync(*p, c->copy_stream);
+            *p = nullptr;
+        }
+    c->ws_tokens = 0;
+}
+
 ls_status ensure_workspace(ls_ctx* c, int64_t T) {
     if (T <= c->ws_tokens) return LS_OK;
-    cudaDeviceSynchronize();
-    for (void** p : {&c->act[0], &c->act[1], &c->xb, (void**)&c->xf, &c->hbuf, &c->ubuf, &c->moe_xs, &c->moe_hs})
-        if (*p) { cudaFree(*p); *p = nullptr; }
-    for (void* p : {(void*)c->moe_sel, (void*)c->moe_w, (void*)c->moe_table, (void*)c->moe_y})
-        if (p) cudaFree(p);
-    c->moe_sel = nullptr; c->moe_w = nullptr; c->moe_table = nullptr; c->moe_y = nullptr;
+    sync_ctx_streams(c);   // no queued pass of this context uses the old workspaces any more
+    free_workspaces(c);
+    cudaStream_t a = c->copy_stream;
     if (c->N > 1 && c->kind == LS_KIND_LINEAR_GELU_F32) {
-        CK(cudaMalloc(&c->act[0], (size_t)T * c->H * 4));
-        CK(cudaMalloc(&c->act[1], (size_t)T * c->H * 4));
+        CK(cudaMallocAsync(&c->act[0], (size_t)T * c->H * 4, a));
+        CK(cudaMallocAsync(&c->act[1], (size_t)T * c->H * 4, a));
     } else if (c->N > 1) {
-        CK(cudaMalloc(&c->xb, (size_t)T * c->H * 2));
-        CK(cudaMalloc((void**)&c->xf, (size_t)T * c->H * 4));
+        CK(cudaMallocAsync(&c->xb, (size_t)T * c->H * 2, a));
+        CK(cudaMallocAsync((void**)&c->xf, (size_t)T * c->H * 4, a));
     }
     if (c->kind == LS_KIND_FFN_GELU_BF16 || c->kind == LS_KIND_FFN_GELU_SHARED_BF16 || c->kind == LS_KIND_SWIGLU_BF16)
-        CK(cudaMalloc(&c->hbuf, (size_t)T * c->F * 2));
-    if (c->kind == LS_KIND_FFN_GELU_SHARED_BF16) CK(cudaMalloc(&c->ubuf, (size_t)T * c->H * 2));
+        CK(cudaMallocAsync(&c->hbuf, (size_t)T * c->F * 2, a));
+    if (c->kind == LS_KIND_FFN_GELU_SHARED_BF16) CK(cudaMallocAsync(&c->ubuf, (size_t)T * c->H * 2, a));
     if (c->kind == LS_KIND_MOE_SWIGLU_BF16) {
         const int64_t rows = T * 8;
-        CK(cudaMalloc(&c->moe_sel, (size_t)c->N * rows * sizeof(int)));
-        CK(cudaMalloc(&c->moe_w, (size_t)c->N * rows * sizeof(float)));
-        CK(cudaMalloc(&c->moe_table, (size_t)c->N * rows * sizeof(int)));
-        CK(cudaMalloc(&c->moe_xs, (size_t)rows * c->H * 2));
-        CK(cudaMalloc(&c->moe_hs, (size_t)rows * c->F * 2));
-        CK(cudaMalloc(&c->moe_y, (size_t)rows * c->H * sizeof(float)));
+        CK(cudaMallocAsync((void**)&c->moe_sel, (size_t)c->N * rows * sizeof(int), a));
+        CK(cudaMallocAsync((void**)&c->moe_w, (size_t)c->N * rows * sizeof(float), a));
+        CK(cudaMallocAsync((void**)&c->moe_table, (size_t)c->N * rows * sizeof(int), a));
+        CK(cudaMallocAsync(&c->moe_xs, (size_t)rows * c->H * 2, a));
+        CK(cudaMallocAsync(&c->moe_hs, (size_t)rows * c->F * 2, a));
+        CK(cudaMallocAsync((void**)&c->moe_y, (size_t)rows * c->H * sizeof(float), a));
     }
+    CK(cudaStreamSynchronize(a));   // the new workspaces are usable on any stream
     c->ws_tokens = T;
     return LS_OK;
 }
@@ -1637,7 +1655,8 @@ ls_status ls_get_kernel_times(ls_ctx* c, ls_kernel_time* out, int32_t cap, int32
 static void release_resources(ls_ctx* c) {
     if (c->N > 0) {
         cudaSetDevice(c->device);
-        cudaDeviceSynchronize();
+        sync_ctx_streams(c);
+        free_workspaces(c);
         for (int s = 0; s < (int)c->seg_buf.size(); ++s)
             if (c->seg_buf[s]) dev_free(c, c->seg_buf[s], (size_t)c->segs[s].slot_bytes, c->copy_stream);
         if (c->pool) dev_free(c, c->pool, (size_t)c->pool_bytes, c->copy_stream);
@@ -1646,10 +1665,8 @@ static void release_resources(ls_ctx* c) {
         if (c->copy_stream) cudaStreamSynchronize(c->copy_stream);
         for (auto& sr : c->segs)
             if (sr.ranges_dev) cudaFree(sr.ranges_dev);
-        for (void* p : {(void*)c->ready, (void*)c->tickets, c->act[0], c->act[1], c->xb, (void*)c->xf, c->hbuf, c->ubuf,
-                        (void*)c->moe_sel, (void*)c->moe_w, (void*)c->moe_table, (void*)c->moe_bounds,
-                        (void*)c->moe_used, c->moe_xs, c->moe_hs, (void*)c->moe_y, c->stage_x, c->stage_y,
-                        (void*)c->stage_logits})
+        for (void* p : {(void*)c->ready, (void*)c->tickets, (void*)c->moe_bounds, (void*)c->moe_used, c->stage_x,
+                        c->stage_y, (void*)c->stage_logits})
             if (p) cudaFree(p);
         if (c->moe_used_host) cudaFreeHost(c->moe_used_host);
         if (c->ecache_rows_host) cudaFreeHost(c->ecache_rows_host);
