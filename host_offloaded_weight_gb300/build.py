@@ -20,7 +20,8 @@ INCLUDE = os.path.join(ROOT, "include")
 BUILD = os.path.join(PKG, "_build")
 LIB = os.path.join(PKG, "liblstream.so")
 ARCH = ["-gencode", "arch=compute_103a,code=sm_103a"]
-SOURCES = ["ls_sched.cpp", "runtime.cu", "k_copy.cu", "k_gemm.cu", "k_simt.cu", "k_moe.cu", "kapi.cu", "kapi_static.cu"]
+SOURCES = ["ls_sched.cpp", "runtime.cu", "k_copy.cu", "k_gemm.cu", "k_simt.cu", "k_moe.cu", "k_debug.cu", "kapi.cu",
+           "kapi_static.cu"]
 
 
 def _nvcc() -> str:

@@ -12,6 +12,7 @@ enum : uint32_t {
     DERR_HANDOFF_TIMEOUT = 0x01,  // a ready word stayed down (bits 8.. = slot)
     DERR_GEMM_TIMEOUT = 0x02,     // an mbarrier wait inside a GEMM ran out (bits 8.. = role)
     DERR_BAD_ARG = 0x03,          // a kernel found an argument it cannot handle
+    DERR_BOUNDS = 0x04,           // a debug check failed (bits 8.. = region or layer)
 };
 
 __device__ __forceinline__ uint64_t globaltimer_ns() {

@@ -77,9 +77,11 @@ __global__ void moe_route_kernel(const float* __restrict__ logits, int rows, int
 static constexpr int GROUP_THREADS = 1024;
 static constexpr int GROUP_WARPS = GROUP_THREADS / 32;
 
+// mask_all (may be NULL): [n_layers, E]; rows routed to an expert whose mask byte is 0 are
+// left out, so the table holds the kept rows only (bounds[E] = their count).
 __global__ void __launch_bounds__(GROUP_THREADS)
 moe_group_kernel(const int* __restrict__ sel_all, int T, int E, int k, int* __restrict__ table_all,
-                 int* __restrict__ bounds_all, uint8_t* __restrict__ used_all) {
+                 int* __restrict__ bounds_all, uint8_t* __restrict__ used_all, const uint8_t* __restrict__ mask_all) {
     extern __shared__ int sm[];
     int* counts = sm;                    // [E]
     int* bounds = counts + E;            // [E + 1]
@@ -88,11 +90,13 @@ moe_group_kernel(const int* __restrict__ sel_all, int T, int E, int k, int* __re
     const int n = T * k;
     const int* sel = sel_all + (int64_t)layer * n;
     int* table = table_all + (int64_t)layer * n;
+    const uint8_t* mask = mask_all ? mask_all + (int64_t)layer * E : nullptr;
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
     for (int i = threadIdx.x; i < E; i += blockDim.x) counts[i] = 0;
     for (int i = threadIdx.x; i < GROUP_WARPS * E; i += blockDim.x) cnt[i] = 0;
     __syncthreads();
-    for (int i = threadIdx.x; i < n; i += blockDim.x) atomicAdd(&counts[sel[i]], 1);
+    for (int i = threadIdx.x; i < n; i += blockDim.x)
+        if (!mask || mask[sel[i]]) atomicAdd(&counts[sel[i]], 1);
     __syncthreads();
     if (threadIdx.x == 0) {
         int acc = 0;
@@ -108,7 +112,7 @@ moe_group_kernel(const int* __restrict__ sel_all, int T, int E, int k, int* __re
     const unsigned lt = (1u << lane) - 1u;
     for (int b = c0; b < c1; b += 32) {
         const int i = b + lane;
-        const bool act = i < c1;
+        const bool act = i < c1 && (!mask || mask[sel[i]]);
         const int e = act ? sel[i] : -1 - lane;  // inactive lanes never match a real expert
         const unsigned peers = __match_any_sync(0xffffffffu, e);
         if (act && (peers & lt) == 0) cnt[warp * E + e] += __popc(peers);
@@ -127,7 +131,7 @@ moe_group_kernel(const int* __restrict__ sel_all, int T, int E, int k, int* __re
     __syncthreads();
     for (int b = c0; b < c1; b += 32) {
         const int i = b + lane;
-        const bool act = i < c1;
+        const bool act = i < c1 && (!mask || mask[sel[i]]);
         const int e = act ? sel[i] : -1 - lane;
         const unsigned peers = __match_any_sync(0xffffffffu, e);
         if (act) table[cnt[warp * E + e] + __popc(peers & lt)] = i;
@@ -177,6 +181,42 @@ __global__ void moe_combine_kernel(const void* __restrict__ x, int x_f32, const 
     if (out32) *reinterpret_cast<float4*>(out32 + idx) = o4;
 }
 
+// dst[dst_table ? dst_table[i] : i] = src[src_table ? src_table[i] : i] for i < rows, fp32
+// rows of H (H % 4 == 0) with 16-byte accesses; either side may be mapped pinned host
+// memory (the hand-off of result rows between two cards without peer access). With
+// `ready`, the last CTA raises ready[0] = epoch after a system fence, as the slot copy does.
+__global__ void moe_rows_copy_kernel(const float4* __restrict__ src, const int* __restrict__ src_table,
+                                     float4* __restrict__ dst, const int* __restrict__ dst_table, int rows, int h4,
+                                     uint32_t* ready, uint32_t* ticket, uint32_t epoch) {
+    for (int r = blockIdx.x; r < rows; r += gridDim.x) {
+        const int64_t si = src_table ? src_table[r] : r;
+        const int64_t di = dst_table ? dst_table[r] : r;
+        for (int i = threadIdx.x; i < h4; i += blockDim.x) dst[di * h4 + i] = src[si * h4 + i];
+    }
+    if (!ready) return;
+    __syncthreads();
+    if (threadIdx.x == 0) {
+        __threadfence_system();
+        const unsigned prev = atomicAdd(ticket, 1u);
+        if (prev == gridDim.x - 1) {
+            *ticket = 0;
+            __threadfence();
+            st_release_gpu(ready, epoch);
+        }
+    }
+}
+
+cudaError_t launch_moe_rows_copy(const float* src, const int* src_table, float* dst, const int* dst_table, int rows,
+                                 int H, uint32_t* ready, uint32_t* ticket, uint32_t epoch, int ctas, cudaStream_t s) {
+    if ((H % 4) != 0 || rows < 0 || (ready && !ticket)) return cudaErrorInvalidValue;
+    int grid = rows < ctas ? rows : ctas;
+    if (grid < 1) grid = 1;
+    moe_rows_copy_kernel<<<grid, 256, 0, s>>>(reinterpret_cast<const float4*>(src), src_table,
+                                              reinterpret_cast<float4*>(dst), dst_table, rows, H / 4, ready, ticket,
+                                              epoch);
+    return cudaGetLastError();
+}
+
 cudaError_t launch_moe_route(const float* logits, int n_layers, int T, int E, int k, int* sel,
                              float* weight, cudaStream_t s) {
     if (E < 1 || E > MOE_MAX_E || k < 1 || k > MOE_MAX_K || k > E) return cudaErrorInvalidValue;
@@ -189,7 +229,7 @@ cudaError_t launch_moe_route(const float* logits, int n_layers, int T, int E, in
 }
 
 cudaError_t launch_moe_group(const int* sel, int n_layers, int T, int E, int k, int* row_table,
-                             int* group_bounds, uint8_t* expert_used, cudaStream_t s) {
+                             int* group_bounds, uint8_t* expert_used, cudaStream_t s, const uint8_t* expert_mask) {
     if (E < 1 || E > MOE_MAX_E || n_layers <= 0) return cudaErrorInvalidValue;
     size_t smem = (size_t)(E + E + 1 + GROUP_WARPS * E) * sizeof(int);
     static size_t attr = 0;
@@ -199,7 +239,8 @@ cudaError_t launch_moe_group(const int* sel, int n_layers, int T, int E, int k, 
         if (e != cudaSuccess) return e;
         attr = smem;
     }
-    moe_group_kernel<<<n_layers, GROUP_THREADS, smem, s>>>(sel, T, E, k, row_table, group_bounds, expert_used);
+    moe_group_kernel<<<n_layers, GROUP_THREADS, smem, s>>>(sel, T, E, k, row_table, group_bounds, expert_used,
+                                                           expert_mask);
     return cudaGetLastError();
 }
 

@@ -1,6 +1,9 @@
 // Standalone C entry points of the device kernels (see ls_kernels.h).
 #include <cuda_runtime.h>
 
+#include <algorithm>
+#include <cmath>
+
 #include <mutex>
 
 #include "common.cuh"
@@ -161,6 +164,80 @@ ls_status lsk_moe_group(const int32_t* sel, int32_t n_layers, int32_t T, int32_t
     return st(launch_moe_group(sel, n_layers, T, E, k, row_table, group_bounds, expert_used, (cudaStream_t)stream));
 }
 
+ls_status lsk_moe_group_masked(const int32_t* sel, int32_t n_layers, int32_t T, int32_t E, int32_t k,
+                               const uint8_t* expert_mask, int32_t* row_table, int32_t* group_bounds,
+                               uint8_t* expert_used, void* stream) {
+    if (!sel || !expert_mask || !row_table || !group_bounds || T < 0 || k < 1) return LS_ERR_INVALID_ARG;
+    return st(launch_moe_group(sel, n_layers, T, E, k, row_table, group_bounds, expert_used, (cudaStream_t)stream,
+                               expert_mask));
+}
+
+// The device address of p: p itself for device memory, the mapped address for pinned host
+// memory; NULL when the device cannot reach p.
+static const void* device_address(const void* p) {
+    cudaPointerAttributes a;
+    if (cudaPointerGetAttributes(&a, p) != cudaSuccess) {
+        cudaGetLastError();
+        return nullptr;
+    }
+    if (a.type == cudaMemoryTypeDevice || a.type == cudaMemoryTypeManaged) return p;
+    if (a.type == cudaMemoryTypeHost) return a.devicePointer;
+    return nullptr;
+}
+
+ls_status lsk_moe_rows_copy(const float* src, const int32_t* src_table, float* dst, const int32_t* dst_table,
+                            int32_t rows, int32_t H, uint32_t* ready_dev, uint32_t* ticket_dev, uint32_t epoch,
+                            int32_t ctas, void* stream) {
+    if (!src || !dst || rows < 0 || H < 4 || (H % 4) || (ready_dev && !ticket_dev)) return LS_ERR_INVALID_ARG;
+    const float* s = static_cast<const float*>(device_address(src));
+    float* d = static_cast<float*>(const_cast<void*>(device_address(dst)));
+    if (!s || !d || ((uintptr_t)s & 15) || ((uintptr_t)d & 15)) return LS_ERR_INVALID_ARG;
+    const int c = ctas > 0 ? ctas : gemm_num_sms();
+    return st(launch_moe_rows_copy(s, src_table, d, dst_table, rows, H, ready_dev, ticket_dev, epoch, c,
+                                   (cudaStream_t)stream));
+}
+
+ls_status ls_host_alloc(uint64_t bytes, void** out) {
+    if (!out || bytes == 0) return LS_ERR_INVALID_ARG;
+    *out = nullptr;
+    if (cudaHostAlloc(out, (size_t)bytes, cudaHostAllocMapped | cudaHostAllocPortable) != cudaSuccess) {
+        cudaGetLastError();
+        *out = nullptr;
+        return LS_ERR_OOM;
+    }
+    return LS_OK;
+}
+
+ls_status ls_host_free(void* p) {
+    if (!p) return LS_OK;
+    if (cudaFreeHost(p) != cudaSuccess) {
+        cudaGetLastError();
+        return LS_ERR_INVALID_ARG;
+    }
+    return LS_OK;
+}
+
+double ls_helper_share(int64_t tokens) {
+    // "prefill: a layer split's idle card streams a share of a one-chunk prompt's experts",
+    // What: min(0.45, 0.5 - T/16384), off below 0.3
+    const double s = std::min(0.45, 0.5 - (double)tokens / 16384.0);
+    return s >= 0.3 ? s : 0.0;
+}
+
+ls_status ls_helper_split(const uint8_t* routed, int32_t E, double share, uint8_t* helper_mask) {
+    if (!routed || !helper_mask || E < 0 || !(share >= 0.0 && share <= 1.0)) return LS_ERR_INVALID_ARG;
+    int n = 0;
+    for (int e = 0; e < E; ++e) n += routed[e] != 0;
+    const int n_h = (int)std::floor(share * n);
+    // the helper takes the n_h highest-numbered routed experts
+    int left = n_h;
+    for (int e = E - 1; e >= 0; --e) {
+        helper_mask[e] = (routed[e] && left > 0) ? 1 : 0;
+        if (helper_mask[e]) --left;
+    }
+    return LS_OK;
+}
+
 ls_status lsk_moe_gather(const void* x, const int32_t* row_table, int32_t rows, int32_t k, int32_t H,
                          void* x_sorted, void* stream) {
     if (!x || !row_table || !x_sorted || rows < 0 || k < 1) return LS_ERR_INVALID_ARG;
@@ -171,6 +248,17 @@ ls_status lsk_moe_combine(const void* x, int32_t x_f32, const float* y, int32_t 
                           float* out32, void* stream) {
     if (!x || !y || !out || T < 0 || k < 1) return LS_ERR_INVALID_ARG;
     return st(launch_moe_combine(x, x_f32 != 0, y, T, k, H, out, out32, (cudaStream_t)stream));
+}
+
+ls_status lsk_moe_check(const int32_t* sel, const int32_t* table, const int32_t* bounds, int32_t n_layers, int32_t T,
+                        int32_t k, int32_t E, uint32_t* err_host, void* stream) {
+    if (!sel || !table || !bounds || !err_host || n_layers < 0 || T < 0 || k < 1 || E < 1) return LS_ERR_INVALID_ARG;
+    uint32_t* ed = nullptr;
+    if (cudaHostGetDevicePointer((void**)&ed, err_host, 0) != cudaSuccess) {
+        cudaGetLastError();
+        return LS_ERR_INVALID_ARG;
+    }
+    return st(launch_moe_check(sel, table, bounds, n_layers, T, k, E, ed, 0x20000u, (cudaStream_t)stream));
 }
 
 }  // extern "C"

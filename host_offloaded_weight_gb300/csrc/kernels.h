@@ -89,12 +89,31 @@ int gemm_pair_tile_n(int64_t M, int64_t N);
 // ---------------------------------------------------------------- MoE
 cudaError_t launch_moe_route(const float* logits, int n_layers, int T, int E, int k, int* sel,
                              float* weight, cudaStream_t s);
+// expert_mask (may be NULL): [n_layers, E]; rows of masked-out experts are left out of the table.
 cudaError_t launch_moe_group(const int* sel, int n_layers, int T, int E, int k, int* row_table,
-                             int* group_bounds, uint8_t* expert_used, cudaStream_t s);
+                             int* group_bounds, uint8_t* expert_used, cudaStream_t s,
+                             const uint8_t* expert_mask = nullptr);
+// Row hand-off: dst[dst_table ? dst_table[i] : i] = src[src_table ? src_table[i] : i] (fp32 rows
+// of H); with ready, the last CTA publishes ready[0] = epoch after a system fence.
+cudaError_t launch_moe_rows_copy(const float* src, const int* src_table, float* dst, const int* dst_table, int rows,
+                                 int H, uint32_t* ready, uint32_t* ticket, uint32_t epoch, int ctas, cudaStream_t s);
 cudaError_t launch_moe_gather(const void* x, const int* row_table, int rows, int k, int H,
                               void* x_sorted, cudaStream_t s);
 // out = x + sum_j y[t*k+j]; x bf16 (or fp32 with x_f32); out bf16, plus out32 fp32 if given
 cudaError_t launch_moe_combine(const void* x, bool x_f32, const float* y, int T, int k, int H, void* out,
                                float* out32, cudaStream_t s);
+
+// ---------------------------------------------------------------- debug checks
+// Canaries: `count` regions of CANARY_BYTES at base, base + stride, ...; fill writes the
+// pattern, check compares it and raises DERR_BOUNDS | (region0 + r) << 8 on a mismatch.
+constexpr int64_t CANARY_BYTES = 256;
+cudaError_t launch_canary(void* base, int64_t stride, int count, bool check, uint32_t* err_word,
+                          uint32_t region0, cudaStream_t s);
+// Validates a MoE routing of n_layers layers (sel [L, T*k], row_table [L, T*k], bounds
+// [L, E+1]): bounds start at 0, end at T*k and never decrease; the rows of group e are
+// the rows routed to expert e, in increasing order, so the table is a permutation of
+// 0..T*k-1. Reads only inside those arrays. Raises DERR_BOUNDS | (region0 + layer) << 8.
+cudaError_t launch_moe_check(const int* sel, const int* row_table, const int* bounds, int n_layers, int T,
+                             int k, int E, uint32_t* err_word, uint32_t region0, cudaStream_t s);
 
 }  // namespace ls

@@ -84,6 +84,10 @@ struct ls_ctx {
     void* shared_dev = nullptr;
     void* pool = nullptr;
     int64_t pool_bytes = 0;
+    int64_t slot_stride = 0;             // bytes between slots (slot size + canary with debug_checks)
+    int pool_slots = 0;
+    int64_t shared_bytes_dev = 0;        // the shared region's bytes before its canary
+    int64_t debug_violations = 0;
     std::vector<void*> seg_buf;          // pool off: current buffer of each segment
     uint32_t* ready = nullptr;           // [P] ready words
     uint32_t* tickets = nullptr;         // [P] last-CTA tickets
@@ -180,6 +184,11 @@ void set_err(ls_ctx* c, const char* fmt, ...) {
     va_end(ap);
     c->err = buf;
 }
+
+// Regions named by a canary violation (bits 8.. of the error word): pool slot i is i.
+constexpr uint32_t CANARY_REGION_SHARED = 0x8000;
+constexpr uint32_t CANARY_REGION_SEGMENT = 0x10000;  // + segment: a per-load buffer with the pool off
+constexpr uint32_t CHECK_REGION_MOE = 0x20000;       // + layer: that layer's MoE routing tables
 
 #define CK(call)                                                                      \
     do {                                                                              \
@@ -556,21 +565,40 @@ struct GpuExec : Executor {
     RunCtx rc;
     explicit GpuExec(ls_ctx* ctx) : c(ctx) { rc = RunCtx{nullptr, nullptr, 0, nullptr, 0}; }
 
+    // With debug_checks every allocation carries a canary after its last byte.
+    int64_t canary() const { return c->prm.debug_checks ? CANARY_BYTES : 0; }
     bool alloc_shared(int64_t bytes) override {
-        c->shared_dev = dev_alloc(c, (size_t)bytes, c->copy_stream);
+        c->shared_dev = dev_alloc(c, (size_t)(bytes + canary()), c->copy_stream);
+        c->shared_bytes_dev = bytes;
+        if (c->shared_dev && canary())
+            track(c, launch_canary((uint8_t*)c->shared_dev + bytes, 0, 1, false, nullptr, 0, c->copy_stream));
         return c->shared_dev != nullptr;
     }
     bool alloc_pool(int slots, int64_t slot_bytes) override {
-        c->pool = dev_alloc(c, (size_t)(slots * slot_bytes), c->copy_stream);
-        c->pool_bytes = slots * slot_bytes;
+        const int64_t stride = slot_bytes + canary();
+        c->pool = dev_alloc(c, (size_t)(slots * stride), c->copy_stream);
+        c->pool_bytes = slots * stride;
+        c->slot_stride = stride;
+        c->pool_slots = slots;
+        if (c->pool && canary())
+            track(c, launch_canary((uint8_t*)c->pool + slot_bytes, stride, slots, false, nullptr, 0, c->copy_stream));
         return c->pool != nullptr;
     }
     bool alloc_segment(int seg, int64_t bytes) override {
-        c->seg_buf[seg] = dev_alloc(c, (size_t)bytes, rc.s);
+        c->seg_buf[seg] = dev_alloc(c, (size_t)(bytes + canary()), rc.s);
+        if (c->seg_buf[seg] && canary())
+            track(c, launch_canary((uint8_t*)c->seg_buf[seg] + bytes, 0, 1, false, nullptr, 0, rc.s));
         return c->seg_buf[seg] != nullptr;
     }
+    // pool off: a per-load buffer's canary is checked right before the buffer is freed
+    void check_segment_canary(int seg, cudaStream_t s) {
+        if (!canary() || !c->seg_buf[seg]) return;
+        track(c, launch_canary((uint8_t*)c->seg_buf[seg] + c->segs[seg].slot_bytes, 0, 1, true, c->err_word_dev,
+                               CANARY_REGION_SEGMENT + (uint32_t)seg, s));
+    }
     void free_segment(int seg) override {
-        dev_free(c, c->seg_buf[seg], (size_t)c->segs[seg].slot_bytes, rc.s);
+        check_segment_canary(seg, rc.s);
+        dev_free(c, c->seg_buf[seg], (size_t)(c->segs[seg].slot_bytes + canary()), rc.s);
         c->seg_buf[seg] = nullptr;
     }
     void begin_run(int) override {}
@@ -582,7 +610,7 @@ struct GpuExec : Executor {
     }
     void load(int seg, int slot, int kind, int64_t) override {
         c->cur_seg = seg;
-        void* dst = c->prm.use_pool ? (uint8_t*)c->pool + (int64_t)slot * c->sched.plan().S : c->seg_buf[seg];
+        void* dst = c->prm.use_pool ? (uint8_t*)c->pool + (int64_t)slot * c->slot_stride : c->seg_buf[seg];
         const uint32_t epoch = ++c->slot_epoch[slot];
         c->seg_epoch[seg] = epoch;
         c->seg_ptr[seg] = dst;
@@ -610,13 +638,15 @@ struct GpuExec : Executor {
         track(c, cudaEventRecord(c->slot_free[slot], rc.s));
     }
     void evict(int seg, int) override {
-        dev_free(c, c->seg_buf[seg], (size_t)c->segs[seg].slot_bytes, rc.s);
+        check_segment_canary(seg, rc.s);
+        dev_free(c, c->seg_buf[seg], (size_t)(c->segs[seg].slot_bytes + canary()), rc.s);
         c->seg_buf[seg] = nullptr;
     }
     void free_pool() override {
         dev_free(c, c->pool, (size_t)c->pool_bytes, c->copy_stream);
         c->pool = nullptr;
         c->pool_bytes = 0;
+        c->pool_slots = 0;
     }
 };
 
@@ -668,6 +698,8 @@ ls_status check_params(const ls_params* p, ls_params* out, std::string* why) {
     if ((d.alloc_fn == nullptr) != (d.free_fn == nullptr)) { *why = "alloc_fn and free_fn go together"; return LS_ERR_INVALID_ARG; }
     if (d.cross_run_prefetch != 0 && d.cross_run_prefetch != 1) { *why = "cross_run_prefetch must be 0 or 1"; return LS_ERR_INVALID_ARG; }
     if (d.expert_cache_bytes < 0) { *why = "expert_cache_bytes < 0"; return LS_ERR_INVALID_ARG; }
+    if (d.debug_checks != 0 && d.debug_checks != 1) { *why = "debug_checks must be 0 or 1"; return LS_ERR_INVALID_ARG; }
+    if (d.test_corrupt_canary < 0) { *why = "test_corrupt_canary < 0"; return LS_ERR_INVALID_ARG; }
     *out = d;
     return LS_OK;
 }
@@ -812,6 +844,11 @@ ls_status build_ranges(ls_ctx* c, SegRec& sr) {
         chunk += std::max<int64_t>(1, copy_chunks_for(r.n16));
         v.push_back(r);
     }
+    for (auto& r : v)  // every range ends inside the slot (the layout is built above; a cheap guard)
+        if (r.dst_off < 0 || r.dst_off + r.n16 * 16 + r.tail > sr.slot_bytes) {
+            set_err(c, "internal: a copy range ends past its slot");
+            return LS_ERR_INVALID_ARG;
+        }
     sr.n_ranges = (int)v.size();
     sr.n_chunks = chunk;
     if (v.empty()) return LS_OK;
@@ -963,6 +1000,7 @@ const char* ls_status_string(ls_status s) {
         case LS_ERR_CUDA: return "CUDA error";
         case LS_ERR_STATE: return "call out of order";
         case LS_ERR_UNSUPPORTED: return "unsupported shape, kind or alignment";
+        case LS_ERR_BOUNDS: return "debug check failed (canary overwritten or invalid routing table)";
     }
     return "unknown status";
 }
@@ -1169,12 +1207,28 @@ static ls_status register_impl(ls_ctx* c, const ls_segment_desc* segs, int32_t n
     CK(cudaStreamSynchronize(c->copy_stream));
     st = autotune_copy(c);
     if (st != LS_OK) return st;
+    if (c->prm.debug_checks && c->prm.test_corrupt_canary > 0 && c->pool &&
+        c->prm.test_corrupt_canary <= c->pool_slots) {  // test hook: an overrun past one slot, made by the host
+        uint8_t* cn = (uint8_t*)c->pool + (int64_t)(c->prm.test_corrupt_canary - 1) * c->slot_stride + c->sched.plan().S;
+        CK(cudaMemset(cn, 0, 8));
+    }
     if (c->cuda_err != cudaSuccess) {
         set_err(c, "registration: %s", cudaGetErrorString(c->cuda_err));
         return LS_ERR_CUDA;
     }
     c->registered = true;
     return plan_st;
+}
+
+// params.debug_checks: compare the canaries of every pool slot and of the shared region, in
+// stream order after the pass's last kernel (copies in flight write inside their slots).
+static void check_canaries(ls_ctx* c, cudaStream_t s) {
+    if (c->pool && c->pool_slots > 0)
+        track(c, launch_canary((uint8_t*)c->pool + c->sched.plan().S, c->slot_stride, c->pool_slots, true,
+                               c->err_word_dev, 0, s));
+    if (c->shared_dev)
+        track(c, launch_canary((uint8_t*)c->shared_dev + c->shared_bytes_dev, 0, 1, true, c->err_word_dev,
+                               CANARY_REGION_SHARED, s));
 }
 
 static void destroy_graph(ls_ctx* c) {
@@ -1304,6 +1358,9 @@ static ls_status prepare_pass(ls_ctx* c, const void* x_dev, void* y_dev, int64_t
             CK(launch_moe_route(routing->logits, c->N, (int)tokens, E, k, c->moe_sel, c->moe_w, s));
             CK(launch_moe_group(c->moe_sel, c->N, (int)tokens, E, k, c->moe_table, c->moe_bounds, c->moe_used, s));
         }
+        if (c->prm.debug_checks)
+            CK(launch_moe_check(c->moe_sel, c->moe_table, c->moe_bounds, c->N, (int)tokens, k, E, c->err_word_dev,
+                                CHECK_REGION_MOE, s));
         CK(cudaMemcpyAsync(c->moe_used_host, c->moe_used, (size_t)c->N * E, cudaMemcpyDeviceToHost, s));
         CK(cudaStreamSynchronize(s));
         if (c->ecache_K > 0) {
@@ -1334,6 +1391,7 @@ ls_status ls_run_async(ls_ctx* c, const void* x_dev, void* y_dev, int64_t tokens
     GpuExec ex(c);
     ex.rc = RunCtx{x_dev, y_dev, tokens, s, (uint64_t)c->prm.wait_limit_ms * 1000000ull};
     ls_status rs = c->sched.run(ex, load_bytes.data());
+    if (c->prm.debug_checks) check_canaries(c, s);
     track(c, cudaEventRecord(c->run_done, s));
     if (rs < 0) set_err(c, "run %d: %s", c->sched.runs() - 1, ls_status_string(rs));
     return rs;
@@ -1488,6 +1546,21 @@ ls_status ls_sync(ls_ctx* c) {
                     c->prm.wait_limit_ms);
             return LS_ERR_HANDOFF_TIMEOUT;
         }
+        if ((ew & 0xff) == DERR_BOUNDS) {
+            ++c->debug_violations;
+            const uint32_t r = ew >> 8;
+            if (r >= CHECK_REGION_MOE)
+                set_err(c, "run %d: debug check failed: MoE row table or group bounds of layer %u are invalid",
+                        c->sched.runs() - 1, r - CHECK_REGION_MOE);
+            else if (r >= CANARY_REGION_SEGMENT)
+                set_err(c, "run %d: debug check failed: canary after the buffer of segment %u overwritten",
+                        c->sched.runs() - 1, r - CANARY_REGION_SEGMENT);
+            else if (r == CANARY_REGION_SHARED)
+                set_err(c, "run %d: debug check failed: canary after the shared region overwritten", c->sched.runs() - 1);
+            else
+                set_err(c, "run %d: debug check failed: canary after pool slot %u overwritten", c->sched.runs() - 1, r);
+            return LS_ERR_BOUNDS;
+        }
         set_err(c, "run %d: device error word 0x%x", c->sched.runs() - 1, ew);
         return LS_ERR_CUDA;
     }
@@ -1611,6 +1684,7 @@ ls_status ls_get_stats(ls_ctx* c, ls_stats* out) {
     s.graph_replays = c->graph_replays;
     s.expert_cache_hits = c->n_ecache_hits;
     s.expert_host_loads = c->n_ecache_host;
+    s.debug_violations = c->debug_violations;
     const uint32_t n = std::min<uint32_t>(out->struct_size, sizeof(s));
     memcpy(out, &s, n);
     out->struct_size = n;
@@ -1658,7 +1732,9 @@ static void release_resources(ls_ctx* c) {
         sync_ctx_streams(c);
         free_workspaces(c);
         for (int s = 0; s < (int)c->seg_buf.size(); ++s)
-            if (c->seg_buf[s]) dev_free(c, c->seg_buf[s], (size_t)c->segs[s].slot_bytes, c->copy_stream);
+            if (c->seg_buf[s])
+                dev_free(c, c->seg_buf[s], (size_t)(c->segs[s].slot_bytes + (c->prm.debug_checks ? CANARY_BYTES : 0)),
+                         c->copy_stream);
         if (c->pool) dev_free(c, c->pool, (size_t)c->pool_bytes, c->copy_stream);
         if (c->shared_dev) dev_free(c, c->shared_dev, 0, c->copy_stream);
         if (c->ecache) dev_free(c, c->ecache, (size_t)(c->ecache_K * c->ecache_eb), c->copy_stream);

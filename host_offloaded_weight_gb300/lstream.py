@@ -23,7 +23,7 @@ _lib = C.CDLL(LIB_PATH)
 LS_PARAMS_VERSION = 1
 LS_OK, LS_WARN_MANDATORY_SLOT, LS_WARN_SYNC_FALLBACK = 0, 1, 2
 LS_ERR_INVALID_ARG, LS_ERR_VERSION, LS_ERR_OOM = -1, -2, -3
-LS_ERR_HANDOFF_TIMEOUT, LS_ERR_CUDA, LS_ERR_STATE, LS_ERR_UNSUPPORTED = -4, -5, -6, -7
+LS_ERR_HANDOFF_TIMEOUT, LS_ERR_CUDA, LS_ERR_STATE, LS_ERR_UNSUPPORTED, LS_ERR_BOUNDS = -4, -5, -6, -7, -8
 LS_KIND_LINEAR_GELU_F32, LS_KIND_FFN_GELU_BF16, LS_KIND_FFN_GELU_SHARED_BF16 = 0, 1, 2
 LS_KIND_SWIGLU_BF16, LS_KIND_MOE_SWIGLU_BF16 = 3, 4
 LS_DTYPE_F32, LS_DTYPE_BF16 = 0, 1
@@ -44,7 +44,8 @@ class ls_params(C.Structure):
                 ("alloc_fn", ALLOC_FN), ("free_fn", FREE_FN), ("alloc_user", C.c_void_p),
                 ("test_alloc_cap_bytes", C.c_int64), ("test_fail_async", C.c_int32),
                 ("test_drop_publish", C.c_int32), ("kernel_timing", C.c_int32),
-                ("cross_run_prefetch", C.c_int32), ("expert_cache_bytes", C.c_int64)]
+                ("cross_run_prefetch", C.c_int32), ("expert_cache_bytes", C.c_int64),
+                ("debug_checks", C.c_int32), ("test_corrupt_canary", C.c_int32)]
 
 
 class ls_tensor_desc(C.Structure):
@@ -92,7 +93,7 @@ class ls_stats(C.Structure):
                 ("bytes_loaded", C.c_int64), ("copy_kernel_gbs", C.c_double),
                 ("copy_engine_gbs", C.c_double), ("graph_captures", C.c_int64),
                 ("graph_replays", C.c_int64), ("expert_cache_hits", C.c_int64),
-                ("expert_host_loads", C.c_int64)]
+                ("expert_host_loads", C.c_int64), ("debug_violations", C.c_int64)]
 
 
 _P = C.c_void_p
@@ -136,6 +137,13 @@ _sig = {
     "lsk_moe_group": (_I32, [_P, _I32, _I32, _I32, _I32, _P, _P, _P, _P]),
     "lsk_moe_gather": (_I32, [_P, _P, _I32, _I32, _I32, _P, _P]),
     "lsk_moe_combine": (_I32, [_P, _I32, _P, _I32, _I32, _I32, _P, _P, _P]),
+    "lsk_moe_check": (_I32, [_P, _P, _P, _I32, _I32, _I32, _I32, _P, _P]),
+    "lsk_moe_group_masked": (_I32, [_P, _I32, _I32, _I32, _I32, _P, _P, _P, _P, _P]),
+    "lsk_moe_rows_copy": (_I32, [_P, _P, _P, _P, _I32, _I32, _P, _P, _U32, _I32, _P]),
+    "ls_helper_share": (C.c_double, [_I64]),
+    "ls_host_alloc": (_I32, [_U64, C.POINTER(_P)]),
+    "ls_host_free": (_I32, [_P]),
+    "ls_helper_split": (_I32, [_P, _I32, C.c_double, _P]),
 }
 for _name, (_res, _args) in _sig.items():
     _f = getattr(_lib, _name)
@@ -470,6 +478,48 @@ def lsk_moe_group(sel, n_layers, T, E, k, row_table, group_bounds, expert_used=N
 
 def lsk_moe_gather(x, row_table, rows, k, H, x_sorted, stream=None) -> int:
     return _check(_lib.lsk_moe_gather(_ptr(x), _ptr(row_table), rows, k, H, _ptr(x_sorted), _stream(stream)))
+
+
+def lsk_moe_check(sel, row_table, group_bounds, n_layers: int, T: int, k: int, E: int, err_host,
+                  stream=None) -> int:
+    return _check(_lib.lsk_moe_check(_ptr(sel), _ptr(row_table), _ptr(group_bounds), n_layers, T, k, E,
+                                     _ptr(err_host), _stream(stream)))
+
+
+def lsk_moe_group_masked(sel, n_layers, T, E, k, expert_mask, row_table, group_bounds, expert_used=None,
+                         stream=None) -> int:
+    return _check(_lib.lsk_moe_group_masked(_ptr(sel), n_layers, T, E, k, _ptr(expert_mask), _ptr(row_table),
+                                            _ptr(group_bounds), _ptr(expert_used), _stream(stream)))
+
+
+def lsk_moe_rows_copy(src, dst, rows: int, H: int, src_table=None, dst_table=None, ready=None, ticket=None,
+                      epoch: int = 0, ctas: int = 0, stream=None) -> int:
+    return _check(_lib.lsk_moe_rows_copy(_ptr(src), _ptr(src_table), _ptr(dst), _ptr(dst_table), rows, H,
+                                         _ptr(ready), _ptr(ticket), epoch, ctas, _stream(stream)))
+
+
+def ls_host_alloc(nbytes: int) -> int:
+    """Pinned, device-mapped host memory of nbytes bytes (address as an int)."""
+    p = _P()
+    _check(_lib.ls_host_alloc(nbytes, C.byref(p)))
+    return p.value
+
+
+def ls_host_free(ptr: int) -> None:
+    _check(_lib.ls_host_free(ptr))
+
+
+def ls_helper_share(tokens: int) -> float:
+    return float(_lib.ls_helper_share(tokens))
+
+
+def ls_helper_split(routed, share: float):
+    """routed: uint8 numpy array [E] (nonzero = routed) -> the helper's mask, uint8 [E]."""
+    import numpy as np
+    r = np.ascontiguousarray(routed, dtype=np.uint8)
+    out = np.zeros_like(r)
+    _check(_lib.ls_helper_split(_ptr(r), r.size, share, _ptr(out)))
+    return out
 
 
 def lsk_moe_combine(x, y, T, k, H, out, out32=None, stream=None) -> int:

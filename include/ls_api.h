@@ -56,7 +56,9 @@ enum {
     LS_ERR_HANDOFF_TIMEOUT = -4, /* a ready word stayed down past wait_limit_ms; that run's output is invalid */
     LS_ERR_CUDA = -5,            /* a CUDA call failed; see ls_last_error */
     LS_ERR_STATE = -6,           /* call out of order (e.g. ls_run before ls_register_segments) */
-    LS_ERR_UNSUPPORTED = -7      /* shape or alignment the kernels do not handle */
+    LS_ERR_UNSUPPORTED = -7,     /* shape or alignment the kernels do not handle */
+    LS_ERR_BOUNDS = -8           /* params.debug_checks found a canary overwritten or an invalid MoE row
+                                    table; see ls_last_error (the run's output is invalid) */
 };
 
 /* Segment kinds: what one segment computes (x: [tokens, hidden] activations). */
@@ -135,9 +137,18 @@ typedef struct ls_params {
                                      experts: in each pass, the K (layer, expert) pairs routed in the most
                                      earlier passes (ties to the lower expert, then layer); a hot expert is
                                      copied in when its layer next loads it from the host, and a routed
-                                     expert found there is copied within device memory instead of over
-                                     the host link. Bits are unchanged; the schedule's load bytes count
+                                     expert found there is read in place by the grouped GEMMs instead of
+                                     crossing the host link. Bits are unchanged; the schedule's load bytes count
                                      the host copies only. */
+    int32_t debug_checks;         /* 1 = bounds checks that need no sanitizer: a 256-byte canary after every
+                                     pool slot, after the shared region and after every per-load buffer
+                                     (pool off), filled at allocation and verified after each ls_run (and
+                                     before a per-load buffer is freed); the MoE row table and group bounds
+                                     are validated on the device after routing. A violation fails the run
+                                     with LS_ERR_BOUNDS. Canaries are device memory beyond max_vram_bytes.
+                                     0 (default) = off */
+    int32_t test_corrupt_canary;  /* test hook (debug_checks only): N > 0 overwrites the canary of pool slot
+                                     N - 1 once, right after registration */
 } ls_params;
 
 /* One tensor of a segment: host memory owned by the caller, kept alive and
@@ -212,6 +223,7 @@ typedef struct ls_stats {
     int64_t graph_replays;     /* passes issued as a replay of the captured graph */
     int64_t expert_cache_hits; /* routed experts of streamed layers served from the expert cache */
     int64_t expert_host_loads; /* routed experts of streamed layers copied from the host */
+    int64_t debug_violations;  /* runs failed by params.debug_checks */
 } ls_stats;
 
 /* Per-kernel timing, accumulated over runs while params.kernel_timing is on.
@@ -368,6 +380,33 @@ ls_status ls_simulate(const ls_params* params, const int64_t* seg_slot_bytes, in
                       const int64_t* shared_bytes, const int32_t* shared_ids, int32_t n_shared,
                       int32_t runs, const int64_t* load_bytes, ls_sched_event* events,
                       int64_t cap, int64_t* n_events, ls_stats* stats, ls_status* run_status);
+
+/* Pinned, device-mapped host memory for segment tensors (no counterpart on the pages,
+ * which pin the caller's memory; this is the driver's own pinned allocation, portable
+ * across devices). Memory from ls_host_alloc is used as is by ls_register_segments (it is
+ * not registered again). ls_host_alloc: LS_ERR_OOM when the driver refuses;
+ * ls_host_free(NULL) does nothing; freeing memory a context still uses is undefined. */
+ls_status ls_host_alloc(uint64_t bytes, void** out);
+ls_status ls_host_free(void* p);
+
+/* Idle-stage helper of a two-stage layer split ("prefill: a layer split's idle card
+ * streams a share of a one-chunk prompt's experts", Strata #663, What). While one stage
+ * computes its MoE layers the other card idles; it takes a share of each layer's routed
+ * experts, streams them over its own host link, computes their (token, k) rows and hands
+ * the rows back through mapped host memory (lsk_moe_group_masked, lsk_moe_rows_copy and
+ * lsk_wait_ready in ls_kernels.h are the device steps). Each row is computed on one card
+ * by the same kernels, so the combined layer has the bits of the unsplit one. Measured on
+ * one GPU only: the two cards' steps run one after the other there.
+ *
+ * ls_helper_share: the share for a one-chunk prompt of `tokens` tokens,
+ * min(0.45, 0.5 - tokens/16384), and 0 (helper off) when that is below 0.3. */
+double ls_helper_share(int64_t tokens);
+
+/* Which of a layer's routed experts the helper takes: routed[E] (nonzero = routed in this
+ * pass, host memory) -> helper_mask[E] (1 = the helper's, host memory). The helper takes
+ * floor(share * routed count) experts, the highest-numbered routed ones; the active card
+ * keeps the others. LS_ERR_INVALID_ARG for NULL pointers, E < 0 or share outside [0, 1]. */
+ls_status ls_helper_split(const uint8_t* routed, int32_t E, double share, uint8_t* helper_mask);
 
 #ifdef __cplusplus
 }

@@ -134,6 +134,28 @@ ls_status lsk_moe_group(const int32_t* sel_dev, int32_t n_layers, int32_t T, int
                         int32_t* row_table_dev, int32_t* group_bounds_dev, uint8_t* expert_used_dev,
                         void* stream);
 
+/* lsk_moe_group over a subset of the experts: expert_mask_dev [n_layers, E] (1 = keep);
+ * rows routed to a masked-out expert are left out, so row_table holds only the kept rows,
+ * still grouped by expert in (token, k) order, and group_bounds[E] is their count. The
+ * split of a layer between the active card and the idle-stage helper (see
+ * ls_helper_split): each card groups the rows of its own experts. */
+ls_status lsk_moe_group_masked(const int32_t* sel_dev, int32_t n_layers, int32_t T, int32_t E, int32_t k,
+                               const uint8_t* expert_mask_dev, int32_t* row_table_dev, int32_t* group_bounds_dev,
+                               uint8_t* expert_used_dev, void* stream);
+
+/* Hand-off of fp32 result rows (H floats each, H % 4 == 0): for i < rows,
+ * dst[dst_table ? dst_table[i] : i] = src[src_table ? src_table[i] : i], with 16-byte
+ * loads and stores ("prefill: a layer split's idle card streams a share of a one-chunk
+ * prompt's experts", What: result rows go through mapped host memory and are read by
+ * copy kernels on the device that needs them). src and dst are device memory or pinned,
+ * mapped host memory (host pointers are translated); tables are device int32 arrays or
+ * NULL. With ready_dev, the last CTA raises ready_dev[0] = epoch after a system fence
+ * (ticket_dev: one zeroed uint32, left at 0), so a reader can lsk_wait_ready on it.
+ * ctas <= 0: one per SM. */
+ls_status lsk_moe_rows_copy(const float* src, const int32_t* src_table, float* dst, const int32_t* dst_table,
+                            int32_t rows, int32_t H, uint32_t* ready_dev, uint32_t* ticket_dev, uint32_t epoch,
+                            int32_t ctas, void* stream);
+
 /* x_sorted[i] = x[row_table[i] / k] for i < rows; bf16 rows of H (H % 8 == 0). */
 ls_status lsk_moe_gather(const void* x_dev, const int32_t* row_table_dev, int32_t rows, int32_t k, int32_t H,
                          void* x_sorted_dev, void* stream);
@@ -142,6 +164,17 @@ ls_status lsk_moe_gather(const void* x_dev, const int32_t* row_table_dev, int32_
  * x is bf16, or fp32 when x_f32 != 0; out32_dev (may be NULL) gets the fp32 sum. */
 ls_status lsk_moe_combine(const void* x_dev, int32_t x_f32, const float* y_dev, int32_t T, int32_t k, int32_t H,
                           void* out_dev, float* out32_dev, void* stream);
+
+/* The routing check of params.debug_checks (no counterpart on the pages; it stands in for
+ * a memory sanitizer). For n_layers layers of a MoE routing - sel_dev [L, T*k] int32 (the
+ * expert of row t*k + j), row_table_dev [L, T*k] int32 and group_bounds_dev [L, E+1] int32
+ * as lsk_moe_group writes them - it checks that the bounds run from 0 to T*k without
+ * decreasing and that group e holds exactly the rows routed to expert e, in increasing
+ * order. It only reads the three arrays; an invalid layer sets err_host[0] (pinned, mapped
+ * host memory) = 4 | ((0x20000 + layer) << 8) if it is still 0. Returns LS_OK once
+ * queued; the verdict is in err_host after the stream drains. */
+ls_status lsk_moe_check(const int32_t* sel_dev, const int32_t* row_table_dev, const int32_t* group_bounds_dev,
+                        int32_t n_layers, int32_t T, int32_t k, int32_t E, uint32_t* err_host, void* stream);
 
 #ifdef __cplusplus
 }
