@@ -1,12 +1,14 @@
 #!/usr/bin/env python
 """Layer-streamed execution benchmark (one JSON line on stdout, rank 0).
 
-Workload (default): the 12-segment DiT-style FFN stack — each segment a bf16
-linear 1024->4096 + GELU + linear 4096->1024 + residual (16.8 MB of parameters),
-4096 tokens — with its parameters in pinned host memory, prefetch depth 1, no
-residents, a two-slot pool. One step = one streamed pass over all 12 segments
-(every segment's parameters cross the host link again). Inputs are synthetic
-(seeded N(0,1) activations, N(0, 1/sqrt(fan_in)) weights).
+Workload (default): the 48-layer MoE prefill stack - per layer 128 experts, each
+a bf16 SwiGLU 2048->768->2048 (9.4 MB), top-8 routing of 2048 tokens from N(0,1)
+router logits - with its 58 GB of experts in pinned host memory, prefetch depth 1,
+no residents, a two-slot pool of 1.2 GB slots. One step = one streamed pass over
+all 48 layers: each layer's routed experts cross the host link again, tokens are
+grouped by expert and run through the grouped GEMMs. The other stacks run with
+--workload. Inputs are synthetic (seeded N(0,1) activations, N(0, 1/sqrt(fan_in))
+weights).
 
   python bench.py [--gpus N] [--steps K] [--warmup W] [--impl ours|reference]
 
@@ -155,35 +157,64 @@ def aggregate(step_seconds: float, units: float, world: int, device=None) -> tup
 
 
 # ---------------------------------------------------------------- oracle (CPU) timing
-class OracleRun:
-    """The fp64 oracle forward of the first `tokens` rows through every segment.
+# Bounded samples of each workload for the CPU oracle: (token rows, leading segments).
+# Rows are independent in every kind and all segments of a stack have the same shapes,
+# so the time of a sample scales to the whole stack by n_segments / segments sampled.
+CPU_SAMPLE = {"tiny_f32_4x256": (8, None), "dit_ffn_12x1024x4096": (1024, None),
+              "shared_proj_24x3072x12288": (256, 4), "swiglu_48x5120x13824": (512, 2),
+              "moe_48x128x2048x768": (256, 1)}
+REF_SAMPLE = {"tiny_f32_4x256": (8, None), "dit_ffn_12x1024x4096": (256, None),
+              "shared_proj_24x3072x12288": (64, 2), "swiglu_48x5120x13824": (128, 1),
+              "moe_48x128x2048x768": (128, 1)}
 
-    Only the oracle's arithmetic is timed: drawing the weights and widening them
-    to fp64 happen per segment before its timer starts (and are kept between
-    passes when the widened stack fits in CACHE_BYTES). For the MoE stack the
-    routed experts of the sampled rows are widened before the layer's timer."""
+
+class OracleRun:
+    """The fp64 oracle forward of the first `tokens` rows through the first `layers`
+    segments of the stack.
+
+    Only the oracle's arithmetic is timed: drawing the weights (or taking them from
+    `hs`, the host stack the GPU streams from) and widening them to fp64 happen per
+    segment before its timer starts, and the widened segments are kept between passes
+    while they fit in CACHE_BYTES. For the MoE kind only the experts routed by the
+    sampled rows are widened."""
     CACHE_BYTES = 8 << 30
 
-    def __init__(self, cfg, tokens: int):
+    def __init__(self, cfg, tokens: int, layers=None, hs=None):
         from oracle import forward as F
         from oracle import stack as ostack
-        self.cfg, self.F, self.ostack = cfg, F, ostack
+        self.cfg, self.F, self.ostack, self.hs = cfg, F, ostack, hs
+        self.layers = cfg.n_segments if layers is None else min(layers, cfg.n_segments)
         self.rows = np.arange(tokens)
         self.x0 = F.as_f64(synth.draw_x(cfg, tokens), cfg.dtype)
         self.shared = ostack.shared_f64(cfg)[0] if cfg.kind == synth.KIND_FFN_GELU_SHARED_BF16 else None
         per_seg = sum(t.numel for t in synth.segment_tensors(cfg)) * 8
-        self.cache = {} if per_seg * cfg.n_segments <= self.CACHE_BYTES else None
+        self.cache = {} if per_seg * self.layers <= self.CACHE_BYTES else None
+        self.moe = {}
+        if cfg.kind == synth.KIND_MOE_SWIGLU_BF16:
+            for s in range(self.layers):
+                logits = synth.draw_logits(cfg, s)[self.rows]
+                sel, _ = F.route_topk(logits, cfg.top_k)
+                self.moe[s] = (logits, [int(e) for e in np.unique(sel)])
+
+    @property
+    def scale(self) -> float:
+        """Whole-stack time over sample time (segments of one stack share their shapes)."""
+        return self.cfg.n_segments / self.layers
 
     def _prepare(self, s):
         if self.cache is not None and s in self.cache:
             return self.cache[s]
-        cfg, F = self.cfg, self.F
+        cfg = self.cfg
         if cfg.kind == synth.KIND_MOE_SWIGLU_BF16:
-            logits = synth.draw_logits(cfg, s)[self.rows]
-            sel, _ = F.route_topk(logits, cfg.top_k)
-            experts = {int(e): [F.as_f64(a, "bf16") for a in synth.draw_expert(cfg, s, int(e))]
-                       for e in np.unique(sel)}
+            logits, routed = self.moe[s]
+            experts = {}
+            for e in routed:
+                bits = self.hs.seg_views[s][3 * e:3 * e + 3] if self.hs is not None else synth.draw_expert(cfg, s, e)
+                experts[e] = [self.F.as_f64(np.asarray(b), "bf16") for b in bits]
             out = (logits, experts)
+        elif self.hs is not None:
+            out = [self.F.as_f64(np.asarray(a), sp.dtype)
+                   for a, sp in zip(self.hs.seg_views[s], synth.segment_tensors(cfg))]
         else:
             out = self.ostack.segment_f64(cfg, s)
         if self.cache is not None:
@@ -191,41 +222,50 @@ class OracleRun:
         return out
 
     def time_pass(self) -> float:
-        cfg, x, total = self.cfg, self.x0, 0.0
-        for s in range(cfg.n_segments):
+        """Seconds of the oracle's arithmetic over the sample."""
+        cfg, F, x, total = self.cfg, self.F, self.x0, 0.0
+        for s in range(self.layers):
             prep = self._prepare(s)
             t0 = time.perf_counter()
             if cfg.kind == synth.KIND_MOE_SWIGLU_BF16:
                 logits, experts = prep
-                x = self.F.moe_swiglu(x, logits, lambda e: experts[e], cfg.top_k)
+                x = F.moe_swiglu(x, logits, experts.__getitem__, cfg.top_k)
             else:
                 x = self.ostack.apply_segment(cfg, s, x, rows=self.rows, tensors=prep, shared=self.shared)
             total += time.perf_counter() - t0
         return total
 
-
-def oracle_time(cfg, tokens: int) -> tuple:
-    """(seconds of one oracle pass over `tokens` rows, cores used)."""
-    return OracleRun(cfg, tokens).time_pass(), len(os.sched_getaffinity(0))
+    def describe(self) -> str:
+        what = f"{len(self.rows)} of {self.cfg.tokens} tokens through "
+        if self.layers == self.cfg.n_segments:
+            what += f"all {self.cfg.n_segments} segments"
+        else:
+            what += (f"the first {self.layers} of {self.cfg.n_segments} segments (same shapes), "
+                     f"time scaled by {self.scale:g}")
+        what += ", fp64; weight drawing and widening not timed"
+        if self.cfg.kind == synth.KIND_MOE_SWIGLU_BF16:
+            what += " (only the routed experts of the sampled rows are widened)"
+        return what
 
 
 def run_reference(args, cfg, world, rank):
     if rank != 0:
         return 0
-    tokens = args.ref_tokens
-    run = OracleRun(cfg, tokens)
+    tokens, layers = REF_SAMPLE.get(cfg.name, (256, None))
+    tokens = args.ref_tokens or tokens
+    run = OracleRun(cfg, tokens, layers)
     for _ in range(args.warmup):
         run.time_pass()
-    secs = [run.time_pass() for _ in range(args.steps)]
+    secs = [run.time_pass() * run.scale for _ in range(args.steps)]
     cores = len(os.sched_getaffinity(0))
     mean = statistics.mean(secs)
     value = tokens / mean
-    sample = f"{tokens} of {cfg.tokens} tokens through all {cfg.n_segments} segments per step (rows are independent)"
     line = {"impl": "reference", "metric": METRIC, "value": value, "unit": UNIT, "n_gpus": args.gpus,
             "steps": args.steps, "warmup": args.warmup, "ms_per_step": mean * 1e3, "higher_is_better": True,
             "scaling": "weak", "vs_baseline": None, "dtype": "f64", "data": "synthetic",
             "config": {"workload": cfg.name, "tokens": cfg.tokens, "segments": cfg.n_segments},
-            "cpu_baseline": {"value": value, "unit": UNIT, "cores": cores, "kind": "oracle", "sample": sample},
+            "cpu_baseline": {"value": value, "unit": UNIT, "cores": cores, "kind": "oracle",
+                             "sample": run.describe()},
             "e2e": {"value": value, "unit": UNIT, "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0}}
     print(json.dumps(line), flush=True)
     return 0
@@ -282,9 +322,86 @@ def write_timeline(path, L, ctx, x, y, T, s, logits, cfg):
                 f.write(f"{seg} | {name} | {'copy' if stream else 'compute'} | {a:.3f} | {b:.3f} | {b - a:.3f}\n")
 
 
+def time_alone(torch, L, cfg, hs, x, logits, reps=20) -> dict:
+    """{kernel class: average ms per launch} of a stack's GEMMs timed alone, at the workload's
+    shapes: back-to-back launches on one stream between one pair of CUDA events, operands
+    rotated over enough sets (more than twice the L2 together) that every launch reads its
+    inputs from DRAM. MoE: two layers' experts copied from the host stack and routed by their
+    own logits; dense kinds: random bf16 operands of the segment's shapes."""
+    dev = x.device
+    T, H, F = cfg.tokens, cfg.hidden, cfg.ffn
+    l2 = 2 * L2_BYTES
+    bf = torch.bfloat16
+    launches = {}
+    if cfg.kind == synth.KIND_MOE_SWIGLU_BF16:
+        E, k = cfg.n_experts, cfg.top_k
+        seg = synth.segment_slot_bytes(cfg)
+        n = 2
+        rows = T * k
+        W = [torch.from_numpy(hs.buffer[l * seg:(l + 1) * seg]).to(dev) for l in range(n)]
+        sel = torch.empty(n, rows, dtype=torch.int32, device=dev)
+        w = torch.empty(n, rows, dtype=torch.float32, device=dev)
+        table = torch.empty(n, rows, dtype=torch.int32, device=dev)
+        bounds = torch.empty(n, E + 1, dtype=torch.int32, device=dev)
+        L.lsk_moe_route(logits[:n].contiguous(), n, T, E, k, sel, w)
+        L.lsk_moe_group(sel, n, T, E, k, table, bounds)
+        xs = [torch.empty(rows, H, dtype=bf, device=dev) for _ in range(n)]
+        hsd = [torch.empty(rows, F, dtype=bf, device=dev) for _ in range(n)]
+        y = [torch.empty(rows, H, dtype=torch.float32, device=dev) for _ in range(n)]
+        for l in range(n):
+            L.lsk_moe_gather(x, table[l], rows, k, H, xs[l])
+        eb = seg // E
+        launches["gemm_up"] = lambda i: L.lsk_gemm_grouped_bf16(
+            L.LSK_EPI_SWIGLU, xs[i % n], W[i % n], seg // (2 * H), 0, eb // (2 * H), F, bounds[i % n], E,
+            hsd[i % n], rows, F, H)
+        launches["gemm_down"] = lambda i: L.lsk_gemm_grouped_bf16(
+            L.LSK_EPI_SCALE_F32, hsd[i % n], W[i % n], seg // (2 * F), 2 * H, eb // (2 * F), 0, bounds[i % n], E,
+            y[i % n], rows, H, F, row_table=table[i % n], row_weight=w[i % n])
+    elif cfg.kind != synth.KIND_LINEAR_GELU_F32:
+        g = torch.Generator(device=dev).manual_seed(0)
+
+        def rnd(*shape, dtype=bf):
+            return torch.randn(*shape, device=dev, generator=g).to(dtype)
+        swiglu = cfg.kind == synth.KIND_SWIGLU_BF16
+        up_bytes = 2 * (T * H + (2 if swiglu else 1) * F * H + T * F)
+        dn_bytes = 2 * (T * F + H * F) + 12 * T * H
+        nu, nd = -(-l2 // up_bytes), -(-l2 // dn_bytes)
+        ups = [(rnd(T, H), rnd((2 if swiglu else 1) * F, H), rnd(F), torch.empty(T, F, dtype=bf, device=dev))
+               for _ in range(nu)]
+        dns = [(rnd(T, F), rnd(H, F), rnd(H), rnd(T, H, dtype=torch.float32), torch.empty(T, H, dtype=bf, device=dev),
+                torch.empty(T, H, dtype=torch.float32, device=dev)) for _ in range(nd)]
+        if swiglu:
+            launches["gemm_up"] = lambda i: L.lsk_gemm_bf16(L.LSK_EPI_SWIGLU, ups[i % nu][0], ups[i % nu][1],
+                                                            ups[i % nu][3], T, F, H, b_rows=2 * F, b2_row_off=F)
+            launches["gemm_down"] = lambda i: L.lsk_gemm_bf16(L.LSK_EPI_RESID, dns[i % nd][0], dns[i % nd][1],
+                                                              dns[i % nd][4], T, H, F, resid=dns[i % nd][3],
+                                                              C32=dns[i % nd][5])
+        else:
+            launches["gemm_up"] = lambda i: L.lsk_gemm_bf16(L.LSK_EPI_BIAS_GELU, ups[i % nu][0], ups[i % nu][1],
+                                                            ups[i % nu][3], T, F, H, bias=ups[i % nu][2])
+            launches["gemm_down"] = lambda i: L.lsk_gemm_bf16(L.LSK_EPI_BIAS_RESID, dns[i % nd][0], dns[i % nd][1],
+                                                              dns[i % nd][4], T, H, F, bias=dns[i % nd][2],
+                                                              resid=dns[i % nd][3], C32=dns[i % nd][5])
+    out = {}
+    s = torch.cuda.current_stream()
+    for name, fn in launches.items():
+        for i in range(3):
+            fn(i)
+        e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        torch.cuda.synchronize()
+        e0.record(s)
+        for i in range(reps):
+            fn(i)
+        e1.record(s)
+        e1.synchronize()
+        out[name] = e0.elapsed_time(e1) / reps
+    return out
+
+
 def run_ours(args, cfg, world, rank, local):
     import torch
     from host_offloaded_weight_gb300 import lstream as L
+    from host_offloaded_weight_gb300.profiling import traffic
 
     torch.cuda.set_device(local)
     dev = torch.device("cuda", local)
@@ -366,9 +483,11 @@ def run_ours(args, cfg, world, rank, local):
     # segment compute spans: the same K passes with events only around each segment's
     # compute kernels (after the hand-off wait) and the copies; launches keep programmatic
     # dependent launch, so a span shows the kernels as the throughput passes run them
-    L.ls_set_kernel_timing(ctx, 3)
-    timed_passes()
-    spans = L.ls_get_kernel_times(ctx, reset=True)
+    spans = {}
+    if cfg.kind in (synth.KIND_FFN_GELU_BF16, synth.KIND_SWIGLU_BF16):
+        L.ls_set_kernel_timing(ctx, 3)
+        timed_passes()
+        spans = L.ls_get_kernel_times(ctx, reset=True)
     L.ls_set_kernel_timing(ctx, 0)
     if args.timeline and rank == 0:
         write_timeline(args.timeline, L, ctx, x, y, T, s, logits, cfg)
@@ -395,6 +514,7 @@ def run_ours(args, cfg, world, rank, local):
     h2d = xh.numel() * xh.element_size() + (lh.numel() * 4 if lh is not None else 0)
     d2h = yh.numel() * yh.element_size()
     L.ls_get_kernel_times(ctx, reset=True)
+    alone = time_alone(torch, L, cfg, hs, x, logits) if not args.no_alone else {}
     # --- kernels: live averages over the timed region
     kt = {k: {"launches": n, "avg_ms": ms / max(n, 1), "total_ms": ms} for k, (n, ms) in ktimes.items()}
     # kernels of this library launched in the timed region (a copy-engine load raises its
@@ -409,33 +529,42 @@ def run_ours(args, cfg, world, rank, local):
     if cfg.kind == synth.KIND_MOE_SWIGLU_BF16:   # experts a streamed layer moves, on average
         routed = per_load / (sum(t.nbytes for t in synth.segment_tensors(cfg)) / cfg.n_experts)
     kb = kernel_bytes(cfg, T, routed)
-    def roof(name):
+    def roof(name, avg_ms=None):
+        avg_ms = kt[name]["avg_ms"] if avg_ms is None else avg_ms
         if name in ("copy_h2slot", "copy_engine"):
-            ach = per_load / (kt[name]["avg_ms"] * 1e-3) / 1e9
+            ach = per_load / (avg_ms * 1e-3) / 1e9
             return {"kernel": name, "bound": "host_link", "achieved": ach, "peak": link_peak, "unit": "GB/s",
-                    "frac": ach / link_peak, "traffic": TRAFFIC.get((cfg.name, name)),
+                    "frac": ach / link_peak, "traffic": traffic(cfg.name, name),
                     "peak_source": "pinned copy-engine H2D, 1 GiB, best of 10, measured in this run"}
         if name == "linear_gelu_f32":   # CUDA-core FMA: 152 SMs x 128 lanes x 2 FLOP x max clock
             peak = 152 * 128 * 2 * 2.07e9 / 1e12
-            ach = seg_flops(cfg, T) / (kt[name]["avg_ms"] * 1e-3) / 1e12
+            ach = seg_flops(cfg, T) / (avg_ms * 1e-3) / 1e12
             return {"kernel": name, "bound": "alu", "achieved": ach, "peak": peak, "unit": "TFLOP/s",
-                    "frac": ach / peak, "traffic": TRAFFIC.get((cfg.name, name)),
+                    "frac": ach / peak, "traffic": traffic(cfg.name, name),
                     "peak_source": "fp32 FMA lanes x clock (152 x 128 x 2 x 2.07 GHz)"}
         if name in kf:
             # below the ridge (FLOP per byte under peak FLOP/s over peak bytes/s) a launch is
             # bound by HBM: the MoE layers' expert GEMMs, ~128 rows per expert
-            sec = kt[name]["avg_ms"] * 1e-3
+            sec = avg_ms * 1e-3
             if kf[name] / kb[name] < tc_peak * 1e12 / (hbm_peak * 1e9):
                 ach = kb[name] / sec / 1e9
                 return {"kernel": name, "bound": "hbm", "achieved": ach, "peak": hbm_peak, "unit": "GB/s",
-                        "frac": ach / hbm_peak, "traffic": TRAFFIC.get((cfg.name, name)),
+                        "frac": ach / hbm_peak, "traffic": traffic(cfg.name, name),
                         "algorithmic_bytes": kb[name], "peak_source": f"hbm_gbs ({peak_src})"}
             ach = kf[name] / sec / 1e12
             return {"kernel": name, "bound": "tensor", "achieved": ach, "peak": tc_peak, "unit": "TFLOP/s",
-                    "frac": ach / tc_peak, "traffic": TRAFFIC.get((cfg.name, name)),
+                    "frac": ach / tc_peak, "traffic": traffic(cfg.name, name),
                     "peak_source": f"bf16_tflops ({peak_src})"}
         return None
     roofline = roof(dominant) if dominant else None
+    # the same kernels timed alone (back to back, inputs from DRAM): no launch delay or
+    # copy-engine traffic in the event brackets
+    roofline_alone = None
+    if alone:
+        roofline_alone = {k: dict(roof(k, ms), avg_ms=ms) for k, ms in alone.items()}
+        for v in roofline_alone.values():
+            v["measured"] = ("kernel alone: 20 launches back to back between one pair of CUDA events, operands "
+                             "rotated over sets larger than twice the L2")
     # the dense stacks' segment compute as the throughput passes run it (GEMMs back to back
     # with programmatic dependent launch, the next segment's copy running meanwhile)
     segment_compute = None
@@ -470,6 +599,7 @@ def run_ours(args, cfg, world, rank, local):
         "link_frac": link_bytes / mean_s / 1e9 / link_peak,
         "bytes_per_step": link_bytes, "flops_per_step": flops,
         "roofline": roofline,
+        "roofline_alone": roofline_alone,
         "roofline_gemm": roof(gemm_name) if gemm_name else None,
         "segment_compute": segment_compute,
         "kernels": kt,
@@ -486,30 +616,19 @@ def run_ours(args, cfg, world, rank, local):
         if cfg.kind == synth.KIND_MOE_SWIGLU_BF16 else None,
     }
     L.ls_ctx_destroy(ctx)
-    del hs
     if rank == 0 and not args.no_cpu_baseline:
-        ntok = min(args.cpu_tokens, T)
-        secs, cores = oracle_time(cfg, ntok)
-        line["cpu_baseline"] = {"value": ntok / secs, "unit": UNIT, "cores": cores, "kind": "oracle",
-                                "sample": f"{ntok} of {T} tokens through all {cfg.n_segments} segments, fp64; "
-                                          "weight drawing and widening not timed"}
+        ntok, nlay = CPU_SAMPLE.get(cfg.name, (1024, None))
+        ntok = min(args.cpu_tokens or ntok, T)
+        run = OracleRun(cfg, ntok, nlay, hs=hs)
+        secs = run.time_pass() * run.scale
+        line["cpu_baseline"] = {"value": ntok / secs, "unit": UNIT, "cores": len(os.sched_getaffinity(0)),
+                                "kind": "oracle", "sample": run.describe()}
+    del hs
     if rank == 0:
         print(json.dumps(line), flush=True)
     if world > 1:
         torch.distributed.destroy_process_group()
     return 0
-
-
-# DRAM bytes (read + write) per launch from ncu captures of the current kernels
-# (profiles/gemm_pair_*.md); absent = not captured.
-TRAFFIC: dict = {
-    ("dit_ffn_12x1024x4096", "gemm_up"): 16_812_800 + 527_360,
-    ("dit_ffn_12x1024x4096", "gemm_down"): 50_413_312 + 2_203_648,
-    # profiles/gemm_pair_shared_proj_24x3072x12288.md
-    ("shared_proj_24x3072x12288", "gemm_proj"): 31_478_528 + 65_792,
-    ("shared_proj_24x3072x12288", "gemm_up"): 88_222_464 + 26_256_384,
-    ("shared_proj_24x3072x12288", "gemm_down"): 196_126_976 + 24_913_920,
-}
 
 
 def main() -> int:
@@ -518,13 +637,14 @@ def main() -> int:
     ap.add_argument("--steps", type=int, default=20)
     ap.add_argument("--warmup", type=int, default=3)
     ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
-    ap.add_argument("--workload", default=synth.DIT.name, choices=sorted(synth.STACKS))
+    ap.add_argument("--workload", default=synth.MOE.name, choices=sorted(synth.STACKS))
     ap.add_argument("--copy-path", default="auto", choices=["auto", "kernel", "engine"])
     ap.add_argument("--copy-ctas", type=int, default=0)
     ap.add_argument("--reserve-sms", type=int, default=-1)
-    ap.add_argument("--cpu-tokens", type=int, default=1024)
-    ap.add_argument("--ref-tokens", type=int, default=256)
+    ap.add_argument("--cpu-tokens", type=int, default=0, help="token rows of the CPU oracle sample (0: per workload)")
+    ap.add_argument("--ref-tokens", type=int, default=0, help="token rows of the reference arm's sample (0: per workload)")
     ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--no-alone", action="store_true", help="skip timing the GEMMs alone after the passes")
     ap.add_argument("--prefetch-depth", type=int, default=None,
                     help="override the workload's prefetch depth (the planner re-derives residents)")
     ap.add_argument("--expert-cache-gb", type=float, default=0.0,
@@ -533,6 +653,10 @@ def main() -> int:
                     help="issue the timed passes as replays of a captured CUDA graph (ls_run_graph)")
     ap.add_argument("--cross-run", action="store_true",
                     help="let the prefetch window cross the pass boundary (off by default, as in the pages)")
+    ap.add_argument("--segments", type=int, default=None,
+                    help="run only the first N segments of the workload (same per-segment shapes; e.g. a "
+                         "profiler capture of the per-segment kernels on a smaller stack)")
+    ap.add_argument("--tokens", type=int, default=None, help="override the workload's token count")
     ap.add_argument("--max-vram-bytes", type=int, default=None,
                     help="override the workload's parameter budget (e.g. a one-slot run)")
     ap.add_argument("--timeline", default=None, metavar="FILE",
@@ -547,6 +671,10 @@ def main() -> int:
         cfg = cfg.with_(prefetch_depth=args.prefetch_depth)
     if args.max_vram_bytes is not None:
         cfg = cfg.with_(max_vram_bytes=args.max_vram_bytes)
+    if args.segments is not None:
+        cfg = cfg.with_(n_segments=max(1, min(args.segments, cfg.n_segments)))
+    if args.tokens is not None:
+        cfg = cfg.with_(tokens=max(1, args.tokens))
     if args.graph and (cfg.kind == synth.KIND_MOE_SWIGLU_BF16 or args.cross_run):
         ap.error("--graph needs a kind without per-pass routing and no --cross-run")
     if args.impl == "reference":

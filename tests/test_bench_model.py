@@ -63,3 +63,45 @@ def test_reference_arm_line():
     assert d["cpu_baseline"]["kind"] == "oracle" and d["cpu_baseline"]["value"] == d["value"]
     assert d["e2e"]["value"] == d["value"] and d["e2e"]["h2d_bytes_per_step"] == 0
     assert d["config"]["workload"] == "tiny_f32_4x256"
+
+
+def test_oracle_sample_is_the_oracle_forward():
+    """The bench's timed CPU sample computes the oracle's stack forward of its rows and
+    leading segments, with the weights taken from the host stack or drawn afresh."""
+    import numpy as np
+    from oracle import stack as S
+    for cfg in (synth.MOE.with_(n_segments=4, tokens=12, hidden=16, ffn=8, n_experts=6, top_k=2),
+                synth.DIT.with_(n_segments=3, tokens=10, hidden=16, ffn=24)):
+        hs = synth.HostStack(cfg)
+        for src in (hs, None):
+            run = bench.OracleRun(cfg, 7, layers=2, hs=src)
+            assert run.scale == cfg.n_segments / 2
+            assert run.time_pass() > 0
+            # the forward it times, replayed outside the timer
+            x = run.x0
+            F = run.F
+            for s in range(2):
+                if s in run.moe:
+                    logits, experts = run._prepare(s)
+                    x = F.moe_swiglu(x, logits, experts.__getitem__, cfg.top_k)
+                else:
+                    x = S.apply_segment(cfg, s, x, rows=run.rows, tensors=run._prepare(s))
+            ref = S.stack_forward(cfg, rows=np.arange(7), n_segments=2)
+            np.testing.assert_allclose(x, ref, rtol=1e-12, atol=1e-12)
+            assert f"time scaled by {cfg.n_segments / 2:g}" in run.describe()
+
+
+def test_traffic_is_dropped_when_the_kernel_source_changes(tmp_path, monkeypatch):
+    import json
+    from host_offloaded_weight_gb300 import profiling as P
+    path = tmp_path / "traffic.json"
+    monkeypatch.setattr(P, "TRAFFIC_FILE", str(path))
+    assert P.traffic("w", "gemm_up") is None                       # no capture
+    entry = {"workload": "w", "kernel": "gemm_up", "dram_bytes_per_launch": 1234, "launches": 2,
+             "source": P.SOURCES["gemm_up"], "source_sha256": P.source_sha("gemm_up"), "report": "r"}
+    path.write_text(json.dumps({"entries": [entry]}))
+    assert P.traffic("w", "gemm_up") == 1234
+    assert P.traffic("w", "gemm_down") is None
+    entry["source_sha256"] = "0" * 64                               # taken on another version
+    path.write_text(json.dumps({"entries": [entry]}))
+    assert P.traffic("w", "gemm_up") is None
