@@ -331,9 +331,11 @@ __device__ __forceinline__ int sw4(int r, int c4) { return r * 8 + (c4 ^ (r & 7)
 // row-wise in registers; everything that touches global memory goes through
 // the warp's staging buffer, so each instruction reads or writes four whole
 // 32-column row segments with 16-byte (fp32) or 8-byte (bf16) accesses per lane.
+// EPI_SCALE_F32: lane l also holds row_dst (the row table's entry for row row0 + l)
+// and row_w (the routing weight of that destination row), loaded once per tile.
 template <int EPI>
 __device__ __forceinline__ void epilogue_chunk(const GemmParams& p, int row0, int row_end, int n, float* v,
-                                               const float* u, float* buf) {
+                                               const float* u, float* buf, int row_dst = 0, float row_w = 0.f) {
     const int lane = threadIdx.x & 31;
     float4* b4 = reinterpret_cast<float4*>(buf);
     const int c4 = lane & 7;              // this lane's float4 column in the transposed phase
@@ -394,11 +396,12 @@ __device__ __forceinline__ void epilogue_chunk(const GemmParams& p, int row0, in
 #pragma unroll
     for (int it = 0; it < 8; ++it) {
         const int row = row0 + it * 4 + (lane >> 3);
+        // every lane takes part in the shuffles, before any of them skips its row
+        const int dst = EPI == EPI_SCALE_F32 ? __shfl_sync(0xffffffffu, row_dst, it * 4 + (lane >> 3)) : 0;
+        const float w = EPI == EPI_SCALE_F32 ? __shfl_sync(0xffffffffu, row_w, it * 4 + (lane >> 3)) : 0.f;
         if (row >= row_end || !col_ok) continue;
         const float4 o = b4[sw4(it * 4 + (lane >> 3), c4)];
         if (EPI == EPI_SCALE_F32) {
-            const int dst = p.row_table[row];
-            const float w = p.row_weight[dst];
             *reinterpret_cast<float4*>(reinterpret_cast<float*>(p.C) + (int64_t)dst * p.ldc + col) =
                 make_float4(w * o.x, w * o.y, w * o.z, w * o.w);
         } else {
@@ -568,15 +571,23 @@ __global__ void __launch_bounds__(NUM_THREADS, 1) gemm_bf16_tc(const __grid_cons
         for (int t = blockIdx.x; t < num_tiles; t += gridDim.x, ++tcount) {
             const int buf = tcount & 1;
             const uint32_t tph = (uint32_t)(tcount >> 1) & 1u;
+            // the row table and routing weights of this warp's 32 rows are inputs: read them
+            // before the accumulator is ready, once per tile (lane l: row row0 + l)
+            const Tile tl = tile_of<GROUPED, DUAL>(p, t, s_mt_prefix);
+            const int row0 = tl.a_row + q * 32;            // first row of this warp's 32
+            const int row_end = tl.row_end < p.M ? tl.row_end : p.M;
+            int row_dst = 0;
+            float row_w = 0.f;
+            if (EPI == EPI_SCALE_F32 && row0 + lane < row_end) {
+                row_dst = p.row_table[row0 + lane];
+                row_w = p.row_weight[row_dst];
+            }
             // warp-uniform outcome: the warp's TMEM loads and its single arrive below need every lane
             if (!__all_sync(0xffffffffu, mbar_wait(tfull_bar(buf), tph, p.err, 4, p.mbar_limit_ns) && !s_abort)) {
                 s_abort = 1;
                 break;
             }
             tc_fence_after();
-            const Tile tl = tile_of<GROUPED, DUAL>(p, t, s_mt_prefix);
-            const int row0 = tl.a_row + q * 32;            // first row of this warp's 32
-            const int row_end = tl.row_end < p.M ? tl.row_end : p.M;
             const uint32_t tbase = tmem_base + ((uint32_t)(q * 32) << 16) + (uint32_t)(buf * ACC_COLS);
             constexpr int CHUNKS = DUAL ? ACC_COLS / 64 : ACC_COLS / 32;
             constexpr int PER_WARP = CHUNKS / (EPI_WARPS / 4);
@@ -594,7 +605,7 @@ __global__ void __launch_bounds__(NUM_THREADS, 1) gemm_bf16_tc(const __grid_cons
                         v[j] = __uint_as_float(r[j]);
                         u[j] = DUAL ? __uint_as_float(r2[j]) : 0.f;
                     }
-                    epilogue_chunk<EPI>(p, row0, row_end, n, v, u, ebuf);
+                    epilogue_chunk<EPI>(p, row0, row_end, n, v, u, ebuf, row_dst, row_w);
                 }
             }
             tc_fence_before();

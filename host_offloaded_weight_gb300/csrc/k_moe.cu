@@ -152,20 +152,17 @@ __global__ void moe_gather_kernel(const uint4* __restrict__ x, const int* __rest
     for (int i = threadIdx.x; i < h16; i += blockDim.x) xs[(int64_t)r * h16 + i] = x[(int64_t)t * h16 + i];
 }
 
+// K = top-k as a template parameter: the K row loads of a thread are all in flight before
+// the first add; the adds run in j order (0 + y0) + y1 + ..., as for any K.
+template <int K>
 __global__ void moe_combine_kernel(const void* __restrict__ x, int x_f32, const float* __restrict__ y,
-                                   int T, int k, int H, __nv_bfloat16* __restrict__ out,
-                                   float* __restrict__ out32) {
+                                   int T, int H, __nv_bfloat16* __restrict__ out, float* __restrict__ out32) {
     const int64_t idx = ((int64_t)blockIdx.x * blockDim.x + threadIdx.x) * 4;
     if (idx >= (int64_t)T * H) return;
     const int t = (int)(idx / H), c = (int)(idx % H);
-    float4 acc = make_float4(0.f, 0.f, 0.f, 0.f);
-    for (int j = 0; j < k; ++j) {
-        const float4 v = *reinterpret_cast<const float4*>(y + ((int64_t)t * k + j) * H + c);
-        acc.x += v.x;
-        acc.y += v.y;
-        acc.z += v.z;
-        acc.w += v.w;
-    }
+    float4 v[K];
+#pragma unroll
+    for (int j = 0; j < K; ++j) v[j] = __ldg(reinterpret_cast<const float4*>(y + ((int64_t)t * K + j) * H + c));
     float4 xr;
     if (x_f32) {
         xr = *reinterpret_cast<const float4*>(reinterpret_cast<const float*>(x) + idx);
@@ -173,6 +170,14 @@ __global__ void moe_combine_kernel(const void* __restrict__ x, int x_f32, const 
         const __nv_bfloat162* xb = reinterpret_cast<const __nv_bfloat162*>(reinterpret_cast<const __nv_bfloat16*>(x) + idx);
         const float2 a = __bfloat1622float2(xb[0]), b = __bfloat1622float2(xb[1]);
         xr = make_float4(a.x, a.y, b.x, b.y);
+    }
+    float4 acc = make_float4(0.f, 0.f, 0.f, 0.f);
+#pragma unroll
+    for (int j = 0; j < K; ++j) {
+        acc.x += v[j].x;
+        acc.y += v[j].y;
+        acc.z += v[j].z;
+        acc.w += v[j].w;
     }
     const float4 o4 = make_float4(xr.x + acc.x, xr.y + acc.y, xr.z + acc.z, xr.w + acc.w);
     __nv_bfloat162* o = reinterpret_cast<__nv_bfloat162*>(out + idx);
@@ -259,8 +264,20 @@ cudaError_t launch_moe_combine(const void* x, bool x_f32, const float* y, int T,
     const int64_t n4 = (int64_t)T * H / 4;
     if (n4 <= 0) return cudaSuccess;
     const int threads = 256;
-    moe_combine_kernel<<<(int)((n4 + threads - 1) / threads), threads, 0, s>>>(
-        x, x_f32 ? 1 : 0, y, T, k, H, reinterpret_cast<__nv_bfloat16*>(out), out32);
+    const int grid = (int)((n4 + threads - 1) / threads);
+    __nv_bfloat16* o = reinterpret_cast<__nv_bfloat16*>(out);
+    const int xf = x_f32 ? 1 : 0;
+    switch (k) {
+        case 1: moe_combine_kernel<1><<<grid, threads, 0, s>>>(x, xf, y, T, H, o, out32); break;
+        case 2: moe_combine_kernel<2><<<grid, threads, 0, s>>>(x, xf, y, T, H, o, out32); break;
+        case 3: moe_combine_kernel<3><<<grid, threads, 0, s>>>(x, xf, y, T, H, o, out32); break;
+        case 4: moe_combine_kernel<4><<<grid, threads, 0, s>>>(x, xf, y, T, H, o, out32); break;
+        case 5: moe_combine_kernel<5><<<grid, threads, 0, s>>>(x, xf, y, T, H, o, out32); break;
+        case 6: moe_combine_kernel<6><<<grid, threads, 0, s>>>(x, xf, y, T, H, o, out32); break;
+        case 7: moe_combine_kernel<7><<<grid, threads, 0, s>>>(x, xf, y, T, H, o, out32); break;
+        case 8: moe_combine_kernel<8><<<grid, threads, 0, s>>>(x, xf, y, T, H, o, out32); break;
+        default: return cudaErrorInvalidValue;
+    }
     return cudaGetLastError();
 }
 

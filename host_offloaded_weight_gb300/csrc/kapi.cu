@@ -246,7 +246,7 @@ ls_status lsk_moe_gather(const void* x, const int32_t* row_table, int32_t rows, 
 
 ls_status lsk_moe_combine(const void* x, int32_t x_f32, const float* y, int32_t T, int32_t k, int32_t H, void* out,
                           float* out32, void* stream) {
-    if (!x || !y || !out || T < 0 || k < 1) return LS_ERR_INVALID_ARG;
+    if (!x || !y || !out || T < 0 || k < 1 || k > 8) return LS_ERR_INVALID_ARG;
     return st(launch_moe_combine(x, x_f32 != 0, y, T, k, H, out, out32, (cudaStream_t)stream));
 }
 

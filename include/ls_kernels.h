@@ -160,7 +160,7 @@ ls_status lsk_moe_rows_copy(const float* src, const int32_t* src_table, float* d
 ls_status lsk_moe_gather(const void* x_dev, const int32_t* row_table_dev, int32_t rows, int32_t k, int32_t H,
                          void* x_sorted_dev, void* stream);
 
-/* out[t] = x[t] + sum_{j<k} y[t*k + j] (fp32 sum in j order, one bf16 rounding).
+/* out[t] = x[t] + sum_{j<k} y[t*k + j] (fp32 sum in j order, one bf16 rounding), 1 <= k <= 8.
  * x is bf16, or fp32 when x_f32 != 0; out32_dev (may be NULL) gets the fp32 sum. */
 ls_status lsk_moe_combine(const void* x_dev, int32_t x_f32, const float* y_dev, int32_t T, int32_t k, int32_t H,
                           void* out_dev, float* out32_dev, void* stream);
