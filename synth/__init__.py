@@ -281,7 +281,10 @@ class HostStack:
     (segment, tensor_index, shared_id), the shapes the C ABI registers.
     bf16 tensors are uint16 views holding the bit patterns."""
 
-    def __init__(self, cfg: StackConfig, n_segments: int | None = None, threads: int = 0):
+    def __init__(self, cfg: StackConfig, n_segments: int | None = None, threads: int = 0, alloc=None):
+        """``alloc(nbytes) -> (address, release)``, optional: where the buffer lives (for example
+        pinned memory from a driver allocator); ``release()`` is called by ``close()``. Default:
+        anonymous pages of the process."""
         self.cfg = cfg
         n = cfg.n_segments if n_segments is None else n_segments
         specs = segment_tensors(cfg)
@@ -289,16 +292,23 @@ class HostStack:
         seg_bytes = segment_slot_bytes(cfg)
         sh_bytes = sum(align256(t.nbytes) for t in sh)
         total = n * seg_bytes + sh_bytes
-        # anonymous pages of its own: nothing else lives in the buffer's pages. Large
-        # pages where the kernel offers them on request: fewer translations for the
-        # device's reads of pinned host memory (a hint; ignored where unsupported)
-        self._map = mmap.mmap(-1, max(total, 1))
-        if hasattr(mmap, "MADV_HUGEPAGE") and total >= (64 << 20):
-            try:
-                self._map.madvise(mmap.MADV_HUGEPAGE)
-            except OSError:
-                pass
-        self.buffer = np.frombuffer(self._map, dtype=np.uint8, count=total)
+        self._release = None
+        self._map = None
+        if alloc is not None:
+            import ctypes
+            addr, self._release = alloc(max(total, 1))
+            self.buffer = np.ctypeslib.as_array((ctypes.c_uint8 * max(total, 1)).from_address(addr))[:total]
+        else:
+            # anonymous pages of its own: nothing else lives in the buffer's pages. Large
+            # pages where the kernel offers them on request: fewer translations for the
+            # device's reads of pinned host memory (a hint; ignored where unsupported)
+            self._map = mmap.mmap(-1, max(total, 1))
+            if hasattr(mmap, "MADV_HUGEPAGE") and total >= (64 << 20):
+                try:
+                    self._map.madvise(mmap.MADV_HUGEPAGE)
+                except OSError:
+                    pass
+            self.buffer = np.frombuffer(self._map, dtype=np.uint8, count=total)
         self.shared_views = []
         o = n * seg_bytes
         for t in sh:
@@ -328,6 +338,20 @@ class HostStack:
                 for i in range(len(sh)):
                     self.shared_map.append((s, i, i))
             self.segments.append((cfg.kind, tensors))
+
+    def close(self) -> None:
+        """Give the buffer back now (views into it must no longer be used)."""
+        self.seg_views, self.shared_views, self.segments = [], [], []
+        self.buffer = None
+        if self._release is not None:
+            self._release()
+            self._release = None
+        if self._map is not None:
+            try:
+                self._map.close()
+            except BufferError:   # a view is still alive; the mapping goes with the last one
+                pass
+            self._map = None
 
     def _view(self, off: int, t: TensorSpec) -> np.ndarray:
         dt = np.float32 if t.dtype == "f32" else np.uint16
