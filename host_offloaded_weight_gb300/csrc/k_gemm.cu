@@ -85,6 +85,7 @@ struct GemmParams {
     uint32_t* err;
     uint64_t mbar_limit_ns;  // bound of every internal mbarrier wait
     int pdl;                 // host side: launch with programmatic stream serialization
+    int splits;              // EPI_PARTIAL: K slices; slice s of tile t is work item s * num_tiles + t
 };
 
 // ------------------------------------------------------------------ PTX helpers
@@ -335,7 +336,8 @@ __device__ __forceinline__ int sw4(int r, int c4) { return r * 8 + (c4 ^ (r & 7)
 // and row_w (the routing weight of that destination row), loaded once per tile.
 template <int EPI>
 __device__ __forceinline__ void epilogue_chunk(const GemmParams& p, int row0, int row_end, int n, float* v,
-                                               const float* u, float* buf, int row_dst = 0, float row_w = 0.f) {
+                                               const float* u, float* buf, int row_dst = 0, float row_w = 0.f,
+                                               int64_t c_off = 0) {
     const int lane = threadIdx.x & 31;
     float4* b4 = reinterpret_cast<float4*>(buf);
     const int c4 = lane & 7;              // this lane's float4 column in the transposed phase
@@ -404,6 +406,8 @@ __device__ __forceinline__ void epilogue_chunk(const GemmParams& p, int row0, in
         if (EPI == EPI_SCALE_F32) {
             *reinterpret_cast<float4*>(reinterpret_cast<float*>(p.C) + (int64_t)dst * p.ldc + col) =
                 make_float4(w * o.x, w * o.y, w * o.z, w * o.w);
+        } else if (EPI == EPI_PARTIAL) {
+            *reinterpret_cast<float4*>(reinterpret_cast<float*>(p.C) + c_off + (int64_t)row * p.ldc + col) = o;
         } else {
             if ((EPI == EPI_BIAS_RESID || EPI == EPI_RESID) && p.C32)
                 *reinterpret_cast<float4*>(p.C32 + (int64_t)row * p.ldc + col) = o;
@@ -474,6 +478,12 @@ __global__ void __launch_bounds__(NUM_THREADS, 1) gemm_bf16_tc(const __grid_cons
     int num_tiles = p.num_tiles;
     if (GROUPED) num_tiles = s_mt_prefix[p.n_groups] * p.num_n_tiles;
     const int kb_n = p.num_k_blocks;
+    // split K (EPI_PARTIAL): work item t is K slice t / num_tiles of tile t % num_tiles
+    const int n_items = EPI == EPI_PARTIAL ? num_tiles * p.splits : num_tiles;
+    auto kb_lo = [&](int t) { return EPI == EPI_PARTIAL ? (int)((int64_t)(t / num_tiles) * kb_n / p.splits) : 0; };
+    auto kb_hi = [&](int t) {
+        return EPI == EPI_PARTIAL ? (int)((int64_t)(t / num_tiles + 1) * kb_n / p.splits) : kb_n;
+    };
 
     if (warp == 0) {
         // ------------------------------------------------------------ TMA producer
@@ -484,9 +494,9 @@ __global__ void __launch_bounds__(NUM_THREADS, 1) gemm_bf16_tc(const __grid_cons
             bool ok = true;
             int it = 0;
             uint32_t issued_mask = 0;
-            for (int t = blockIdx.x; t < num_tiles && ok; t += gridDim.x) {
-                const Tile tl = tile_of<GROUPED, DUAL>(p, t, s_mt_prefix);
-                for (int kb = 0; kb < kb_n; ++kb, ++it) {
+            for (int t = blockIdx.x; t < n_items && ok; t += gridDim.x) {
+                const Tile tl = tile_of<GROUPED, DUAL>(p, t % num_tiles, s_mt_prefix);
+                for (int kb = kb_lo(t); kb < kb_hi(t); ++kb, ++it) {
                     const int s = it % STAGES;
                     const uint32_t ph = (uint32_t)(it / STAGES) & 1u;
                     if (!mbar_wait(empty_bar(s), ph ^ 1u, p.err, 1, p.mbar_limit_ns)) {
@@ -523,7 +533,7 @@ __global__ void __launch_bounds__(NUM_THREADS, 1) gemm_bf16_tc(const __grid_cons
             constexpr uint32_t IDESC = DUAL ? make_idesc(BM, ACC_COLS / 2) : make_idesc(BM, ACC_COLS);
             int it = 0, tcount = 0;
             bool ok = true;
-            for (int t = blockIdx.x; t < num_tiles && ok; t += gridDim.x, ++tcount) {
+            for (int t = blockIdx.x; t < n_items && ok; t += gridDim.x, ++tcount) {
                 const int buf = tcount & 1;
                 const uint32_t tph = (uint32_t)(tcount >> 1) & 1u;
                 if (!mbar_wait(tempty_bar(buf), tph ^ 1u, p.err, 2, p.mbar_limit_ns) || s_abort) {
@@ -532,7 +542,8 @@ __global__ void __launch_bounds__(NUM_THREADS, 1) gemm_bf16_tc(const __grid_cons
                 }
                 tc_fence_after();
                 const uint32_t d = tmem_base + (uint32_t)(buf * ACC_COLS);
-                for (int kb = 0; kb < kb_n; ++kb, ++it) {
+                const int kb0 = kb_lo(t);
+                for (int kb = kb0; kb < kb_hi(t); ++kb, ++it) {
                     const int s = it % STAGES;
                     const uint32_t ph = (uint32_t)(it / STAGES) & 1u;
                     if (!mbar_wait(full_bar(s), ph, p.err, 3, p.mbar_limit_ns)) {
@@ -546,7 +557,7 @@ __global__ void __launch_bounds__(NUM_THREADS, 1) gemm_bf16_tc(const __grid_cons
 #pragma unroll
                     for (int kk = 0; kk < BK / 16; ++kk) {
                         const uint64_t ad = make_sdesc(sa + kk * 32);
-                        const uint32_t acc = (kb > 0 || kk > 0) ? 1u : 0u;
+                        const uint32_t acc = (kb > kb0 || kk > 0) ? 1u : 0u;
                         if (DUAL) {
                             umma_bf16(d, ad, make_sdesc(sb + kk * 32), IDESC, acc);
                             umma_bf16(d + ACC_COLS / 2, ad, make_sdesc(sb + B_BYTES / 2 + kk * 32), IDESC, acc);
@@ -568,12 +579,14 @@ __global__ void __launch_bounds__(NUM_THREADS, 1) gemm_bf16_tc(const __grid_cons
         const int half = (warp - 2) >> 2;       // which half of the tile's columns
         float* ebuf = reinterpret_cast<float*>(gbase + STAGES * STAGE_BYTES + (warp - 2) * EPI_BUF_BYTES);
         int tcount = 0;
-        for (int t = blockIdx.x; t < num_tiles; t += gridDim.x, ++tcount) {
+        for (int t = blockIdx.x; t < n_items; t += gridDim.x, ++tcount) {
             const int buf = tcount & 1;
             const uint32_t tph = (uint32_t)(tcount >> 1) & 1u;
             // the row table and routing weights of this warp's 32 rows are inputs: read them
             // before the accumulator is ready, once per tile (lane l: row row0 + l)
-            const Tile tl = tile_of<GROUPED, DUAL>(p, t, s_mt_prefix);
+            const Tile tl = tile_of<GROUPED, DUAL>(p, t % num_tiles, s_mt_prefix);
+            // split K: slice t / num_tiles writes its partial tile into its own M x N plane
+            const int64_t c_off = EPI == EPI_PARTIAL ? (int64_t)(t / num_tiles) * p.M * p.ldc : 0;
             const int row0 = tl.a_row + q * 32;            // first row of this warp's 32
             const int row_end = tl.row_end < p.M ? tl.row_end : p.M;
             int row_dst = 0;
@@ -605,7 +618,7 @@ __global__ void __launch_bounds__(NUM_THREADS, 1) gemm_bf16_tc(const __grid_cons
                         v[j] = __uint_as_float(r[j]);
                         u[j] = DUAL ? __uint_as_float(r2[j]) : 0.f;
                     }
-                    epilogue_chunk<EPI>(p, row0, row_end, n, v, u, ebuf, row_dst, row_w);
+                    epilogue_chunk<EPI>(p, row0, row_end, n, v, u, ebuf, row_dst, row_w, c_off);
                 }
             }
             tc_fence_before();
@@ -1093,6 +1106,57 @@ __global__ void __launch_bounds__(s2_threads(EPI), 1) gemm_bf16_tc2(const __grid
         tmem_dealloc2(tmem_base, 512);
     }
 }
+// ------------------------------------------------------------------ split-K reduction
+// C = epilogue(sum over s of part[s]) for a GEMM whose K was cut into `splits` slices: the
+// partial tiles are added in slice order (fixed, so the bits do not depend on timing), then
+// the same elementwise epilogue as the unsplit kernels (bias, GELU, residual) runs on the
+// sum. One thread per 4 consecutive columns.
+template <int EPI>
+__global__ void splitk_reduce_kernel(const float* __restrict__ part, int splits, int M, int N,
+                                     const __nv_bfloat16* __restrict__ bias, const void* __restrict__ resid,
+                                     int resid_f32, int64_t ldr, __nv_bfloat16* __restrict__ C, int64_t ldc,
+                                     float* __restrict__ C32) {
+    const int64_t i4 = (int64_t)blockIdx.x * blockDim.x + threadIdx.x;
+    const int n4 = N / 4;
+    if (i4 >= (int64_t)M * n4) return;
+    const int row = (int)(i4 / n4), col = (int)(i4 % n4) * 4;
+    const int64_t plane = (int64_t)M * N;
+    float v[4] = {0.f, 0.f, 0.f, 0.f};
+    const float* src = part + (int64_t)row * N + col;
+    for (int s0 = 0; s0 < splits; s0 += 8) {  // eight slices' loads in flight, then added in order
+        float4 t[8];
+#pragma unroll
+        for (int j = 0; j < 8; ++j)
+            t[j] = s0 + j < splits ? __ldcg(reinterpret_cast<const float4*>(src + (s0 + j) * plane))
+                                   : make_float4(0.f, 0.f, 0.f, 0.f);
+#pragma unroll
+        for (int j = 0; j < 8; ++j)
+            if (s0 + j < splits) { v[0] += t[j].x; v[1] += t[j].y; v[2] += t[j].z; v[3] += t[j].w; }
+    }
+    if (EPI == EPI_BIAS_GELU || EPI == EPI_BIAS_RESID) {
+        const uint2 h = *reinterpret_cast<const uint2*>(reinterpret_cast<const uint16_t*>(bias) + col);
+        v[0] += bf2f((uint16_t)(h.x & 0xffff)); v[1] += bf2f((uint16_t)(h.x >> 16));
+        v[2] += bf2f((uint16_t)(h.y & 0xffff)); v[3] += bf2f((uint16_t)(h.y >> 16));
+    }
+    if (EPI == EPI_BIAS_GELU) gelu_inplace<4>(v);
+    if (EPI == EPI_BIAS_RESID || EPI == EPI_RESID) {
+        if (resid_f32) {
+            const float4 r = *reinterpret_cast<const float4*>(reinterpret_cast<const float*>(resid) + (int64_t)row * ldr + col);
+            v[0] += r.x; v[1] += r.y; v[2] += r.z; v[3] += r.w;
+        } else {
+            const uint2 h = *reinterpret_cast<const uint2*>(reinterpret_cast<const uint16_t*>(resid) + (int64_t)row * ldr + col);
+            v[0] += bf2f((uint16_t)(h.x & 0xffff)); v[1] += bf2f((uint16_t)(h.x >> 16));
+            v[2] += bf2f((uint16_t)(h.y & 0xffff)); v[3] += bf2f((uint16_t)(h.y >> 16));
+        }
+        if (C32) *reinterpret_cast<float4*>(C32 + (int64_t)row * ldc + col) = make_float4(v[0], v[1], v[2], v[3]);
+    }
+    __nv_bfloat162 lo = __floats2bfloat162_rn(v[0], v[1]), hi = __floats2bfloat162_rn(v[2], v[3]);
+    uint2 pk;
+    pk.x = *reinterpret_cast<uint32_t*>(&lo);
+    pk.y = *reinterpret_cast<uint32_t*>(&hi);
+    *reinterpret_cast<uint2*>(C + (int64_t)row * ldc + col) = pk;
+}
+
 // ------------------------------------------------------------------ host side
 typedef CUresult (*EncodeTiledFn)(CUtensorMap*, CUtensorMapDataType, cuuint32_t, void*, const cuuint64_t*,
                                   const cuuint64_t*, const cuuint32_t*, const cuuint32_t*,
@@ -1229,7 +1293,38 @@ cudaError_t launch_t2_bn(const GemmParams& p, int bn, int clusters, cudaStream_t
     return cudaErrorInvalidValue;
 }
 
+template <int EPI>
+cudaError_t launch_splitk_reduce(const float* part, int splits, const GemmDesc& d, cudaStream_t s) {
+    const int64_t n4 = (int64_t)d.M * (d.N / 4);
+    const int threads = 256;
+    splitk_reduce_kernel<EPI><<<(int)((n4 + threads - 1) / threads), threads, 0, s>>>(
+        part, splits, d.M, d.N, reinterpret_cast<const __nv_bfloat16*>(d.bias), d.resid, d.resid_f32 ? 1 : 0, d.ldr,
+        reinterpret_cast<__nv_bfloat16*>(d.C), d.ldc, reinterpret_cast<float*>(d.C32));
+    return cudaGetLastError();
+}
+
 }  // namespace
+
+int gemm_split_k(int64_t M, int64_t N, int64_t K, int epi) {
+    if (M <= 0 || M > BM || N <= 0 || K <= 0) return 1;
+    if (epi != EPI_STORE && epi != EPI_BIAS_GELU && epi != EPI_BIAS_RESID && epi != EPI_RESID) return 1;
+    const int64_t tiles = (N + ACC_COLS - 1) / ACC_COLS;
+    const int64_t kb = (K + BK - 1) / BK;
+    // enough K slices to give every SM a work item, each at least two k-blocks long, but no
+    // more than the slices whose fp32 partial tiles (M x N x 4 bytes each) together weigh
+    // about what the weights do (N x K x 2 bytes): beyond that the partials' traffic costs
+    // more than the parallelism gains
+    const int64_t sp = std::min<int64_t>(std::min<int64_t>(gemm_num_sms() / tiles, kb / 2),
+                                         std::max<int64_t>(2, K / (2 * M)));
+    return sp >= 2 ? (int)sp : 1;
+}
+
+int64_t gemm_split_ws_bytes(int64_t M, int64_t N, int64_t K, int epi) {
+    const int sp = gemm_split_k(M, N, K, epi);
+    return sp > 1 ? (int64_t)sp * M * N * (int64_t)sizeof(float) : 0;
+}
+
+int64_t gemm_split_ws_max() { return (int64_t)gemm_num_sms() * BM * ACC_COLS * (int64_t)sizeof(float); }
 
 // Tile width of a dense pair GEMM. A k-block of a 256 x BN tile costs about the time
 // of BN + 1024 columns: measured on GB300, narrowing the tile from 256 to 160
@@ -1317,6 +1412,7 @@ cudaError_t launch_gemm_bf16(const GemmDesc& d, int max_ctas, cudaStream_t s) {
     p.err = d.err_word;
     p.mbar_limit_ns = MBAR_LIMIT_NS;
     p.pdl = d.pdl ? 1 : 0;
+    p.splits = 1;
     int tiles = p.num_tiles;
     if (grouped) {
         // sum over groups of ceil(rows/BM) <= M/BM + n_groups
@@ -1347,6 +1443,28 @@ cudaError_t launch_gemm_bf16(const GemmDesc& d, int max_ctas, cudaStream_t s) {
             case EPI_BIAS_RESID: return launch_t2_bn<EPI_BIAS_RESID>(p, bn2, clusters, s);
             case EPI_RESID: return launch_t2_bn<EPI_RESID>(p, bn2, clusters, s);
             case EPI_SWIGLU: return launch_t2<EPI_SWIGLU, true, 256>(p, clusters, s);
+        }
+        return cudaErrorInvalidValue;
+    }
+    // a small dense GEMM with few tiles: its K slices go to separate CTAs, and a reduction adds
+    // their partial tiles in slice order and runs the epilogue
+    const int splits = grouped || dual ? 1 : gemm_split_k(d.M, d.N, d.K, d.epi);
+    if (splits > 1 && d.splitk_ws && d.splitk_ws_bytes >= gemm_split_ws_bytes(d.M, d.N, d.K, d.epi) &&
+        !(reinterpret_cast<uintptr_t>(d.splitk_ws) & 15)) {
+        GemmParams q = p;
+        q.splits = splits;
+        q.C = d.splitk_ws;
+        q.ldc = d.N;
+        q.C32 = nullptr;
+        int g2 = grid < tiles * splits ? grid : tiles * splits;
+        if (g2 < 1) g2 = 1;
+        cudaError_t e = launch_t<EPI_PARTIAL, false, false>(q, g2, s);
+        if (e != cudaSuccess) return e;
+        switch (d.epi) {
+            case EPI_STORE: return launch_splitk_reduce<EPI_STORE>(d.splitk_ws, splits, d, s);
+            case EPI_BIAS_GELU: return launch_splitk_reduce<EPI_BIAS_GELU>(d.splitk_ws, splits, d, s);
+            case EPI_BIAS_RESID: return launch_splitk_reduce<EPI_BIAS_RESID>(d.splitk_ws, splits, d, s);
+            case EPI_RESID: return launch_splitk_reduce<EPI_RESID>(d.splitk_ws, splits, d, s);
         }
         return cudaErrorInvalidValue;
     }

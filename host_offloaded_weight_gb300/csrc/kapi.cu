@@ -93,6 +93,35 @@ ls_status lsk_wait_ready(const uint32_t* ready_dev, uint32_t epoch, int32_t limi
                                 DERR_HANDOFF_TIMEOUT | ((uint32_t)slot << 8), (cudaStream_t)stream));
 }
 
+// A memory pool per device for the entry points' short-lived scratch (the split-K partial
+// tiles): freed blocks stay in the pool (no release threshold), so calls in a loop do not map
+// and unmap device memory each time. Other allocators' pools are left alone.
+static cudaMemPool_t scratch_pool() {
+    static std::mutex mu;
+    static cudaMemPool_t pools[64] = {};
+    int dev = 0;
+    if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= 64) {
+        cudaGetLastError();
+        return nullptr;
+    }
+    std::lock_guard<std::mutex> g(mu);
+    if (!pools[dev]) {
+        cudaMemPoolProps props = {};
+        props.allocType = cudaMemAllocationTypePinned;
+        props.location.type = cudaMemLocationTypeDevice;
+        props.location.id = dev;
+        if (cudaMemPoolCreate(&pools[dev], &props) != cudaSuccess) {
+            cudaGetLastError();
+            pools[dev] = nullptr;
+            return nullptr;
+        }
+        uint64_t keep = UINT64_MAX;
+        cudaMemPoolSetAttribute(pools[dev], cudaMemPoolAttrReleaseThreshold, &keep);
+        cudaGetLastError();
+    }
+    return pools[dev];
+}
+
 ls_status lsk_gemm_bf16(int32_t epilogue, const void* A, const void* B, int64_t b_rows, int32_t b2_row_off,
                         const void* bias, const void* resid, int32_t resid_f32, void* C, void* C32, int32_t M,
                         int32_t N, int32_t K, int32_t max_ctas, void* stream) {
@@ -113,7 +142,21 @@ ls_status lsk_gemm_bf16(int32_t epilogue, const void* A, const void* B, int64_t 
     d.C32 = C32;
     d.M = M; d.N = N; d.K = K;
     d.err_word = err_dev();
-    return st(launch_gemm_bf16(d, max_ctas, (cudaStream_t)stream));
+    // a small GEMM split along K needs a workspace for its partial tiles: stream-ordered, from
+    // a memory pool of this library's own that keeps freed memory for the next call
+    cudaStream_t s = (cudaStream_t)stream;
+    const int64_t ws = gemm_split_ws_bytes(M, N, K, epilogue);
+    if (ws > 0) {
+        cudaMemPool_t pool = scratch_pool();
+        if (!pool || cudaMallocFromPoolAsync((void**)&d.splitk_ws, (size_t)ws, pool, s) != cudaSuccess) {
+            cudaGetLastError();
+            return LS_ERR_OOM;
+        }
+        d.splitk_ws_bytes = ws;
+    }
+    const cudaError_t e = launch_gemm_bf16(d, max_ctas, s);
+    if (d.splitk_ws) cudaFreeAsync(d.splitk_ws, s);
+    return st(e);
 }
 
 int32_t lsk_gemm_tile_n(int32_t epilogue, int32_t M, int32_t N) {

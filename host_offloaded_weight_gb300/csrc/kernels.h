@@ -40,6 +40,7 @@ enum GemmEpilogue : int {
     EPI_SWIGLU = 3,     // dual B: C = SiLU(acc_g) * acc_u  -> bf16
     EPI_RESID = 4,      // C = acc + R                      -> bf16
     EPI_SCALE_F32 = 5,  // grouped: Y[row_table[i]] = w[row_table[i]] * acc -> fp32
+    EPI_PARTIAL = 6,    // internal (split K): the fp32 accumulator of one K slice, as is
 };
 
 struct GemmDesc {
@@ -74,6 +75,10 @@ struct GemmDesc {
     const int* group_b_row = nullptr;
     const void* B2 = nullptr;
     int64_t b2_rows = 0;
+    // dense GEMMs with M <= 128 and few tiles (see gemm_split_k): fp32 workspace for the K
+    // slices' partial tiles; without one (or too small) the GEMM runs unsplit
+    float* splitk_ws = nullptr;
+    int64_t splitk_ws_bytes = 0;
     uint32_t* err_word = nullptr;       // mapped host word for internal timeouts
     // programmatic dependent launch: the prologue overlaps the previous kernel's tail.
     // Off where events bracket each launch, so that an event pair times this kernel alone.
@@ -85,6 +90,12 @@ cudaError_t launch_gemm_bf16(const GemmDesc& d, int max_ctas, cudaStream_t s);
 int gemm_num_sms();
 // Tile width (output columns) of the dense pair-CTA GEMM for an M x N output.
 int gemm_pair_tile_n(int64_t M, int64_t N);
+// K slices of a dense single-CTA GEMM (M <= 128, not the gate/up pair): 1 when it is not split.
+// A function of the shape and the device only, so the bits do not depend on the grid.
+int gemm_split_k(int64_t M, int64_t N, int64_t K, int epi);
+// Workspace bytes the split needs (0 when not split); at most GEMM_SPLITK_WS_MAX.
+int64_t gemm_split_ws_bytes(int64_t M, int64_t N, int64_t K, int epi);
+int64_t gemm_split_ws_max();
 
 // ---------------------------------------------------------------- MoE
 cudaError_t launch_moe_route(const float* logits, int n_layers, int T, int E, int k, int* sel,

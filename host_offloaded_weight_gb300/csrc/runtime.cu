@@ -116,6 +116,7 @@ struct ls_ctx {
     float* xf = nullptr;                // bf16 kinds: fp32 residual stream (updated in place)
     void* hbuf = nullptr;
     void* ubuf = nullptr;
+    float* splitk_ws = nullptr;         // partial tiles of split-K GEMMs at <= 128 tokens (kept for life)
     // MoE workspaces
     int top_k = 0;
     int* moe_sel = nullptr;
@@ -423,6 +424,8 @@ void compute_segment(ls_ctx* c, const RunCtx& rc, int seg, bool wait) {
     GemmDesc w0;
     w0.err_word = c->err_word_dev;
     w0.pdl = pdl;
+    w0.splitk_ws = c->splitk_ws;
+    w0.splitk_ws_bytes = c->splitk_ws ? gemm_split_ws_max() : 0;
     const int ctas = gemm_ctas(c);
     if (!wait) open_span();
     switch (c->kind) {
@@ -961,6 +964,11 @@ ls_status ensure_workspace(ls_ctx* c, int64_t T) {
         CK(cudaMallocAsync(&c->moe_hs, (size_t)rows * c->F * 2, a));
         CK(cudaMallocAsync((void**)&c->moe_y, (size_t)rows * c->H * sizeof(float), a));
     }
+    // dense bf16 kinds: the split-K workspace of small token counts, allocated once, so that a
+    // given token count always takes the same path (and gives the same bits)
+    if (!c->splitk_ws && (c->kind == LS_KIND_FFN_GELU_BF16 || c->kind == LS_KIND_FFN_GELU_SHARED_BF16 ||
+                          c->kind == LS_KIND_SWIGLU_BF16))
+        CK(cudaMallocAsync((void**)&c->splitk_ws, (size_t)gemm_split_ws_max(), a));
     CK(cudaStreamSynchronize(a));   // the new workspaces are usable on any stream
     c->ws_tokens = T;
     return LS_OK;
@@ -1731,6 +1739,7 @@ static void release_resources(ls_ctx* c) {
         cudaSetDevice(c->device);
         sync_ctx_streams(c);
         free_workspaces(c);
+        if (c->splitk_ws) cudaFreeAsync(c->splitk_ws, c->copy_stream);
         for (int s = 0; s < (int)c->seg_buf.size(); ++s)
             if (c->seg_buf[s])
                 dev_free(c, c->seg_buf[s], (size_t)(c->segs[s].slot_bytes + (c->prm.debug_checks ? CANARY_BYTES : 0)),

@@ -91,7 +91,13 @@ ls_status lsk_wait_ready(const uint32_t* ready_dev, uint32_t epoch, int32_t limi
  * >= N, or >= b2_row_off + N for SWIGLU), bias [N], R [M,N], C [M,N]; bf16
  * row-major, dense, except R, which is fp32 when resid_f32 != 0. The residual
  * epilogues also write the fp32 result to C32_dev [M,N] when it is not NULL.
- * K and N multiples of 8, pointers 16-byte aligned. max_ctas <= 0: one CTA per SM. */
+ * K and N multiples of 8, pointers 16-byte aligned. max_ctas <= 0: one CTA per SM.
+ * A small GEMM (M <= 128, not SWIGLU) whose 256-column tiles leave SMs idle is split along
+ * K: the slices' fp32 partial tiles go to a workspace this call takes on `stream` from a
+ * memory pool of the library's own, which keeps freed blocks for later calls (stream-ordered,
+ * at most one 128 x 256 fp32 tile per SM; LS_ERR_OOM if refused), and a reduction adds them
+ * in slice order before the epilogue. The slice count depends only on
+ * the shape and the device, so the bits do not depend on max_ctas. */
 ls_status lsk_gemm_bf16(int32_t epilogue, const void* A_dev, const void* B_dev, int64_t b_rows,
                         int32_t b2_row_off, const void* bias_dev, const void* resid_dev, int32_t resid_f32,
                         void* C_dev, void* C32_dev, int32_t M, int32_t N, int32_t K, int32_t max_ctas,

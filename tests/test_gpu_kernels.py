@@ -133,6 +133,41 @@ def test_gemm_bit_identical_across_grid_sizes(ctas):
     assert torch.equal(out.view(torch.int16), ref.view(torch.int16))
 
 
+# Small GEMMs (M <= 128) with few 256-column tiles are split along K: each slice's partial tile
+# is written in fp32 and a reduction adds them in slice order, then runs the epilogue. On a
+# 152-SM device these take 16, 5, 16 and 2 slices.
+SPLIT_SHAPES = [(128, 1024, 4096), (100, 4096, 1024), (1, 520, 2000), (77, 264, 304)]
+
+
+@pytest.mark.parametrize("M,N,K", SPLIT_SHAPES)
+@pytest.mark.parametrize("epi", [L.LSK_EPI_STORE, L.LSK_EPI_BIAS_GELU, L.LSK_EPI_BIAS_RESID, L.LSK_EPI_RESID])
+def test_split_k_gemm_vs_oracle(M, N, K, epi):
+    ab, a = rand_bf16((M, K), 41, 1.0)
+    bb, b = rand_bf16((N, K), 42, 1.0 / np.sqrt(K))
+    biasb, bias = rand_bf16((N,), 43, 0.5)
+    r = np.random.default_rng(44).standard_normal((M, N)).astype(np.float32)
+    C = torch.empty((M, N), dtype=torch.bfloat16, device="cuda")
+    C32 = torch.empty((M, N), dtype=torch.float32, device="cuda")
+    resid = epi in (L.LSK_EPI_BIAS_RESID, L.LSK_EPI_RESID)
+    A, B, Bias, R = bf16_dev(ab), bf16_dev(bb), bf16_dev(biasb), torch.from_numpy(r).cuda()
+    L.lsk_gemm_bf16(epi, A, B, C, M, N, K, bias=Bias, resid=R, C32=C32 if resid else None)
+    torch.cuda.synchronize()
+    _no_device_error()
+    ref = _gemm_ref(epi, a, b, bias, r.astype(np.float64), 0, N)
+    got = to_f64(C)
+    tol = 2.0 ** -8 * np.abs(ref) + 1e-5 * np.sqrt(K) * np.abs(ref).max()
+    assert np.all(np.abs(got - ref) <= tol), (epi, np.max(np.abs(got - ref) - tol))
+    if resid:
+        assert torch.equal(C.cpu(), C32.cpu().to(torch.bfloat16))
+    # the slice count depends on the shape only: the grid a call gets does not change a bit
+    for ctas in (7, 37):
+        out = torch.empty_like(C)
+        L.lsk_gemm_bf16(epi, A, B, out, M, N, K, bias=Bias, resid=R, C32=C32 if resid else None,
+                        max_ctas=ctas)
+        torch.cuda.synchronize()
+        assert torch.equal(out.view(torch.int16), C.view(torch.int16)), ctas
+
+
 # Tile widths of the pair GEMM: on a 152-SM device these shapes (ragged M and N) take
 # 256 x 160, 192, 224 and 256 tiles.
 TILE_N_SHAPES = {160: (300, 520, 200), 192: (520, 4008, 200), 224: (520, 4808, 200), 256: (520, 5608, 200)}
