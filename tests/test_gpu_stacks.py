@@ -209,14 +209,36 @@ def test_moe_stack_full_size_with_and_without_expert_cache():
     cfg = synth.MOE
     hs = synth.HostStack(cfg)
     lg_dev, _ = logits_dev(cfg)
-    y0, ev0, stats0, st0, _ = _run(cfg, hs, logits=lg_dev, runs=1)
+    # the uncached pass runs with the debug checks on (canaries after both 1.2 GB slots, the
+    # routing tables of all 48 layers validated): they find nothing and change no bit
+    y0, ev0, stats0, st0, _ = _run(cfg, hs, logits=lg_dev, runs=1, debug_checks=1)
     assert st0 == L.LS_OK and stats0["pool_slots"] == 2 and stats0["depth"] == 1
+    assert stats0["debug_violations"] == 0
     rows = _rows(cfg, 8)
     ref = _oracle_from_host(cfg, hs, rows)
     assert rel_err(to_f64(y0)[rows], ref) <= BOUND
     y, ev, stats, st, sts = _run(cfg, hs, logits=lg_dev, runs=3, expert_cache_bytes=40 << 30)
     assert stats["expert_cache_hits"] > 4000
     assert np.array_equal(_bits(y), _bits(y0))
+
+
+def test_driver_pinned_host_memory_gives_the_same_bits():
+    """The stack's tensors in memory from ls_host_alloc (already pinned and mapped, so the
+    library registers nothing) stream and compute exactly as from registered pages."""
+    cfg = SMALL["ffn"]
+    hs = synth.HostStack(cfg)
+    y0, ev0, *_ = _run(cfg, hs, runs=2)
+
+    def pinned(n):
+        ptr = L.ls_host_alloc(n)
+        return ptr, (lambda: L.ls_host_free(ptr))
+    hp = synth.HostStack(cfg, alloc=pinned)
+    try:
+        y1, ev1, *_ = _run(cfg, hp, runs=2)
+    finally:
+        hp.close()
+    assert ev1 == ev0
+    assert np.array_equal(_bits(y1), _bits(y0))
 
 
 # ------------------------------------------------------------------ faults (host-made, bounded)
