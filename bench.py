@@ -14,7 +14,9 @@ weights).
 
 N > 1 runs N independent replicas (one process per GPU under torchrun): the
 path has no exchange step, so the ranks share nothing but the barrier and the
-max-over-ranks timing. --impl reference times the CPU fp64 oracle instead.
+max-over-ranks timing (and, when N copies of the host stack would not fit the
+host's memory, one read-only host stack per node). --impl reference times the CPU
+fp64 oracle instead.
 """
 from __future__ import annotations
 
@@ -322,6 +324,61 @@ def write_timeline(path, L, ctx, x, y, T, s, logits, cfg):
                 f.write(f"{seg} | {name} | {'copy' if stream else 'compute'} | {a:.3f} | {b:.3f} | {b - a:.3f}\n")
 
 
+def mem_available() -> int:
+    """MemAvailable of the host in bytes (0 when unknown)."""
+    try:
+        with open("/proc/meminfo") as f:
+            for line in f:
+                if line.startswith("MemAvailable:"):
+                    return int(line.split()[1]) * 1024
+    except OSError:
+        pass
+    return 0
+
+
+def shared_host_stack(cfg, local_rank: int, barrier, local_world: int = 2):
+    """One host stack for all ranks of a node: local rank 0 draws it into a memfd and hands
+    the descriptor to the other local ranks over a Unix socket; they map the same pages.
+    Each process registers its own mapping with the library."""
+    import ctypes
+    import mmap as _mmap
+    import socket
+    total = synth.stack_bytes(cfg)
+    path = os.path.join(tempfile.gettempdir(), f"ls_bench_{cfg.name}_{os.environ.get('MASTER_PORT', '0')}.sock")
+    if local_rank == 0:
+        fd = os.memfd_create(f"ls_{cfg.name}")
+        os.ftruncate(fd, total)
+        if os.path.exists(path):
+            os.remove(path)
+        srv = socket.socket(socket.AF_UNIX, socket.SOCK_STREAM)
+        srv.bind(path)
+        srv.listen(local_world)
+        barrier()                   # the socket is listening
+        for _ in range(local_world - 1):
+            conn, _ = srv.accept()
+            socket.send_fds(conn, [b"fd"], [fd])
+            conn.close()
+        srv.close()
+        os.remove(path)
+    else:
+        barrier()
+        cli = socket.socket(socket.AF_UNIX, socket.SOCK_STREAM)
+        cli.connect(path)
+        _, fds, _, _ = socket.recv_fds(cli, 16, 1)
+        cli.close()
+        fd = fds[0]
+    m = _mmap.mmap(fd, total, _mmap.MAP_SHARED, _mmap.PROT_READ | _mmap.PROT_WRITE)
+    os.close(fd)
+    addr = ctypes.addressof(ctypes.c_char.from_buffer(m))
+
+    def alloc(n):
+        return addr, m.close
+
+    hs = synth.HostStack(cfg, alloc=alloc, draw=local_rank == 0)
+    barrier()                       # drawn before the other ranks read it
+    return hs
+
+
 def time_alone(torch, L, cfg, hs, x, logits, reps=20) -> dict:
     """{kernel class: average ms per launch} of a stack's GEMMs timed alone, at the workload's
     shapes: back-to-back launches on one stream between one pair of CUDA events, operands
@@ -414,7 +471,15 @@ def run_ours(args, cfg, world, rank, local):
     def pinned(nbytes):   # the stack's host memory: pinned and mapped by the driver (ls_host_alloc)
         ptr = L.ls_host_alloc(nbytes)
         return ptr, (lambda: L.ls_host_free(ptr))
-    hs = synth.HostStack(cfg, alloc=pinned)
+    local_world = int(os.environ.get("LOCAL_WORLD_SIZE", "1"))
+    barrier = (lambda: torch.distributed.barrier()) if world > 1 else (lambda: None)
+    host_memory = "ls_host_alloc (pinned and mapped by the driver)"
+    if local_world > 1 and mem_available() < local_world * synth.stack_bytes(cfg) * 1.1:
+        # N replicas of the stack do not fit the host: the ranks of this node share one
+        hs = shared_host_stack(cfg, local, barrier, local_world)
+        host_memory = f"one stack shared by the node's {local_world} ranks (memfd), registered by each"
+    else:
+        hs = synth.HostStack(cfg, alloc=pinned)
     p = L.ls_params_init(prefetch_depth=cfg.prefetch_depth, resident_layers=cfg.resident_layers,
                          max_vram_bytes=cfg.max_vram_bytes, use_pool=cfg.use_pool,
                          copy_path={"auto": 0, "kernel": 1, "engine": 2}[args.copy_path],
@@ -593,7 +658,7 @@ def run_ours(args, cfg, world, rank, local):
                             "warnings": stats["warnings"]},
                    "parallelism": f"replicas{world}" if world > 1 else "single",
                    "cross_run_prefetch": bool(args.cross_run),
-                   "host_memory": "ls_host_alloc (pinned and mapped by the driver)",
+                   "host_memory": host_memory,
                    "cuda_graph": bool(args.graph),
                    "expert_cache_bytes": int(args.expert_cache_gb * 2**30),
                    "l2": ("flushed between timed passes (256 MB write)" if flush_between else

@@ -133,6 +133,11 @@ def segment_slot_bytes(cfg: StackConfig) -> int:
     return sum(align256(t.nbytes) for t in segment_tensors(cfg))
 
 
+def stack_bytes(cfg: StackConfig) -> int:
+    """Bytes of a HostStack's buffer: every segment's footprint, then the shared tensors."""
+    return cfg.n_segments * segment_slot_bytes(cfg) + sum(align256(t.nbytes) for t in shared_tensors(cfg))
+
+
 # ---------------------------------------------------------------- the stacks
 def _tiny() -> StackConfig:
     s = 256 * 256 * 4 + 256 * 4
@@ -281,10 +286,12 @@ class HostStack:
     (segment, tensor_index, shared_id), the shapes the C ABI registers.
     bf16 tensors are uint16 views holding the bit patterns."""
 
-    def __init__(self, cfg: StackConfig, n_segments: int | None = None, threads: int = 0, alloc=None):
+    def __init__(self, cfg: StackConfig, n_segments: int | None = None, threads: int = 0, alloc=None,
+                 draw: bool = True):
         """``alloc(nbytes) -> (address, release)``, optional: where the buffer lives (for example
-        pinned memory from a driver allocator); ``release()`` is called by ``close()``. Default:
-        anonymous pages of the process."""
+        pinned memory from a driver allocator, or memory another process shares); ``release()``
+        is called by ``close()``. Default: anonymous pages of the process. ``draw=False`` lays
+        the views over a buffer that already holds the stack (drawn by another process)."""
         self.cfg = cfg
         n = cfg.n_segments if n_segments is None else n_segments
         specs = segment_tensors(cfg)
@@ -327,8 +334,9 @@ class HostStack:
             self.seg_views.append(views)
         jobs += [(SHARED_SEGMENT_ID, t, v) for t, v in zip(sh, self.shared_views)]
         threads = threads or (os.cpu_count() or 1)
-        with ThreadPoolExecutor(threads) as ex:
-            list(ex.map(lambda j: draw_tensor(cfg, j[0], j[1], j[2]), jobs))
+        if draw:
+            with ThreadPoolExecutor(threads) as ex:
+                list(ex.map(lambda j: draw_tensor(cfg, j[0], j[1], j[2]), jobs))
         self.segments = []
         self.shared_map = []
         for s in range(n):
