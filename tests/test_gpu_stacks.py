@@ -214,6 +214,13 @@ def test_moe_stack_full_size_with_and_without_expert_cache():
     y0, ev0, stats0, st0, _ = _run(cfg, hs, logits=lg_dev, runs=1, debug_checks=1)
     assert st0 == L.LS_OK and stats0["pool_slots"] == 2 and stats0["depth"] == 1
     assert stats0["debug_violations"] == 0
+    # the executed schedule is the simulator's, each load moving its layer's routed experts
+    from oracle import forward as F
+    eb = synth.segment_slot_bytes(cfg) // cfg.n_experts
+    lg = lg_dev.cpu().numpy()
+    load = [[len(np.unique(F.route_topk(lg[l], cfg.top_k)[0])) * eb for l in range(cfg.n_segments)]]
+    sim, _ = _sim_events(cfg, hs, 1, 0, cfg.max_vram_bytes, 1, 1, load=load)
+    assert ev0 == [tuple(e) for e in sim.events]
     rows = _rows(cfg, 8)
     ref = _oracle_from_host(cfg, hs, rows)
     assert rel_err(to_f64(y0)[rows], ref) <= BOUND
