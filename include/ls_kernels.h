@@ -178,7 +178,7 @@ ls_status lsk_moe_combine(const void* x_dev, int32_t x_f32, const float* y_dev, 
  * decreasing and that group e holds exactly the rows routed to expert e, in increasing
  * order. It only reads the three arrays; an invalid layer sets err_host[0] (pinned, mapped
  * host memory) = 4 | ((0x20000 + layer) << 8) if it is still 0. Returns LS_OK once
- * queued; the verdict is in err_host after the stream drains. */
+ * queued; the outcome is in err_host after the stream drains. */
 ls_status lsk_moe_check(const int32_t* sel_dev, const int32_t* row_table_dev, const int32_t* group_bounds_dev,
                         int32_t n_layers, int32_t T, int32_t k, int32_t E, uint32_t* err_host, void* stream);
 
