@@ -759,6 +759,17 @@ __device__ __forceinline__ void add_bias_row(const GemmParams& p, int n0, float 
         }
     }
 }
+// The bias of one 32-column chunk held across the warp: lane j has bias[n0 + j] (0 past N).
+// Read before the accumulator is ready (the bias is an input), it is then broadcast to every
+// row by shuffles: the epilogue touches no global memory for it after the wait.
+__device__ __forceinline__ float bias_lane(const GemmParams& p, int n0) {
+    const int c = n0 + (int)(threadIdx.x & 31);
+    return c < p.N ? bf2f(reinterpret_cast<const uint16_t*>(p.bias)[c]) : 0.f;
+}
+__device__ __forceinline__ void add_bias_lanes(float b, float (&v)[32]) {
+#pragma unroll
+    for (int j = 0; j < 32; ++j) v[j] += __shfl_sync(0xffffffffu, b, j);
+}
 // Four residual values at (row, col .. col+3), zeros past M or N (N % 8 == 0, so a
 // group of four never straddles N).
 __device__ __forceinline__ float4 load_resid4(const GemmParams& p, int row, int col) {
@@ -994,6 +1005,12 @@ __global__ void __launch_bounds__(s2_threads(EPI), 1) gemm_bf16_tc2(const __grid
             const int m2 = t % num_m2, n = t / num_m2;
             const int row0 = m2 * 256 + (int)rank * 128 + q * 32;
             const int nbase = DUAL ? n * 128 : n * BN;
+            // GELU epilogue: the bias of this warp's first two chunks, one value per lane (more
+            // chunks are rare: they read theirs after the wait)
+            const bool has_bias = EPI == EPI_BIAS_GELU;
+            const float bl0 = has_bias && n_chunks > 0 ? bias_lane(p, nbase + c_begin * 32) : 0.f;
+            const float bl1 = has_bias && n_chunks > 1 ? bias_lane(p, nbase + (c_begin + 1) * 32) : 0.f;
+            auto bias_of = [&](int i, int n0) { return i == 0 ? bl0 : i == 1 ? bl1 : bias_lane(p, n0); };
             // A CTA's last tile leaves the other accumulator buffer unused: its residual
             // goes there (row per lane, as the accumulator) while the MMAs still run, so the
             // epilogue after the last accumulator reads no global memory.
@@ -1062,7 +1079,7 @@ __global__ void __launch_bounds__(s2_threads(EPI), 1) gemm_bf16_tc2(const __grid
 #pragma unroll
                     for (int j = 0; j < 32; ++j) v[j] = __uint_as_float(r[j]);
                     if (EPI == EPI_BIAS_GELU) {
-                        add_bias_row(p, n0, v);
+                        add_bias_lanes(bias_of(i, n0), v);
                         gelu_inplace<32>(v);
                     }
                     const uint32_t s32 = stg + NBUF * S2_STG_BF + (uint32_t)sb * S2_STG_F32;
