@@ -1618,7 +1618,10 @@ ls_status ls_run(ls_ctx* c, const void* x_dev, void* y_dev, int64_t tokens, void
     return st;
 }
 
-ls_status ls_run_host(ls_ctx* c, const void* x_host, void* y_host, int64_t tokens, const ls_moe_routing* routing_host) {
+// ls_run_host (sync) and ls_run_host_async (!sync): the inputs' copies, the pass and the
+// output's copy, queued in that order on the context's own stream
+static ls_status run_host(ls_ctx* c, const void* x_host, void* y_host, int64_t tokens,
+                          const ls_moe_routing* routing_host, bool sync) {
     if (!c) return LS_ERR_INVALID_ARG;
     if (!c->registered) {
         set_err(c, "ls_run_host before ls_register_segments");
@@ -1665,9 +1668,19 @@ ls_status ls_run_host(ls_ctx* c, const void* x_host, void* y_host, int64_t token
         return st;
     }
     CK(cudaMemcpyAsync(y_host, c->stage_y, xb, cudaMemcpyDeviceToHost, c->own_stream));
+    if (!sync) return st;
     const ls_status sy = ls_sync(c);
     if (sy < 0) return sy;
     return st;
+}
+
+ls_status ls_run_host(ls_ctx* c, const void* x_host, void* y_host, int64_t tokens, const ls_moe_routing* routing_host) {
+    return run_host(c, x_host, y_host, tokens, routing_host, true);
+}
+
+ls_status ls_run_host_async(ls_ctx* c, const void* x_host, void* y_host, int64_t tokens,
+                            const ls_moe_routing* routing_host) {
+    return run_host(c, x_host, y_host, tokens, routing_host, false);
 }
 
 ls_status ls_get_schedule(ls_ctx* c, ls_sched_event* out, int64_t cap, int64_t* n_out) {

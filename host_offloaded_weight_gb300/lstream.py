@@ -104,6 +104,7 @@ _sig = {
     "ls_register_segments": (_I32, [_P, C.POINTER(ls_segment_desc), _I32, C.POINTER(ls_shared_ref), _I32]),
     "ls_run": (_I32, [_P, _P, _P, _I64, _P, C.POINTER(ls_moe_routing)]),
     "ls_run_host": (_I32, [_P, _P, _P, _I64, C.POINTER(ls_moe_routing)]),
+    "ls_run_host_async": (_I32, [_P, _P, _P, _I64, C.POINTER(ls_moe_routing)]),
     "ls_run_async": (_I32, [_P, _P, _P, _I64, _P, C.POINTER(ls_moe_routing)]),
     "ls_sync": (_I32, [_P]),
     "ls_get_schedule": (_I32, [_P, C.POINTER(ls_sched_event), _I64, C.POINTER(_I64)]),
@@ -290,6 +291,13 @@ def ls_run_host(ctx: Ctx, x_host, y_host, tokens: int, logits_host=None, top_k: 
     r = _routing(logits_host, top_k)
     return _check(_lib.ls_run_host(ctx.handle, _ptr(x_host), _ptr(y_host), int(tokens),
                                    C.byref(r) if r is not None else None), ctx)
+
+
+def ls_run_host_async(ctx: Ctx, x_host, y_host, tokens: int, logits_host=None, top_k: int = 0) -> int:
+    """ls_run_host queued on the context's own stream; y_host is valid after ls_sync."""
+    r = _routing(logits_host, top_k)
+    return _check(_lib.ls_run_host_async(ctx.handle, _ptr(x_host), _ptr(y_host), int(tokens),
+                                         C.byref(r) if r is not None else None), ctx)
 
 
 def _events(buf, n):

@@ -291,6 +291,18 @@ ls_status ls_sync(ls_ctx* ctx);
 ls_status ls_run_host(ls_ctx* ctx, const void* x_host, void* y_host, int64_t tokens,
                       const ls_moe_routing* routing_host);
 
+/* ls_run_host without the final synchronisation: the copy of x_host (and the logits) in,
+ * the pass and the copy of y back into y_host are queued, in that order, on the context's
+ * own stream, and the call returns (for the MoE kind after the routing sync of ls_run_async,
+ * which also waits for the previous pass's compute). Consecutive calls pipeline: a pass's
+ * inputs are copied in once the previous pass has finished with the staging buffers, while
+ * the weight copies of the passes keep the host link busy. The host buffers must stay valid,
+ * and y_host unread, until ls_sync returns; ls_sync also reports the passes' device errors.
+ * Pinned host buffers are needed for the copies to be asynchronous (CUDA copies pageable
+ * memory synchronously). Errors as ls_run_host. */
+ls_status ls_run_host_async(ls_ctx* ctx, const void* x_host, void* y_host, int64_t tokens,
+                            const ls_moe_routing* routing_host);
+
 /* Copy up to `cap` logged events (oldest first) into out; *n_out = total logged. */
 ls_status ls_get_schedule(ls_ctx* ctx, ls_sched_event* out, int64_t cap, int64_t* n_out);
 

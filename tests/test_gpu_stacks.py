@@ -406,6 +406,38 @@ def test_run_host_matches_run():
         L.ls_ctx_destroy(ctx)
 
 
+@pytest.mark.parametrize("kind", ["proj", "moe"])
+def test_run_host_async_pipelines_distinct_inputs(kind):
+    """Passes queued from host buffers (ls_run_host_async), each with its own input, logits and
+    output buffer, then one ls_sync: every output has the bits of an ls_run of its input."""
+    if kind == "moe":
+        cfg = _moe_cfg(3, 200, experts=16, hidden=128, ffn=64, k=4)
+    else:
+        cfg = SMALL["proj"]
+    hs = synth.HostStack(cfg)
+    ctx, _ = make_ctx(cfg, hs, max_vram_bytes=0 if kind == "proj" else cfg.max_vram_bytes)
+    try:
+        g = torch.Generator().manual_seed(5)
+        xs = [(torch.randn(cfg.tokens, cfg.hidden, generator=g) * (i + 1)).to(torch.bfloat16) for i in range(3)]
+        lgs = [torch.randn(cfg.n_segments, cfg.tokens, cfg.n_experts, generator=g) * 2 if kind == "moe" else None
+               for _ in range(3)]
+        refs = []
+        for x, lg in zip(xs, lgs):
+            y = torch.empty(cfg.tokens, cfg.hidden, dtype=torch.bfloat16, device="cuda")
+            L.ls_run(ctx, x.cuda(), y, cfg.tokens, logits=lg.cuda() if lg is not None else None, top_k=cfg.top_k)
+            refs.append(y.cpu())
+        xh = [x.pin_memory() for x in xs]
+        lh = [lg.pin_memory() if lg is not None else None for lg in lgs]
+        yh = [torch.full((cfg.tokens, cfg.hidden), float("nan"), dtype=torch.bfloat16).pin_memory() for _ in range(3)]
+        for i in range(3):
+            L.ls_run_host_async(ctx, xh[i], yh[i], cfg.tokens, lh[i], cfg.top_k)
+        L.ls_sync(ctx)
+        for i in range(3):
+            assert torch.equal(yh[i].view(torch.int16), refs[i].view(torch.int16)), i
+    finally:
+        L.ls_ctx_destroy(ctx)
+
+
 def test_kernel_timing_switch():
     """Per-launch timing switched on between passes: refused while a pass is
     queued, and the results do not depend on it (timed and untimed passes
