@@ -284,6 +284,9 @@ __device__ __forceinline__ float bf2f(uint16_t h) { return __uint_as_float((uint
 // |error| <= 3e-7 (odd extension for z < 0); evaluated in fp32 the sixteenth
 // power amplifies rounding to at most 2e-6 in erf. With z = |v|/sqrt 2 and
 // q = 1 - erf(z), both signs reduce to GELU(v) = max(v, 0) - (|v|/2) q.
+// The argument's scale and the 1/2 are folded into the polynomial, taken in u = |v|:
+// b_i = c a_i 2^(-i/2) with b_0 = c = 2^(1/16), so that (b(u))^16 = 2 (1 + ... + a6 z^6)^16 and
+// GELU(v) = max(v, 0) - u / b(u)^16 (the same function; two multiplications fewer per pair).
 // One approximate reciprocal per element (the only special-function op; +inf
 // gives 0); the rest runs two elements per instruction on the packed fp32
 // pipe. All of it sits far below the bf16 rounding of the output.
@@ -294,20 +297,19 @@ __device__ __forceinline__ float rcp_approx(float x) {
 }
 __device__ __forceinline__ float2 f2(float a) { return make_float2(a, a); }
 __device__ __forceinline__ float2 gelu2(float2 v) {
-    const float2 z = __fmul2_rn(make_float2(fabsf(v.x), fabsf(v.y)), f2(0.70710678118654752f));
-    float2 p = __ffma2_rn(f2(4.30638e-5f), z, f2(2.765672e-4f));
-    p = __ffma2_rn(p, z, f2(1.520143e-4f));
-    p = __ffma2_rn(p, z, f2(9.2705272e-3f));
-    p = __ffma2_rn(p, z, f2(4.22820123e-2f));
-    p = __ffma2_rn(p, z, f2(7.05230784e-2f));
-    p = __ffma2_rn(p, z, f2(1.0f));
+    const float2 u = make_float2(fabsf(v.x), fabsf(v.y));
+    float2 p = __ffma2_rn(f2(5.6213e-06f), u, f2(5.105521e-05f));
+    p = __ffma2_rn(p, u, f2(3.9686136e-05f));
+    p = __ffma2_rn(p, u, f2(3.4227392e-03f));
+    p = __ffma2_rn(p, u, f2(2.2076998e-02f));
+    p = __ffma2_rn(p, u, f2(5.2075163e-02f));
+    p = __ffma2_rn(p, u, f2(1.0442737f));
     p = __fmul2_rn(p, p);
     p = __fmul2_rn(p, p);
     p = __fmul2_rn(p, p);
     p = __fmul2_rn(p, p);
     const float2 q = make_float2(rcp_approx(p.x), rcp_approx(p.y));
-    const float2 w = __fmul2_rn(z, f2(-0.70710678118654752f));  // -|v|/2
-    return __ffma2_rn(w, q, make_float2(fmaxf(v.x, 0.f), fmaxf(v.y, 0.f)));
+    return __ffma2_rn(make_float2(-u.x, -u.y), q, make_float2(fmaxf(v.x, 0.f), fmaxf(v.y, 0.f)));
 }
 // in place over an even-length register array
 template <int N>
