@@ -485,7 +485,8 @@ def run_ours(args, cfg, world, rank, local):
                          copy_path={"auto": 0, "kernel": 1, "engine": 2}[args.copy_path],
                          copy_ctas=args.copy_ctas, reserve_sms=args.reserve_sms, kernel_timing=0,
                          cross_run_prefetch=int(args.cross_run),
-                         expert_cache_bytes=int(args.expert_cache_gb * 2**30))
+                         expert_cache_bytes=int(args.expert_cache_gb * 2**30),
+                         debug_checks=int(args.debug_checks))
     ctx = L.ls_ctx_create(p)
     L.ls_register_segments(ctx, hs.segments, hs.shared_map)
     T = cfg.tokens
@@ -662,7 +663,7 @@ def run_ours(args, cfg, world, rank, local):
                    "parallelism": f"replicas{world}" if world > 1 else "single",
                    "cross_run_prefetch": bool(args.cross_run),
                    "host_memory": host_memory,
-                   "cuda_graph": bool(args.graph),
+                   "cuda_graph": bool(args.graph), "debug_checks": bool(args.debug_checks),
                    "expert_cache_bytes": int(args.expert_cache_gb * 2**30),
                    "l2": ("flushed between timed passes (256 MB write)" if flush_between else
                           f"inputs larger than L2: each pass streams {streamed_per_pass / 1e6:.0f} MB of "
@@ -725,6 +726,8 @@ def main() -> int:
     ap.add_argument("--ref-tokens", type=int, default=0, help="token rows of the reference arm's sample (0: per workload)")
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--no-alone", action="store_true", help="skip timing the GEMMs alone after the passes")
+    ap.add_argument("--debug-checks", action="store_true",
+                    help="run with params.debug_checks (canaries after every slot, MoE table checks): their cost")
     ap.add_argument("--prefetch-depth", type=int, default=None,
                     help="override the workload's prefetch depth (the planner re-derives residents)")
     ap.add_argument("--expert-cache-gb", type=float, default=0.0,
