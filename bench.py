@@ -165,6 +165,7 @@ def aggregate(step_seconds: float, units: float, world: int, device=None) -> tup
 CPU_SAMPLE = {"tiny_f32_4x256": (8, None), "dit_ffn_12x1024x4096": (1024, None),
               "shared_proj_24x3072x12288": (256, 4), "swiglu_48x5120x13824": (512, 2),
               "moe_48x128x2048x768": (256, 1)}
+E2E_BLOCK = 5   # steps per block of the alternating device-buffer / host-buffer measurement
 REF_SAMPLE = {"tiny_f32_4x256": (8, None), "dit_ffn_12x1024x4096": (256, None),
               "shared_proj_24x3072x12288": (64, 2), "swiglu_48x5120x13824": (128, 1),
               "moe_48x128x2048x768": (128, 1)}
@@ -519,15 +520,15 @@ def run_ours(args, cfg, world, rank, local):
         else:
             L.ls_run_async(ctx, x, y, T, s, logits=logits, top_k=cfg.top_k)
     L.ls_sync(ctx)
-    n_ev0 = len(L.ls_get_schedule(ctx))
 
-    def timed_passes(graph=False):
+    def timed_passes(graph=False, n=None):
+        n = args.steps if n is None else n
         ev = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True))
-              for _ in range(args.steps)]
+              for _ in range(n)]
         if world > 1:
             torch.distributed.barrier()
         torch.cuda.synchronize()
-        for i in range(args.steps):
+        for i in range(n):
             if flush_between:
                 flush.zero_()                # write 256 MB (> 129 MB L2) between timed passes
             ev[i][0].record(s)
@@ -542,9 +543,31 @@ def run_ours(args, cfg, world, rank, local):
             torch.distributed.barrier()
         return [a.elapsed_time(b) for a, b in ev]
 
-    # throughput: passes as a user runs them (no per-launch events in the stream)
-    step_ms = timed_passes(graph=args.graph)
-    sched = L.ls_get_schedule(ctx)[n_ev0:]
+    # throughput (device buffers, passes as a user queues them, no per-launch events in the
+    # stream) and end to end (host buffers: every step copies its input in from pinned host memory
+    # and its output back out, queued with ls_run_host_async as a serving loop would queue them,
+    # one ls_sync closing each block) in alternating blocks of E2E_BLOCK steps: both then see the
+    # same state of the host, whose DMA reads of the stack slow down over a process's life
+    xh = x.cpu().pin_memory()
+    yh = torch.empty_like(xh).pin_memory()
+    lh = logits.cpu().pin_memory() if logits is not None else None
+    for _ in range(2):
+        L.ls_run_host(ctx, xh, yh, T, lh, cfg.top_k)
+    L.ls_sync(ctx)
+    step_ms, sched, e2e_total = [], [], 0.0
+    for b0 in range(0, args.steps, E2E_BLOCK):
+        nb = min(E2E_BLOCK, args.steps - b0)
+        n_before = len(L.ls_get_schedule(ctx))
+        step_ms += timed_passes(graph=args.graph, n=nb)
+        sched += L.ls_get_schedule(ctx)[n_before:]
+        if world > 1:
+            torch.distributed.barrier()
+        t0 = time.perf_counter()
+        for _ in range(nb):
+            L.ls_run_host_async(ctx, xh, yh, T, lh, cfg.top_k)
+        L.ls_sync(ctx)
+        e2e_total += time.perf_counter() - t0
+    e2e_s = e2e_total / args.steps
     # kernel times: the same K passes again with every launch bracketed by events
     L.ls_set_kernel_timing(ctx, 1)
     L.ls_get_kernel_times(ctx, reset=True)
@@ -568,21 +591,6 @@ def run_ours(args, cfg, world, rank, local):
     flops = seg_flops(cfg, T) * cfg.n_segments
     max_s, total_tokens = aggregate(mean_s, float(T), world, dev if world > 1 else None)
     value = total_tokens / max_s
-    # --- end to end through the host-buffer entry point: every step copies its input in from
-    # pinned host memory and its output back out, queued (ls_run_host_async) so that the steps
-    # pipeline as a serving loop would; one ls_sync ends the timed region
-    xh = x.cpu().pin_memory()
-    yh = torch.empty_like(xh).pin_memory()
-    lh = logits.cpu().pin_memory() if logits is not None else None
-    for _ in range(2):
-        L.ls_run_host(ctx, xh, yh, T, lh, cfg.top_k)
-    if world > 1:
-        torch.distributed.barrier()
-    t0 = time.perf_counter()
-    for _ in range(args.steps):
-        L.ls_run_host_async(ctx, xh, yh, T, lh, cfg.top_k)
-    L.ls_sync(ctx)
-    e2e_s = (time.perf_counter() - t0) / args.steps
     e2e_max, e2e_tokens = aggregate(e2e_s, float(T), world, dev if world > 1 else None)
     h2d = xh.numel() * xh.element_size() + (lh.numel() * 4 if lh is not None else 0)
     d2h = yh.numel() * yh.element_size()
