@@ -684,6 +684,26 @@ def test_moe_small_all_rows():
     assert np.array_equal(_bits(y0), _bits(y))
 
 
+def test_moe_token_counts_change_between_runs():
+    """One MoE context runs passes of 1, 7, 200 and 33 tokens in turn (most experts empty at one
+    token: 4 of 16 routed); rows are independent given their logits, so each pass matches the
+    oracle's first T rows."""
+    cfg = _moe_cfg(3, 200, experts=16, hidden=128, ffn=64, k=4)
+    hs = synth.HostStack(cfg)
+    lg_dev, _ = logits_dev(cfg)
+    ref = ostack.stack_forward(cfg)
+    ctx, _ = make_ctx(cfg, hs)
+    try:
+        x = x_dev(cfg)
+        for T in (1, 7, 200, 33):
+            y = torch.empty_like(x[:T])
+            L.ls_run(ctx, x[:T].contiguous(), y, T, logits=lg_dev[:, :T].contiguous(), top_k=cfg.top_k)
+            torch.cuda.synchronize()
+            assert rel_err(to_f64(y), ref[:T]) <= BOUND, T
+    finally:
+        L.ls_ctx_destroy(ctx)
+
+
 def test_moe_residents_follow_routing_changes():
     """Resident MoE layers hold every expert: a later pass that routes to other experts
     still matches the oracle (a resident loaded with only the first pass's routed experts
