@@ -656,22 +656,28 @@ constexpr int S2_STG_F32 = 32 * 32 * 4;        // 32x32 fp32 output staging tile
 // per thread, the cap of a 10-warp CTA). The others run 16 epilogue warps (4 per TMEM
 // lane quarter, 96 registers) so that more warps hide each other's latencies; every
 // epilogue warp single-buffers its staging tiles. The mainloop takes as many stages
-// as the rest of shared memory holds (at most 8).
+// as the rest of shared memory holds (at most 8). ONE (residual epilogues where every
+// CTA pair has at most one tile): that tile is the pair's last, so its fp32 chunks are
+// staged in the mainloop's stage memory, free once its MMAs are done, and only the
+// bf16 staging tiles take room from the stages.
 __host__ __device__ constexpr bool s2_out_f32(int epi) { return epi == EPI_BIAS_RESID || epi == EPI_RESID; }
 __host__ __device__ constexpr int s2_nbuf(int) { return 1; }
 __host__ __device__ constexpr int s2_epi_warps(int epi) { return s2_out_f32(epi) ? 8 : 16; }
 __host__ __device__ constexpr int s2_threads(int epi) { return 64 + 32 * s2_epi_warps(epi); }
-__host__ __device__ constexpr int s2_warp_bytes(int epi) {
-    return s2_nbuf(epi) * (S2_STG_BF + (s2_out_f32(epi) ? S2_STG_F32 : 0));
+__host__ __device__ constexpr int s2_warp_bytes(int epi, bool one = false) {
+    return s2_nbuf(epi) * (S2_STG_BF + (s2_out_f32(epi) && !one ? S2_STG_F32 : 0));
 }
-__host__ __device__ constexpr int s2_stages(int epi, int bn) {
-    return (232448 - 1024 - 256 - s2_epi_warps(epi) * s2_warp_bytes(epi)) / s2_stage_bytes(bn) < 8
-               ? (232448 - 1024 - 256 - s2_epi_warps(epi) * s2_warp_bytes(epi)) / s2_stage_bytes(bn)
+__host__ __device__ constexpr int s2_stages(int epi, int bn, bool one = false) {
+    return (232448 - 1024 - 256 - s2_epi_warps(epi) * s2_warp_bytes(epi, one)) / s2_stage_bytes(bn) < 8
+               ? (232448 - 1024 - 256 - s2_epi_warps(epi) * s2_warp_bytes(epi, one)) / s2_stage_bytes(bn)
                : 8;
 }
-__host__ __device__ constexpr int s2_smem_bytes(int epi, int bn) {
-    return s2_stages(epi, bn) * s2_stage_bytes(bn) + s2_epi_warps(epi) * s2_warp_bytes(epi) + 1024 + 256;
+__host__ __device__ constexpr int s2_smem_bytes(int epi, int bn, bool one = false) {
+    return s2_stages(epi, bn, one) * s2_stage_bytes(bn) + s2_epi_warps(epi) * s2_warp_bytes(epi, one) + 1024 + 256;
 }
+static_assert(s2_stages(EPI_BIAS_RESID, 256, true) == 6 && s2_stages(EPI_RESID, 160, true) == 8 &&
+                  8 * S2_STG_F32 <= s2_stages(EPI_RESID, 160, true) * s2_stage_bytes(160),
+              "one-tile residual layout: the fp32 staging fits in the stage memory");
 static_assert(s2_stages(EPI_BIAS_RESID, 256) == 5 && s2_stages(EPI_STORE, 256) == 6, "stages at BN = 256");
 static_assert(s2_smem_bytes(EPI_BIAS_RESID, 160) <= 232448 && s2_smem_bytes(EPI_STORE, 160) <= 232448, "shared memory");
 
@@ -806,16 +812,17 @@ __device__ __forceinline__ float4 ld_shared_f4(uint32_t addr) {
     return v;
 }
 
-template <int EPI, bool DUAL, int BN>
+template <int EPI, bool DUAL, int BN, bool ONE = false>
 __global__ void __launch_bounds__(s2_threads(EPI), 1) gemm_bf16_tc2(const __grid_constant__ GemmParams p) {
     static_assert(BN % 32 == 0 && BN >= 64 && BN <= 256 && (!DUAL || BN == 256), "tile width");
+    static_assert(!ONE || s2_out_f32(EPI), "one-tile layout: residual epilogues");
     extern __shared__ uint8_t smem_raw[];
     const uint32_t raw = smem_u32(smem_raw);
     const uint32_t base = (raw + 1023u) & ~1023u;
     uint8_t* gbase = smem_raw + (base - raw);
-    constexpr int S2_STAGES = s2_stages(EPI, BN);
+    constexpr int S2_STAGES = s2_stages(EPI, BN, ONE);
     constexpr int S2_STAGE = s2_stage_bytes(BN);
-    constexpr int WSB = s2_warp_bytes(EPI);
+    constexpr int WSB = s2_warp_bytes(EPI, ONE);
     constexpr bool OUT32 = s2_out_f32(EPI);
     constexpr int NBUF = s2_nbuf(EPI);
     const uint32_t stg0 = base + S2_STAGES * S2_STAGE;  // epilogue staging tiles, WSB bytes per warp
@@ -975,7 +982,9 @@ __global__ void __launch_bounds__(s2_threads(EPI), 1) gemm_bf16_tc2(const __grid
         // Chunk output: v (row per lane) goes into the swizzled staging tiles and out by
         // bulk tensor stores. The caller has made sure the staging tiles are free.
         auto store_chunk = [&](float (&v)[32], int n0, int row0) {
-            const uint32_t s32 = stg + NBUF * S2_STG_BF + (uint32_t)sb * S2_STG_F32;
+            // ONE: the fp32 tile in the stage memory (the cluster's one tile is its last)
+            const uint32_t s32 = ONE ? base + (uint32_t)(warp - 2) * S2_STG_F32
+                                     : stg + NBUF * S2_STG_BF + (uint32_t)sb * S2_STG_F32;
             const uint32_t sbf = stg + (uint32_t)sb * S2_STG_BF;
             // 64-byte swizzle: 16-byte unit j of row r sits at unit j ^ ((r >> 1) & 3)
 #pragma unroll
@@ -1016,7 +1025,7 @@ __global__ void __launch_bounds__(s2_threads(EPI), 1) gemm_bf16_tc2(const __grid
             // A CTA's last tile leaves the other accumulator buffer unused: its residual
             // goes there (row per lane, as the accumulator) while the MMAs still run, so the
             // epilogue after the last accumulator reads no global memory.
-            const bool last = OUT32 && t + n_clusters >= num_tiles;
+            const bool last = OUT32 && (ONE || t + n_clusters >= num_tiles);
             const uint32_t rbase = tmem_base + ((uint32_t)(q * 32) << 16) + (uint32_t)((buf ^ 1) * ACC_COLS);
             float4 g[2][8];
             if (last) {
@@ -1274,20 +1283,20 @@ cudaError_t launch_t(const GemmParams& p, int grid, cudaStream_t s) {
     return cudaLaunchKernelEx(&cfg, kern, p);
 }
 
-template <int EPI, bool DUAL, int BN>
+template <int EPI, bool DUAL, int BN, bool ONE = false>
 cudaError_t launch_t2(const GemmParams& p, int clusters, cudaStream_t s) {
-    auto kern = gemm_bf16_tc2<EPI, DUAL, BN>;
+    auto kern = gemm_bf16_tc2<EPI, DUAL, BN, ONE>;
     static bool attr_set = false;
     if (!attr_set) {
         cudaError_t e =
-            cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, s2_smem_bytes(EPI, BN));
+            cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, s2_smem_bytes(EPI, BN, ONE));
         if (e != cudaSuccess) return e;
         attr_set = true;
     }
     cudaLaunchConfig_t cfg = {};
     cfg.gridDim = dim3(2 * clusters);
     cfg.blockDim = dim3(s2_threads(EPI));
-    cfg.dynamicSmemBytes = s2_smem_bytes(EPI, BN);
+    cfg.dynamicSmemBytes = s2_smem_bytes(EPI, BN, ONE);
     cfg.stream = s;
     cudaLaunchAttribute at[2];
     at[0].id = cudaLaunchAttributeClusterDimension;
@@ -1301,13 +1310,13 @@ cudaError_t launch_t2(const GemmParams& p, int clusters, cudaStream_t s) {
     return cudaLaunchKernelEx(&cfg, kern, p);
 }
 
-template <int EPI>
+template <int EPI, bool ONE = false>
 cudaError_t launch_t2_bn(const GemmParams& p, int bn, int clusters, cudaStream_t s) {
     switch (bn) {
-        case 256: return launch_t2<EPI, false, 256>(p, clusters, s);
-        case 224: return launch_t2<EPI, false, 224>(p, clusters, s);
-        case 192: return launch_t2<EPI, false, 192>(p, clusters, s);
-        case 160: return launch_t2<EPI, false, 160>(p, clusters, s);
+        case 256: return launch_t2<EPI, false, 256, ONE>(p, clusters, s);
+        case 224: return launch_t2<EPI, false, 224, ONE>(p, clusters, s);
+        case 192: return launch_t2<EPI, false, 192, ONE>(p, clusters, s);
+        case 160: return launch_t2<EPI, false, 160, ONE>(p, clusters, s);
     }
     return cudaErrorInvalidValue;
 }
@@ -1456,11 +1465,18 @@ cudaError_t launch_gemm_bf16(const GemmDesc& d, int max_ctas, cudaStream_t s) {
         int clusters = grid / 2;
         if (clusters > pair_tiles) clusters = pair_tiles;
         if (clusters < 1) clusters = 1;
+        // every cluster with one tile: the residual epilogues' one-tile layout (more stages; the
+        // same arithmetic, so the bits do not change with the grid)
+        const bool one = pair_tiles <= clusters;
         switch (d.epi) {
             case EPI_STORE: return launch_t2_bn<EPI_STORE>(p, bn2, clusters, s);
             case EPI_BIAS_GELU: return launch_t2_bn<EPI_BIAS_GELU>(p, bn2, clusters, s);
-            case EPI_BIAS_RESID: return launch_t2_bn<EPI_BIAS_RESID>(p, bn2, clusters, s);
-            case EPI_RESID: return launch_t2_bn<EPI_RESID>(p, bn2, clusters, s);
+            case EPI_BIAS_RESID:
+                return one ? launch_t2_bn<EPI_BIAS_RESID, true>(p, bn2, clusters, s)
+                           : launch_t2_bn<EPI_BIAS_RESID>(p, bn2, clusters, s);
+            case EPI_RESID:
+                return one ? launch_t2_bn<EPI_RESID, true>(p, bn2, clusters, s)
+                           : launch_t2_bn<EPI_RESID>(p, bn2, clusters, s);
             case EPI_SWIGLU: return launch_t2<EPI_SWIGLU, true, 256>(p, clusters, s);
         }
         return cudaErrorInvalidValue;
