@@ -438,6 +438,38 @@ def test_run_host_async_pipelines_distinct_inputs(kind):
         L.ls_ctx_destroy(ctx)
 
 
+def test_readme_example():
+    """The usage shown in the README: torch bf16 CPU tensors registered as FFN segments, one
+    pass on device tensors, against the fp64 oracle layer by layer."""
+    from oracle import forward as F
+    g = torch.Generator().manual_seed(9)
+    T, H, Fw, n = 300, 256, 512, 5
+    layers = []
+    for _ in range(n):
+        w1 = (torch.randn(Fw, H, generator=g) / H ** 0.5).to(torch.bfloat16)
+        b1 = (torch.randn(Fw, generator=g) * 0.1).to(torch.bfloat16)
+        w2 = (torch.randn(H, Fw, generator=g) / Fw ** 0.5 / n ** 0.5).to(torch.bfloat16)
+        b2 = (torch.randn(H, generator=g) * 0.1).to(torch.bfloat16)
+        layers.append((w1, b1, w2, b2))
+    x = torch.randn(T, H, generator=g).to(torch.bfloat16).cuda()
+    segs = [(L.LS_KIND_FFN_GELU_BF16, [w1, b1, w2, b2]) for (w1, b1, w2, b2) in layers]
+    ctx = L.ls_ctx_create(L.ls_params_init(prefetch_depth=1, resident_layers=-1,
+                                           max_vram_bytes=2 * sum(t.nbytes for t in layers[0]), use_pool=1))
+    try:
+        L.ls_register_segments(ctx, segs)
+        y = torch.empty_like(x)
+        L.ls_run(ctx, x, y, x.shape[0])
+        torch.cuda.synchronize()
+        assert L.ls_get_stats(ctx)["depth"] == 1 and len(L.ls_get_schedule(ctx)) > 0
+    finally:
+        L.ls_ctx_destroy(ctx)
+    f64 = lambda t: t.float().numpy().astype(np.float64)
+    ref = f64(x.cpu())
+    for (w1, b1, w2, b2) in layers:
+        ref = F.ffn_gelu(ref, f64(w1), f64(b1), f64(w2), f64(b2))
+    assert rel_err(to_f64(y), ref) <= BOUND
+
+
 def test_kernel_timing_switch():
     """Per-launch timing switched on between passes: refused while a pass is
     queued, and the results do not depend on it (timed and untimed passes
