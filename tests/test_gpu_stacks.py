@@ -556,6 +556,59 @@ def test_replan_between_runs_keeps_the_bits(pool):
         L.ls_ctx_destroy(ctx)
 
 
+@pytest.mark.parametrize("seed,pool,cross", [(1, 1, False), (2, 0, False), (3, 1, True), (4, 0, True)])
+def test_random_sequences_of_passes_and_replans(seed, pool, cross):
+    """Seeded random sequences on one context: passes of random token counts through ls_run,
+    ls_run_async (synchronised before the next plan change) and ls_run_host, and plan changes
+    of depth, residency and budget in between. Every output matches the oracle's first T rows,
+    full-length passes keep the all-resident bits, and the executed schedule is the
+    simulator's for the same script."""
+    cfg = SMALL["ffn"]
+    hs = synth.HostStack(cfg)
+    S = synth.segment_slot_bytes(cfg)
+    ref_bits, _, _, _, _ = _run(cfg, hs, runs=1, max_vram_bytes=0)
+    ref = ostack.stack_forward(cfg)
+    rng = np.random.default_rng(seed)
+    n = cfg.n_segments
+    script, outs = [], []
+    ctx, _ = make_ctx(cfg, hs, prefetch_depth=1, resident_layers=-1, max_vram_bytes=3 * S, use_pool=pool,
+                      cross_run_prefetch=int(cross))
+    try:
+        x = x_dev(cfg)
+        for _ in range(24):
+            op = rng.choice(["run", "async", "host", "replan"], p=[0.35, 0.25, 0.15, 0.25])
+            if op == "replan":
+                L.ls_sync(ctx)
+                step = ("replan", int(rng.integers(0, 4)), int(rng.choice([-1, 0, 1, 3])),
+                        int(rng.choice([0, S // 2, 2 * S, 3 * S, 5 * S, (n + 3) * S])))
+                L.ls_replan(ctx, *step[1:])
+                script.append(step)
+                continue
+            T = int(rng.choice([1, 2, 64, 129, 200, cfg.tokens]))
+            T = min(T, cfg.tokens)
+            xin = x[:T].contiguous()
+            if op == "host":
+                yh = torch.empty(T, cfg.hidden, dtype=torch.bfloat16).pin_memory()
+                L.ls_run_host(ctx, xin.cpu().pin_memory(), yh, T)
+                outs.append((T, yh))
+            else:
+                y = torch.empty_like(xin)
+                (L.ls_run if op == "run" else L.ls_run_async)(ctx, xin, y, T)
+                outs.append((T, y))
+            script.append(("run",))
+        L.ls_sync(ctx)
+        torch.cuda.synchronize()
+        for T, y in outs:
+            assert rel_err(to_f64(y), ref[:T]) <= BOUND, T
+            if T == cfg.tokens:
+                assert torch.equal(y.cpu().view(torch.int16), ref_bits.cpu().view(torch.int16))
+        ev, sst = _sched_script(cfg, hs, 1, -1, 3 * S, pool, script, cross=cross)
+        assert all(v >= 0 for v in sst)
+        assert L.ls_get_schedule(ctx) == ev
+    finally:
+        L.ls_ctx_destroy(ctx)
+
+
 @pytest.mark.parametrize("pool", [1, 0])
 def test_cross_run_window_matches_simulator_and_bits(pool):
     """The opt-in cross-run window queues the next run's first streamed segment during the
