@@ -824,6 +824,52 @@ def test_moe_residents_follow_routing_changes():
         L.ls_ctx_destroy(ctx)
 
 
+@pytest.mark.parametrize("seed", [5, 6])
+def test_moe_random_sequences_of_routings_and_token_counts(seed):
+    """Seeded random MoE passes on one context (one resident layer, three streamed): each pass
+    draws its own logits (sometimes skewed towards few experts) and token count, and runs
+    through ls_run, ls_run_async or ls_run_host. Every output matches the oracle with those
+    logits, and each streamed load moves exactly the experts its pass's tokens route to."""
+    from oracle import forward as F
+    cfg = _moe_cfg(4, 96, experts=8, hidden=256, ffn=128, k=2)
+    S = synth.segment_slot_bytes(cfg)
+    cfg = cfg.with_(max_vram_bytes=3 * S, resident_layers=1)
+    hs = synth.HostStack(cfg)
+    rng = np.random.default_rng(seed)
+    eb = S // cfg.n_experts
+    exact = sum(t.nbytes for t in synth.segment_tensors(cfg))
+    ctx, _ = make_ctx(cfg, hs)
+    outs, load = [], []
+    try:
+        x = x_dev(cfg)
+        for _ in range(10):
+            lg = rng.standard_normal((cfg.n_segments, cfg.tokens, cfg.n_experts)).astype(np.float32)
+            if rng.random() < 0.4:
+                lg[..., :3] += 4.0                      # most tokens pick the same few experts
+            T = int(rng.choice([1, 5, 50, cfg.tokens]))
+            lg_t = torch.from_numpy(np.ascontiguousarray(lg[:, :T]))
+            xin = x[:T].contiguous()
+            op = rng.choice(["run", "async", "host"])
+            if op == "host":
+                y = torch.empty(T, cfg.hidden, dtype=torch.bfloat16).pin_memory()
+                L.ls_run_host(ctx, xin.cpu().pin_memory(), y, T, lg_t.pin_memory(), cfg.top_k)
+            else:
+                y = torch.empty_like(xin)
+                (L.ls_run if op == "run" else L.ls_run_async)(ctx, xin, y, T, logits=lg_t.cuda(), top_k=cfg.top_k)
+            outs.append((T, y, lg))
+            load.append([exact if l < 1 else len(np.unique(F.route_topk(lg[l, :T], cfg.top_k)[0])) * eb
+                         for l in range(cfg.n_segments)])
+        L.ls_sync(ctx)
+        torch.cuda.synchronize()
+        for T, y, lg in outs:
+            ref = ostack.stack_forward(cfg, logits=list(lg))
+            assert rel_err(to_f64(y), ref[:T]) <= BOUND, T
+        sim, _ = _sim_events(cfg, hs, cfg.prefetch_depth, 1, cfg.max_vram_bytes, 1, len(outs), load=load)
+        assert L.ls_get_schedule(ctx) == [tuple(e) for e in sim.events]
+    finally:
+        L.ls_ctx_destroy(ctx)
+
+
 @pytest.mark.parametrize("copy_path", [2, 1])
 @pytest.mark.parametrize("skewed", [True, False])
 def test_moe_expert_cache_matches_oracle_policy(copy_path, skewed):
