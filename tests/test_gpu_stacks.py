@@ -556,14 +556,16 @@ def test_replan_between_runs_keeps_the_bits(pool):
         L.ls_ctx_destroy(ctx)
 
 
-@pytest.mark.parametrize("seed,pool,cross", [(1, 1, False), (2, 0, False), (3, 1, True), (4, 0, True)])
-def test_random_sequences_of_passes_and_replans(seed, pool, cross):
+@pytest.mark.parametrize("seed,name,pool,cross", [(1, "ffn", 1, False), (2, "ffn", 0, False), (3, "ffn", 1, True),
+                                                   (4, "ffn", 0, True), (7, "proj", 1, False), (8, "proj", 0, True)])
+def test_random_sequences_of_passes_and_replans(seed, name, pool, cross):
     """Seeded random sequences on one context: passes of random token counts through ls_run,
     ls_run_async (synchronised before the next plan change) and ls_run_host, and plan changes
     of depth, residency and budget in between. Every output matches the oracle's first T rows,
     full-length passes keep the all-resident bits, and the executed schedule is the
-    simulator's for the same script."""
-    cfg = SMALL["ffn"]
+    simulator's for the same script. The shared-projection stack adds its deduplicated shared
+    parameter, loaded once and kept across plan changes."""
+    cfg = SMALL[name]
     hs = synth.HostStack(cfg)
     S = synth.segment_slot_bytes(cfg)
     ref_bits, _, _, _, _ = _run(cfg, hs, runs=1, max_vram_bytes=0)
