@@ -981,11 +981,17 @@ __global__ void __launch_bounds__(s2_threads(EPI), 1) gemm_bf16_tc2(const __grid
         int sb = 0;
         // Chunk output: v (row per lane) goes into the swizzled staging tiles and out by
         // bulk tensor stores. The caller has made sure the staging tiles are free.
-        auto store_chunk = [&](float (&v)[32], int n0, int row0) {
-            // ONE: the fp32 tile in the stage memory (the cluster's one tile is its last)
-            const uint32_t s32 = ONE ? base + (uint32_t)(warp - 2) * S2_STG_F32
-                                     : stg + NBUF * S2_STG_BF + (uint32_t)sb * S2_STG_F32;
-            const uint32_t sbf = stg + (uint32_t)sb * S2_STG_BF;
+        // ONE: the cluster's one tile is its last, so all of the stage memory is free for its
+        // epilogue: each warp gets ONE_NS pairs of fp32 and bf16 staging tiles there (one per
+        // chunk where they fit), and a chunk waits only for the stores of the chunk ONE_NS before
+        constexpr int ONE_SLOT = S2_STG_F32 + S2_STG_BF;
+        constexpr int ONE_FIT = S2_STAGES * S2_STAGE / (EW * ONE_SLOT);
+        constexpr int ONE_NS = ONE_FIT < PER_WARP ? ONE_FIT : PER_WARP;
+        static_assert(!ONE || ONE_NS >= 1, "one-tile staging in the stage memory");
+        auto store_chunk = [&](float (&v)[32], int n0, int row0, int slot) {
+            const uint32_t one_slot = base + (uint32_t)(((warp - 2) * ONE_NS + slot) * ONE_SLOT);
+            const uint32_t s32 = ONE ? one_slot : stg + NBUF * S2_STG_BF + (uint32_t)sb * S2_STG_F32;
+            const uint32_t sbf = ONE ? one_slot + S2_STG_F32 : stg + (uint32_t)sb * S2_STG_BF;
             // 64-byte swizzle: 16-byte unit j of row r sits at unit j ^ ((r >> 1) & 3)
 #pragma unroll
             for (int j = 0; j < 4; ++j)
@@ -1063,9 +1069,12 @@ __global__ void __launch_bounds__(s2_threads(EPI), 1) gemm_bf16_tc2(const __grid
                         if (EPI == EPI_BIAS_RESID) add_bias_row(p, n0, v);
 #pragma unroll
                         for (int j = 0; j < 32; ++j) v[j] += __uint_as_float(rr[j]);
-                        if (lane == 0) bulk_wait_read<0>();  // the previous chunk's stores have left the staging tiles
-                        __syncwarp();
-                        store_chunk(v, n0, row0);
+                        if (!ONE || i >= ONE_NS) {
+                            // the stores that last used these staging tiles have read them
+                            if (lane == 0) bulk_wait_read<ONE ? ONE_NS - 1 : 0>();
+                            __syncwarp();
+                        }
+                        store_chunk(v, n0, row0, ONE ? i % ONE_NS : 0);
                     }
                 }
                 release(buf);
@@ -1117,7 +1126,7 @@ __global__ void __launch_bounds__(s2_threads(EPI), 1) gemm_bf16_tc2(const __grid
                         if (lane == 0) bulk_wait_read<NBUF - 1>();
                         __syncwarp();
                     }
-                    store_chunk(v, n0, row0);
+                    store_chunk(v, n0, row0, 0);
                 }
                 if (OUT32 && i + 2 < n_chunks) issue(row0, n0 + 64, g[i & 1]);
             }
