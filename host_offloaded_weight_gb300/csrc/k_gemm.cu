@@ -657,15 +657,15 @@ constexpr int S2_STG_F32 = 32 * 32 * 4;        // 32x32 fp32 output staging tile
 // lane quarter, 96 registers) so that more warps hide each other's latencies; every
 // epilogue warp single-buffers its staging tiles. The mainloop takes as many stages
 // as the rest of shared memory holds (at most 8). ONE (residual epilogues where every
-// CTA pair has at most one tile): that tile is the pair's last, so its fp32 chunks are
-// staged in the mainloop's stage memory, free once its MMAs are done, and only the
-// bf16 staging tiles take room from the stages.
+// CTA pair has at most one tile): that tile is the pair's last, so its fp32 and bf16
+// chunks are staged in the mainloop's stage memory, free once its MMAs are done, and
+// no staging tile takes room from the stages.
 __host__ __device__ constexpr bool s2_out_f32(int epi) { return epi == EPI_BIAS_RESID || epi == EPI_RESID; }
 __host__ __device__ constexpr int s2_nbuf(int) { return 1; }
 __host__ __device__ constexpr int s2_epi_warps(int epi) { return s2_out_f32(epi) ? 8 : 16; }
 __host__ __device__ constexpr int s2_threads(int epi) { return 64 + 32 * s2_epi_warps(epi); }
 __host__ __device__ constexpr int s2_warp_bytes(int epi, bool one = false) {
-    return s2_nbuf(epi) * (S2_STG_BF + (s2_out_f32(epi) && !one ? S2_STG_F32 : 0));
+    return one ? 0 : s2_nbuf(epi) * (S2_STG_BF + (s2_out_f32(epi) ? S2_STG_F32 : 0));
 }
 __host__ __device__ constexpr int s2_stages(int epi, int bn, bool one = false) {
     return (232448 - 1024 - 256 - s2_epi_warps(epi) * s2_warp_bytes(epi, one)) / s2_stage_bytes(bn) < 8
@@ -675,7 +675,7 @@ __host__ __device__ constexpr int s2_stages(int epi, int bn, bool one = false) {
 __host__ __device__ constexpr int s2_smem_bytes(int epi, int bn, bool one = false) {
     return s2_stages(epi, bn, one) * s2_stage_bytes(bn) + s2_epi_warps(epi) * s2_warp_bytes(epi, one) + 1024 + 256;
 }
-static_assert(s2_stages(EPI_BIAS_RESID, 256, true) == 6 && s2_stages(EPI_RESID, 160, true) == 8 &&
+static_assert(s2_stages(EPI_BIAS_RESID, 256, true) == 7 && s2_stages(EPI_RESID, 160, true) == 8 &&
                   8 * S2_STG_F32 <= s2_stages(EPI_RESID, 160, true) * s2_stage_bytes(160),
               "one-tile residual layout: the fp32 staging fits in the stage memory");
 static_assert(s2_stages(EPI_BIAS_RESID, 256) == 5 && s2_stages(EPI_STORE, 256) == 6, "stages at BN = 256");
