@@ -664,7 +664,8 @@ def run_ours(args, cfg, world, rank, local):
         "config": {"workload": cfg.name, "tokens": T, "segments": cfg.n_segments, "hidden": cfg.hidden,
                    "ffn": cfg.ffn, "prefetch_depth": cfg.prefetch_depth, "resident_layers": cfg.resident_layers,
                    "max_vram_bytes": cfg.max_vram_bytes, "pool": cfg.use_pool,
-                   "copy_path": ["auto", "kernel", "engine"][stats["copy_path"]],
+                   "copy_path": ["per segment", "kernel", "engine"][stats["copy_path"]],
+                   "kernel_copy_segments": stats["kernel_copy_segments"],
                    "plan": {"residents": stats["residents"], "depth": stats["depth"],
                             "pool_slots": stats["pool_slots"], "slot_bytes": stats["slot_bytes"],
                             "warnings": stats["warnings"]},

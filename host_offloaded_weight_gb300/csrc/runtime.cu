@@ -54,6 +54,7 @@ struct SegRec {
     int64_t slot_bytes = 0;     // aligned private footprint
     int64_t load_bytes = 0;     // exact private bytes
     bool kernel_ok = true;      // all sources 16-byte aligned
+    bool use_kernel = false;    // this segment's loads go through the copy kernel
     CopyRange* ranges_dev = nullptr;
     int n_ranges = 0;
     int64_t n_chunks = 0;
@@ -100,7 +101,8 @@ struct ls_ctx {
     cudaEvent_t alloc_event = nullptr;
     cudaEvent_t run_done = nullptr;          // end of the last queued pass
     std::vector<cudaStream_t> pending;       // streams with queued passes
-    int copy_path = LS_COPY_ENGINE;
+    int copy_path = LS_COPY_ENGINE;          // summary: ENGINE, KERNEL, or AUTO when segments differ
+    int kernel_copy_segments = 0;            // segments whose loads go through the copy kernel
     int copy_ctas = 0;
     int reserve_sms = 0;
     double gbs_kernel = 0, gbs_engine = 0;
@@ -416,7 +418,7 @@ void compute_segment(ls_ctx* c, const RunCtx& rc, int seg, bool wait) {
         // the GEMM behind it may be placed early only if nothing on the copy stream needs an
         // SM (no copy or publish kernel that the placed CTAs could starve; device-to-device
         // copies of the expert cache may run as kernels too)
-        const bool early = c->copy_path == LS_COPY_ENGINE && publish_needs_no_sm() &&
+        const bool early = c->kernel_copy_segments == 0 && publish_needs_no_sm() &&
                            (!c->capturing || c->capture_stream_ops) && c->ecache_K == 0 && pdl;
         track(c, launch_wait_ready(c->ready + slot, epoch, rc.wait_ns, c->err_word_dev, code, rc.s, early));
         open_span();
@@ -623,7 +625,7 @@ struct GpuExec : Executor {
         const uint8_t* mask = c->kind == LS_KIND_MOE_SWIGLU_BF16 && kind != LS_EV_LOAD_RESIDENT
                                   ? c->moe_used_host_dev + (int64_t)seg * c->E
                                   : nullptr;
-        const bool kern = c->copy_path == LS_COPY_KERNEL;
+        const bool kern = c->segs[seg].use_kernel;
         if (kind == LS_EV_PREFETCH) {
             track(c, cudaStreamWaitEvent(c->copy_stream, c->slot_free[slot], 0));
             if (!c->prm.use_pool) {  // the buffer was allocated in compute-stream order
@@ -694,7 +696,7 @@ ls_status check_params(const ls_params* p, ls_params* out, std::string* why) {
     }
     if (d.copy_path < LS_COPY_AUTO || d.copy_path > LS_COPY_ENGINE) { *why = "bad copy_path"; return LS_ERR_INVALID_ARG; }
     if (d.copy_ctas < 0 || d.test_alloc_cap_bytes < 0 || d.test_drop_publish < 0 || d.kernel_timing < 0 ||
-        d.kernel_timing > 3) {
+        d.kernel_timing > 3 || d.test_kernel_copy_stride < 0) {
         *why = "negative count";
         return LS_ERR_INVALID_ARG;
     }
@@ -860,63 +862,103 @@ ls_status build_ranges(ls_ctx* c, SegRec& sr) {
     return LS_OK;
 }
 
-// Time both copy paths on one segment's load (copy stream, into the first slot or a scratch buffer).
+// The copy path of every segment's loads. A forced path applies to every segment (the copy
+// kernel only where the segment's sources are 16-byte aligned). AUTO times both paths on
+// each segment's own load, once each after an untimed warm-up of both (copy stream, into the
+// first slot or a scratch buffer): how fast the copy engine reads pinned host memory differs
+// between regions of the same host buffer. On GB300 hosts whose memory had been through large
+// allocate-and-free cycles, the copy engine read the first ~14 GB of a 58 GB stack at a third
+// to a tenth of the link rate while the copy kernel's loads read the same pages at the full
+// rate, so one segment's timing does not speak for the others.
 ls_status autotune_copy(ls_ctx* c) {
     const Plan& p = c->sched.plan();
-    const int M = p.N - p.R;
+    const int N = p.N;
     const int forced = c->prm.copy_path;
-    const int seg = p.N - 1;
-    if (M <= 0 || !c->segs[seg].kernel_ok) {  // nothing streamed, or sources not 16-byte aligned
-        c->copy_path = (forced == LS_COPY_KERNEL && c->segs[seg].kernel_ok) ? LS_COPY_KERNEL : LS_COPY_ENGINE;
+    auto summarize = [&]() {
+        c->kernel_copy_segments = 0;
+        for (int i = 0; i < N; ++i) c->kernel_copy_segments += c->segs[i].use_kernel ? 1 : 0;
+        c->copy_path = c->kernel_copy_segments == 0   ? LS_COPY_ENGINE
+                       : c->kernel_copy_segments == N ? LS_COPY_KERNEL
+                                                      : LS_COPY_AUTO;
+    };
+    if (forced != LS_COPY_AUTO || p.N - p.R <= 0) {  // forced, or nothing streamed
+        for (int i = 0; i < N; ++i) c->segs[i].use_kernel = forced == LS_COPY_KERNEL && c->segs[i].kernel_ok;
+        summarize();
         return LS_OK;
     }
+    if (c->prm.test_kernel_copy_stride > 0) {  // test hook: a fixed mix of the two paths
+        for (int i = 0; i < N; ++i)
+            c->segs[i].use_kernel = i % c->prm.test_kernel_copy_stride == 0 && c->segs[i].kernel_ok;
+        summarize();
+        return LS_OK;
+    }
+    int64_t max_slot = 0;
+    for (int i = 0; i < N; ++i) max_slot = std::max(max_slot, c->segs[i].slot_bytes);
     void* dst = c->pool;
     void* scratch = nullptr;
     if (!dst) {
-        CK(cudaMalloc(&scratch, (size_t)c->segs[seg].slot_bytes));
+        CK(cudaMalloc(&scratch, (size_t)max_slot));
         dst = scratch;
     }
     if (c->kind == LS_KIND_MOE_SWIGLU_BF16) {  // time with every expert routed
-        CK(cudaMemset(c->moe_used + (int64_t)seg * c->E, 1, c->E));
-        memset(c->moe_used_host + (int64_t)seg * c->E, 1, c->E);
+        CK(cudaMemset(c->moe_used, 1, (size_t)N * c->E));
+        memset(c->moe_used_host, 1, (size_t)N * c->E);
     }
     cudaEvent_t e0, e1;
     CK(cudaEventCreate(&e0));
     CK(cudaEventCreate(&e1));
-    const uint8_t* mask = c->kind == LS_KIND_MOE_SWIGLU_BF16 ? c->moe_used + (int64_t)seg * c->E : nullptr;
-    double best[2] = {1e30, 1e30};
     const int saved_drop = c->prm.test_drop_publish;
     const int saved_timing = c->prm.kernel_timing;
     c->prm.test_drop_publish = 0;
     c->prm.kernel_timing = 0;
-    for (int path = 0; path < 2; ++path) {
-        for (int rep = 0; rep < 4; ++rep) {
-            CK(cudaEventRecord(e0, c->copy_stream));
-            issue_copy(c, seg, dst, 0, 0x80000000u + rep, c->copy_stream, path == 0, mask);
-            CK(cudaEventRecord(e1, c->copy_stream));
-            CK(cudaEventSynchronize(e1));
-            float ms = 0;
-            CK(cudaEventElapsedTime(&ms, e0, e1));
-            if (rep > 0) best[path] = std::min(best[path], (double)ms);
-        }
+    uint32_t epoch = 0x80000000u;
+    auto time_load = [&](int seg, bool kern, float* ms) -> ls_status {
+        const uint8_t* mask = c->kind == LS_KIND_MOE_SWIGLU_BF16 ? c->moe_used + (int64_t)seg * c->E : nullptr;
+        CK(cudaEventRecord(e0, c->copy_stream));
+        issue_copy(c, seg, dst, 0, epoch++, c->copy_stream, kern, mask);
+        CK(cudaEventRecord(e1, c->copy_stream));
+        CK(cudaEventSynchronize(e1));
+        CK(c->cuda_err);
+        CK(cudaEventElapsedTime(ms, e0, e1));
+        return LS_OK;
+    };
+    // The copy kernel occupies SM issue slots and registers next to the segment's GEMMs
+    // while the copy engine uses none, so a segment takes the kernel only when it is
+    // clearly faster on that segment's load (by more than KERNEL_MARGIN).
+    constexpr double KERNEL_MARGIN = 1.15;
+    double bytes_k = 0, bytes_e = 0, ms_k = 0, ms_e = 0;
+    float ms = 0;
+    ls_status st = LS_OK;
+    for (int kern = 0; kern < 2 && st == LS_OK; ++kern)  // warm-up of both paths
+        if (!kern || c->segs[N - 1].kernel_ok) st = time_load(N - 1, kern != 0, &ms);
+    for (int seg = 0; seg < N && st == LS_OK; ++seg) {
+        SegRec& sr = c->segs[seg];
+        sr.use_kernel = false;
+        if (sr.load_bytes == 0) continue;
+        float me = 0, mk = 0;
+        if ((st = time_load(seg, false, &me)) != LS_OK) break;
+        bytes_e += (double)sr.load_bytes;
+        ms_e += me;
+        if (!sr.kernel_ok) continue;
+        if ((st = time_load(seg, true, &mk)) != LS_OK) break;
+        bytes_k += (double)sr.load_bytes;
+        ms_k += mk;
+        sr.use_kernel = (double)mk * KERNEL_MARGIN < (double)me;
     }
     c->prm.test_drop_publish = saved_drop;
     c->prm.kernel_timing = saved_timing;
-    CK(c->cuda_err);
-    CK(cudaMemsetAsync(c->ready, 0, sizeof(uint32_t) * std::max(1, p.P), c->copy_stream));
-    CK(cudaStreamSynchronize(c->copy_stream));
     cudaEventDestroy(e0);
     cudaEventDestroy(e1);
+    if (st != LS_OK) {
+        if (scratch) cudaFree(scratch);
+        return st;
+    }
+    CK(cudaMemsetAsync(c->ready, 0, sizeof(uint32_t) * std::max(1, p.P), c->copy_stream));
+    CK(cudaStreamSynchronize(c->copy_stream));
     if (scratch) cudaFree(scratch);
-    const double bytes = (double)c->segs[seg].load_bytes;
-    c->gbs_kernel = bytes / (best[0] * 1e-3) / 1e9;
-    c->gbs_engine = bytes / (best[1] * 1e-3) / 1e9;
-    // The copy kernel occupies SM issue slots and registers next to the segment's GEMMs
-    // while the copy engine uses none, so AUTO keeps the kernel only when it is
-    // clearly faster on its own (by more than KERNEL_MARGIN).
-    constexpr double KERNEL_MARGIN = 1.15;
-    c->copy_path = forced != LS_COPY_AUTO ? forced
-                                          : (best[0] * KERNEL_MARGIN < best[1] ? LS_COPY_KERNEL : LS_COPY_ENGINE);
+    c->gbs_kernel = ms_k > 0 ? bytes_k / (ms_k * 1e-3) / 1e9 : 0;
+    c->gbs_engine = ms_e > 0 ? bytes_e / (ms_e * 1e-3) / 1e9 : 0;
+    summarize();
     return LS_OK;
 }
 
@@ -1699,6 +1741,7 @@ ls_status ls_get_stats(ls_ctx* c, ls_stats* out) {
     s.struct_size = sizeof(s);
     if (c->registered || c->sched.plan().N > 0) c->sched.fill_stats(s);
     s.copy_path = c->copy_path;
+    s.kernel_copy_segments = c->kernel_copy_segments;
     s.copy_kernel_gbs = c->gbs_kernel;
     s.copy_engine_gbs = c->gbs_engine;
     s.graph_captures = c->graph_captures;

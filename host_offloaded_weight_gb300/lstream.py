@@ -45,7 +45,8 @@ class ls_params(C.Structure):
                 ("test_alloc_cap_bytes", C.c_int64), ("test_fail_async", C.c_int32),
                 ("test_drop_publish", C.c_int32), ("kernel_timing", C.c_int32),
                 ("cross_run_prefetch", C.c_int32), ("expert_cache_bytes", C.c_int64),
-                ("debug_checks", C.c_int32), ("test_corrupt_canary", C.c_int32)]
+                ("debug_checks", C.c_int32), ("test_corrupt_canary", C.c_int32),
+                ("test_kernel_copy_stride", C.c_int32)]
 
 
 class ls_tensor_desc(C.Structure):
@@ -93,7 +94,8 @@ class ls_stats(C.Structure):
                 ("bytes_loaded", C.c_int64), ("copy_kernel_gbs", C.c_double),
                 ("copy_engine_gbs", C.c_double), ("graph_captures", C.c_int64),
                 ("graph_replays", C.c_int64), ("expert_cache_hits", C.c_int64),
-                ("expert_host_loads", C.c_int64), ("debug_violations", C.c_int64)]
+                ("expert_host_loads", C.c_int64), ("debug_violations", C.c_int64),
+                ("kernel_copy_segments", C.c_int64)]
 
 
 _P = C.c_void_p

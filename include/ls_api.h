@@ -107,7 +107,8 @@ typedef struct ls_params {
     int32_t use_pool;          /* 1 = one contiguous slot pool; 0 (default) = one allocation per load */
     /* ---- end of the minimum struct ---- */
     int32_t wait_limit_ms;     /* bound of every device-side wait, 1..600000; default 30000 */
-    int32_t copy_path;         /* LS_COPY_AUTO (default: timed per size at registration), _KERNEL, _ENGINE */
+    int32_t copy_path;         /* LS_COPY_AUTO (default: both paths timed on each segment's load at
+                                  registration, chosen per segment), _KERNEL, _ENGINE (every segment) */
     int32_t copy_ctas;         /* CTAs of the copy kernel; 0 = default */
     int32_t reserve_sms;       /* SMs the GEMMs leave free while a copy kernel runs; -1 = default */
     int32_t device;            /* CUDA device ordinal; -1 (default) = the current device */
@@ -149,6 +150,9 @@ typedef struct ls_params {
                                      0 (default) = off */
     int32_t test_corrupt_canary;  /* test hook (debug_checks only): N > 0 overwrites the canary of pool slot
                                      N - 1 once, right after registration */
+    int32_t test_kernel_copy_stride; /* test hook (copy_path AUTO only): N > 0 skips the timing and puts the
+                                     loads of the segments whose index is a multiple of N on the copy
+                                     kernel, the others on the copy engine */
 } ls_params;
 
 /* One tensor of a segment: host memory owned by the caller, kept alive and
@@ -203,7 +207,8 @@ typedef struct ls_stats {
     int32_t ring_slots;        /* Q: slots cycling through streamed segments */
     int32_t pool_slots;        /* P = R + Q (planned) */
     int32_t warnings;          /* bit (1 << w) for each warning w raised so far */
-    int32_t copy_path;         /* LS_COPY_KERNEL or LS_COPY_ENGINE as chosen */
+    int32_t copy_path;         /* LS_COPY_KERNEL or LS_COPY_ENGINE when every segment's loads take that
+                                  path; LS_COPY_AUTO when the segments differ (kernel_copy_segments) */
     int64_t slot_bytes;        /* S */
     int64_t shared_bytes;
     int64_t pool_bytes;        /* bytes of the pool allocation (0 with the pool off) */
@@ -217,13 +222,14 @@ typedef struct ls_stats {
     int64_t sync_fallbacks;
     int64_t pool_degradations;
     int64_t bytes_loaded;
-    double copy_kernel_gbs;    /* registration-time timing of both copy paths (0 if not timed) */
+    double copy_kernel_gbs;    /* registration-time timing of both copy paths over the segments' loads (0 if not timed) */
     double copy_engine_gbs;
     int64_t graph_captures;    /* passes captured into a CUDA graph by ls_run_graph */
     int64_t graph_replays;     /* passes issued as a replay of the captured graph */
     int64_t expert_cache_hits; /* routed experts of streamed layers served from the expert cache */
     int64_t expert_host_loads; /* routed experts of streamed layers copied from the host */
     int64_t debug_violations;  /* runs failed by params.debug_checks */
+    int64_t kernel_copy_segments; /* segments whose loads go through the copy kernel */
 } ls_stats;
 
 /* Per-kernel timing, accumulated over runs while params.kernel_timing is on.

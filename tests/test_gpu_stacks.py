@@ -104,6 +104,71 @@ def test_copy_paths_agree(path):
     assert np.array_equal(_bits(y), _bits(y2))
 
 
+@pytest.mark.parametrize("name,depth,pool,stride,graph", [("ffn", 1, 1, 2, False), ("ffn", 2, 0, 3, False),
+                                                          ("proj", 1, 1, 2, True), ("swiglu", 2, 1, 2, False),
+                                                          ("swiglu", 0, 1, 2, False)])
+def test_mixed_copy_paths_keep_bits_and_schedule(name, depth, pool, stride, graph):
+    """Segments whose loads take different copy paths (every stride-th segment on the copy
+    kernel, the others on the copy engine, as the per-segment timing may choose): the bits of
+    every load on the copy engine, and the simulator's schedule."""
+    cfg = SMALL[name]
+    hs = synth.HostStack(cfg)
+    S = synth.segment_slot_bytes(cfg)
+    shared_b = sum(synth.align256(v.nbytes) for v in hs.shared_views)
+    kw = dict(prefetch_depth=depth, resident_layers=0, max_vram_bytes=shared_b + (depth + 1) * S, use_pool=pool)
+    ref, ev_ref, *_ = _run(cfg, hs, runs=3, copy_path=L.LS_COPY_ENGINE, **kw)
+    ctx, _ = make_ctx(cfg, hs, copy_path=L.LS_COPY_AUTO, test_kernel_copy_stride=stride, **kw)
+    try:
+        st = L.ls_get_stats(ctx)
+        n_kernel = len(range(0, cfg.n_segments, stride))
+        assert st["kernel_copy_segments"] == n_kernel and st["copy_path"] == L.LS_COPY_AUTO
+        x = x_dev(cfg)
+        y = torch.empty_like(x)
+        for _ in range(3):
+            if graph:
+                L.ls_run_graph(ctx, x, y, cfg.tokens)
+                L.ls_sync(ctx)
+            else:
+                L.ls_run(ctx, x, y, cfg.tokens)
+            torch.cuda.synchronize()
+            assert np.array_equal(_bits(y), _bits(ref))
+        assert L.ls_get_schedule(ctx) == ev_ref
+    finally:
+        L.ls_ctx_destroy(ctx)
+
+
+def test_auto_copy_path_is_chosen_per_segment():
+    """AUTO times both paths on every segment's own load: the summary agrees with the
+    per-segment count, both rates are measured, and the bits are those of either forced path."""
+    cfg = SMALL["swiglu"]
+    hs = synth.HostStack(cfg)
+    S = synth.segment_slot_bytes(cfg)
+    kw = dict(prefetch_depth=1, resident_layers=0, max_vram_bytes=2 * S, use_pool=1)
+    y, _, st, *_ = _run(cfg, hs, runs=2, copy_path=L.LS_COPY_AUTO, **kw)
+    k = st["kernel_copy_segments"]
+    assert 0 <= k <= cfg.n_segments
+    assert st["copy_path"] == (L.LS_COPY_ENGINE if k == 0 else L.LS_COPY_KERNEL if k == cfg.n_segments
+                               else L.LS_COPY_AUTO)
+    assert st["copy_kernel_gbs"] > 0 and st["copy_engine_gbs"] > 0
+    for path in (L.LS_COPY_KERNEL, L.LS_COPY_ENGINE):
+        y2, _, st2, *_ = _run(cfg, hs, runs=2, copy_path=path, **kw)
+        assert st2["kernel_copy_segments"] == (cfg.n_segments if path == L.LS_COPY_KERNEL else 0)
+        assert np.array_equal(_bits(y), _bits(y2))
+
+
+def test_moe_mixed_copy_paths_keep_bits():
+    """The MoE stack with every second layer's routed experts moved by the copy kernel and the
+    rest by the copy engine: the bits of the all-engine run and its schedule (bytes of the
+    routed experts only)."""
+    cfg = _moe_cfg(4, 200, experts=16, hidden=128, ffn=64, k=4)
+    hs = synth.HostStack(cfg)
+    lg_dev, _ = logits_dev(cfg)
+    ref, ev_ref, *_ = _run(cfg, hs, logits=lg_dev, runs=2, copy_path=L.LS_COPY_ENGINE)
+    y, ev, st, *_ = _run(cfg, hs, logits=lg_dev, runs=2, copy_path=L.LS_COPY_AUTO, test_kernel_copy_stride=2)
+    assert st["kernel_copy_segments"] == 2
+    assert np.array_equal(_bits(y), _bits(ref)) and ev == ev_ref
+
+
 # ------------------------------------------------------------------ full-size stacks, sampled rows
 def _rows(cfg, n=48):
     return np.sort(np.random.default_rng(1).choice(cfg.tokens, n, replace=False))
