@@ -931,6 +931,10 @@ ls_status autotune_copy(ls_ctx* c) {
     ls_status st = LS_OK;
     for (int kern = 0; kern < 2 && st == LS_OK; ++kern)  // warm-up of both paths
         if (!kern || c->segs[N - 1].kernel_ok) st = time_load(N - 1, kern != 0, &ms);
+    // One reading per path and segment, in segment order as a pass reads them: the engine's
+    // reading of a segment comes after the other segments' loads. A second engine reading of
+    // the same segment right after its first was fast for host regions that the engine read
+    // slowly in every pass, so it is not taken.
     for (int seg = 0; seg < N && st == LS_OK; ++seg) {
         SegRec& sr = c->segs[seg];
         sr.use_kernel = false;
