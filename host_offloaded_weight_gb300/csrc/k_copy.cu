@@ -170,6 +170,19 @@ cudaError_t launch_publish(uint32_t* ready, uint32_t epoch, bool publish, cudaSt
     return cudaGetLastError();
 }
 
+// An SM's shared-memory carveout stays as it is while any CTA is resident. A copy or wait CTA
+// placed under the default carveout kept GEMM CTAs (~230 KB of shared memory each) off its SM
+// until it ended: in a MoE pass, a layer's GEMMs then waited out the whole next copy (5.7 ms
+// instead of 0.3) whenever the copy kernel reached the SMs first. Neither kernel uses shared
+// memory, so both ask for the largest carveout, under which a GEMM CTA fits beside them.
+void prepare_copy_kernels() {
+    cudaFuncSetAttribute(copy_h2slot_kernel, cudaFuncAttributePreferredSharedMemoryCarveout,
+                         (int)cudaSharedmemCarveoutMaxShared);
+    cudaFuncSetAttribute(wait_ready_kernel, cudaFuncAttributePreferredSharedMemoryCarveout,
+                         (int)cudaSharedmemCarveoutMaxShared);
+    cudaGetLastError();
+}
+
 cudaError_t launch_wait_ready(const uint32_t* ready, uint32_t epoch, uint64_t limit_ns,
                               uint32_t* err_word, uint32_t code, cudaStream_t s, bool early_dependents) {
     wait_ready_kernel<<<1, 32, 0, s>>>(ready, epoch, limit_ns, err_word, code, early_dependents ? 1 : 0);

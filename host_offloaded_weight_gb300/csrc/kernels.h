@@ -27,6 +27,9 @@ cudaError_t launch_wait_ready(const uint32_t* ready, uint32_t epoch, uint64_t li
                               uint32_t* err_word, uint32_t code, cudaStream_t s, bool early_dependents = false);
 // True when a publish after a copy-engine load is a stream memory operation (no SM).
 bool publish_needs_no_sm();
+// Asks, on the current device, for the largest shared-memory carveout for the copy and wait
+// kernels (called once per context, outside any stream capture; a hint, errors ignored).
+void prepare_copy_kernels();
 
 // ---------------------------------------------------------------- fp32 linear + GELU
 cudaError_t launch_linear_gelu_f32(const float* x, const float* w, const float* b, float* y, int T,

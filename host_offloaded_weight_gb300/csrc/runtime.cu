@@ -1193,6 +1193,7 @@ static ls_status register_impl(ls_ctx* c, const ls_segment_desc* segs, int32_t n
         if (st != LS_OK) return st;
     }
     // streams, words, events
+    prepare_copy_kernels();
     CK(cudaStreamCreateWithFlags(&c->copy_stream, cudaStreamNonBlocking));
     CK(cudaEventCreateWithFlags(&c->alloc_event, cudaEventDisableTiming));
     CK(cudaEventCreateWithFlags(&c->run_done, cudaEventDisableTiming));
