@@ -70,6 +70,33 @@ def test_caller_built_against_the_shorter_struct():
         os.remove(exe)
 
 
+STRUCTS = ("ls_params", "ls_tensor_desc", "ls_segment_desc", "ls_shared_ref", "ls_moe_routing",
+           "ls_kernel_time", "ls_trace_event", "ls_sched_event", "ls_stats")
+
+
+def test_binding_structs_match_the_header_layout(tmp_path):
+    """Every struct the binding declares has the header's size and field offsets, as a C
+    compiler lays them out (a field added to one side only shows up here)."""
+    lines = ["#include <stdio.h>", "#include <stddef.h>", '#include "ls_api.h"', "int main(void) {"]
+    for name in STRUCTS:
+        cls = getattr(L, name)
+        lines.append(f'    printf("{name} size %zu\\n", sizeof({name}));')
+        for field, _ in cls._fields_:
+            lines.append(f'    printf("{name} {field} %zu\\n", offsetof({name}, {field}));')
+    lines += ["    return 0;", "}"]
+    src = tmp_path / "layout.c"
+    src.write_text("\n".join(lines) + "\n")
+    exe = tmp_path / "layout"
+    subprocess.run(["gcc", "-O0", "-I", INCLUDE, "-o", str(exe), str(src)], check=True)
+    out = subprocess.run([str(exe)], capture_output=True, text=True, check=True, timeout=60).stdout
+    c_layout = {tuple(ln.split()[:2]): int(ln.split()[2]) for ln in out.splitlines()}
+    for name in STRUCTS:
+        cls = getattr(L, name)
+        assert c_layout[(name, "size")] == ctypes.sizeof(cls), name
+        for field, _ in cls._fields_:
+            assert c_layout[(name, field)] == getattr(cls, field).offset, (name, field)
+
+
 def _native(seg, shared, depth, resident, budget, pool, runs, cap=None, fail_async=False, load=None):
     p = L.ls_params_init(prefetch_depth=depth, resident_layers=resident, max_vram_bytes=budget,
                          use_pool=pool, test_alloc_cap_bytes=cap or 0,
