@@ -937,12 +937,14 @@ def test_moe_random_sequences_of_routings_and_token_counts(seed):
         L.ls_ctx_destroy(ctx)
 
 
-@pytest.mark.parametrize("copy_path", [2, 1])
+@pytest.mark.parametrize("copy_path", [2, 1, "mixed"])
 @pytest.mark.parametrize("skewed", [True, False])
 def test_moe_expert_cache_matches_oracle_policy(copy_path, skewed):
     """Expert cache of the streamed layers: hot experts come from device memory, the
     schedule's load bytes are the oracle policy's host copies, and the bits equal a run
-    without the cache. Uniform routing makes most counts tie, which the tie rule decides."""
+    without the cache. Uniform routing makes most counts tie, which the tie rule decides.
+    "mixed": every second layer's host copies go through the copy kernel, the rest through
+    the copy engine."""
     from oracle import expert_cache, forward as F
     cfg = _moe_cfg(4, 64, experts=8, hidden=256, ffn=128, k=2)
     S = synth.segment_slot_bytes(cfg)
@@ -955,7 +957,9 @@ def test_moe_expert_cache_matches_oracle_policy(copy_path, skewed):
               for _ in range(5)]
     outs = {}
     for cache in (0, K * eb):
-        ctx, _ = make_ctx(cfg, hs, expert_cache_bytes=cache, copy_path=copy_path)
+        path = dict(copy_path=L.LS_COPY_AUTO, test_kernel_copy_stride=2) if copy_path == "mixed" \
+            else dict(copy_path=copy_path)
+        ctx, _ = make_ctx(cfg, hs, expert_cache_bytes=cache, **path)
         try:
             x = x_dev(cfg)
             ys = []
